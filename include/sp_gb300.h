@@ -1,0 +1,210 @@
+/*
+ * sp_gb300.h -- C ABI of the GB300 (sm_103a) blockwise-attention library.
+ *
+ * One data-parallel hot path, simulated on one GPU:
+ *
+ *   1. The Ulysses sequence-shard <-> head-shard redistribution, which on one
+ *      device is a layout permutation ("Ulysses SP: entrenar modelos con
+ *      millones de tokens", section "Cómo funciona Ulysses Sequence
+ *      Parallelism (SP)"; "DeepSpeed-Ulysses", section "Method":
+ *      (N/P, d) -> (N, d/P)).
+ *   2. Exact softmax attention computed blockwise over P key/value blocks in
+ *      ring order, partial results combined by the cumulative (online)
+ *      softmax ("Ring Attention", section "Cómo funciona la atención en
+ *      anillo"), with the causal mask derived from O(n) position_ids
+ *      ("Ulysses SPで100万トークン学習", section 3).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor argument is a DEVICE pointer to a dense, row-major
+ *   (C-contiguous) buffer owned by the caller.  The library never allocates,
+ *   frees or retains device memory, and keeps no pointer after returning.
+ * - All work is enqueued on `stream` (NULL = legacy default stream) and runs
+ *   asynchronously; the call returns once the kernels are launched.
+ * - Arguments are validated on the host BEFORE anything is launched; a
+ *   rejected call returns an SP_ERR_* status and enqueues nothing.
+ * - A CUDA error when configuring or launching a kernel returns SP_ERR_CUDA
+ *   (the CUDA error itself is left for cudaGetLastError()).
+ * - Outputs must not overlap inputs.
+ * - Sizes are element counts; B, S, H*, d, P must be >= 1 unless stated.
+ *
+ * Layouts (innermost dimension last):
+ *   sequence-sharded  x     [B][S][H][d]        (P shards = P slices of S)
+ *   head-sharded      y     [P][B][S][H/P][d]   (y[r] = what rank r holds)
+ *   q                       [B][S][Hq][d]
+ *   k, v                    [B][S][Hkv][d]      (GQA: q head h uses kv head
+ *                                                h / (Hq/Hkv))
+ *   position_ids            [B][S] int32
+ *   out                     [B][S][Hq][d]
+ *   lse                     [B][Hq][S] float32, natural log of
+ *                           sum_j exp(scale * q.k_j) over the allowed keys
+ */
+#ifndef SP_GB300_H
+#define SP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; declared here so that this header
+ * does not need the CUDA headers. */
+typedef struct CUstream_st* sp_stream_t;
+
+typedef enum sp_status {
+  SP_OK = 0,
+  SP_ERR_INVALID_ARG = 1,     /* bad pointer, size, divisibility or enum   */
+  SP_ERR_UNSUPPORTED = 2,     /* valid request this build cannot run        */
+  SP_ERR_WORKSPACE = 3,       /* workspace NULL/too small/misaligned        */
+  SP_ERR_CUDA = 4,            /* CUDA runtime/driver error at launch        */
+  SP_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up waiting on a barrier      */
+} sp_status;
+
+typedef enum sp_dtype {
+  SP_BF16 = 0,   /* bfloat16 storage; float32 accumulation                */
+  SP_F32 = 1     /* float32 storage and arithmetic                         */
+} sp_dtype;
+
+typedef enum sp_block_order {
+  /* block p = tokens [p*S/P, (p+1)*S/P): the sequence sharding of the
+   * Ulysses pages (GPU i holds tokens [i*n/P, (i+1)*n/P)). */
+  SP_ORDER_CONTIGUOUS = 0,
+  /* block p = tokens {t : t mod P == p}: Striped Attention ("Ring
+   * Attention", "Cómo funciona la atención en anillo": each device's tokens
+   * spread uniformly over the sequence; stripe width 1). */
+  SP_ORDER_STRIPED = 1
+} sp_block_order;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* sp_status_string(sp_status status);
+
+/* ------------------------------------------------------------------------
+ * Ulysses redistribution as a permutation (bit-exact copy).
+ *
+ * sp_ulysses_seq_to_head: y[r][b][t][hl][:] = x[b][t][r*(H/P) + hl][:]
+ *   x: [B][S][H][d], y: [P][B][S][H/P][d], element type `dtype`.
+ *   This is what the first all-to-all of a Ulysses attention layer delivers:
+ *   rank r ends up with every position of head group r (heads
+ *   r*H/P .. (r+1)*H/P - 1, contiguous groups).
+ * sp_ulysses_head_to_seq: the inverse (the second all-to-all):
+ *   x[b][t][r*(H/P) + hl][:] = y[r][b][t][hl][:].
+ *
+ * Errors: SP_ERR_INVALID_ARG if a pointer is NULL, a size < 1, S % P != 0
+ * (the pages require the sequence length to be divisible by sp_size) or
+ * H % P != 0 (Ulysses needs num_heads >= sp_size, in equal groups).
+ * ------------------------------------------------------------------------ */
+sp_status sp_ulysses_seq_to_head(const void* x, void* y, int B, int S, int H, int d, int P,
+                                 sp_dtype dtype, sp_stream_t stream);
+sp_status sp_ulysses_head_to_seq(const void* y, void* x, int B, int S, int H, int d, int P,
+                                 sp_dtype dtype, sp_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Document starts from position_ids (the O(n) causal-mask carrier,
+ * "Ulysses SPで100万トークン学習", section 3).
+ *
+ * A document starts at token 0 and at every t with
+ * position_ids[b][t] != position_ids[b][t-1] + 1.  doc_start[b][t] = the
+ * first token of t's document.  Query t may attend key j iff
+ * doc_start[b][t] <= j <= t, which is "same document and j <= t".
+ *
+ * position_ids: [B][S] int32 (device); doc_start: [B][S] int32 (device).
+ * workspace: device scratch of sp_segment_starts_workspace_bytes(B, S)
+ * bytes, 256-byte aligned.
+ * Errors: SP_ERR_INVALID_ARG (NULL pointer, size < 1),
+ * SP_ERR_WORKSPACE (workspace NULL, misaligned or too small).
+ * ------------------------------------------------------------------------ */
+size_t sp_segment_starts_workspace_bytes(int B, int S);
+sp_status sp_segment_starts(const int32_t* position_ids, int32_t* doc_start, int B, int S,
+                            void* workspace, size_t workspace_bytes, sp_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Blockwise (ring) attention, forward.
+ *
+ * The sequence is cut into P blocks (`order`).  For every query block i the
+ * key/value blocks are visited in ring order j = (i - s) mod P,
+ * s = 0 .. P-1 ("Ring Attention", "Cómo funciona la atención en anillo"),
+ * and merged by the online softmax: a running max m, a running sum of
+ * exponentiated scores l and a running weighted-value sum O, rescaled by
+ * exp(m_old - m_new) when the max grows and divided at the end.  The
+ * result is exact softmax attention (up to rounding):
+ *
+ *   out[b][t][h][:] = sum_{j allowed} softmax_j(scale * q[b][t][h] . k[b][j][h/g]) v[b][j][h/g][:]
+ *   lse[b][h][t]    = log sum_{j allowed} exp(scale * q[b][t][h] . k[b][j][h/g])
+ *
+ * with g = Hq / Hkv.  allowed(t, j): every j when position_ids == NULL;
+ * otherwise doc_start(t) <= j <= t (same document, causal), see
+ * sp_segment_starts.
+ *
+ * q [B][S][Hq][d], k/v [B][S][Hkv][d], out [B][S][Hq][d] in `dtype`;
+ * lse [B][Hq][S] float32 (may be NULL if not wanted).
+ * scale <= 0 selects 1/sqrt(d).
+ * Supported: SP_BF16 with d == 128 (tcgen05 tensor cores, fp32
+ * accumulation, P rounded to bf16 before the PV product, out rounded to
+ * nearest-even bf16); SP_F32 with 1 <= d <= 256 (fp32 FFMA throughout).
+ * A row with no allowed key (only possible with the step variant below)
+ * gets out = 0 and lse = -inf.
+ *
+ * workspace: device scratch of at least
+ * sp_blockwise_attn_workspace_bytes(B, S, position_ids != NULL) bytes,
+ * 256-byte aligned; it holds the device error word and the doc_start
+ * array.  Its contents need not be initialised.
+ *
+ * Errors: SP_ERR_INVALID_ARG (NULL q/k/v/out, size < 1, S % P != 0,
+ * Hq % Hkv != 0, bad order or dtype), SP_ERR_UNSUPPORTED (d outside the
+ * supported set), SP_ERR_WORKSPACE, SP_ERR_CUDA.  Device-side barrier
+ * timeouts (which do not occur in a correct run) are reported afterwards
+ * by sp_get_device_error.
+ * ------------------------------------------------------------------------ */
+size_t sp_blockwise_attn_workspace_bytes(int B, int S, int causal);
+sp_status sp_blockwise_attn_fwd(const void* q, const void* k, const void* v,
+                                const int32_t* position_ids, int B, int S, int Hq, int Hkv, int d,
+                                int P, sp_block_order order, float scale, sp_dtype dtype, void* out,
+                                float* lse, void* workspace, size_t workspace_bytes,
+                                sp_stream_t stream);
+
+/* One ring step only: every query block i attends key/value block
+ * j = (i - step) mod P and nothing else.  This is the partial result device
+ * i holds after ring step `step`; sp_attn_merge_partials over
+ * step = 0 .. P-1 reproduces sp_blockwise_attn_fwd.  Same arguments,
+ * layouts and errors as sp_blockwise_attn_fwd, plus 0 <= step < P.  Rows
+ * with no allowed key in that block get out = 0, lse = -inf. */
+sp_status sp_blockwise_attn_step(const void* q, const void* k, const void* v,
+                                 const int32_t* position_ids, int B, int S, int Hq, int Hkv, int d,
+                                 int P, sp_block_order order, int step, float scale, sp_dtype dtype,
+                                 void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                 sp_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Merge of per-block partial results (the cross-device combine of ring
+ * attention, "Ring Attention", "Cómo funciona la atención en anillo").
+ *
+ *   lse[b][h][t] = log sum_p exp(lses[p][b][h][t])
+ *   out[b][t][h][:] = sum_p exp(lses[p][b][h][t] - lse[b][h][t]) * outs[p][b][t][h][:]
+ *
+ * outs [P][B][S][H][d] in `dtype`, lses [P][B][H][S] float32 (device);
+ * out [B][S][H][d] in `dtype`, lse [B][H][S] float32 (may be NULL).
+ * A partial with lse = -inf has weight 0; if all are -inf, out = 0 and
+ * lse = -inf.  Arithmetic in float32; bf16 output rounded to nearest-even.
+ * Errors: SP_ERR_INVALID_ARG (NULL pointer, size < 1, bad dtype).
+ * ------------------------------------------------------------------------ */
+sp_status sp_attn_merge_partials(const void* outs, const float* lses, int P, int B, int S, int H,
+                                 int d, sp_dtype dtype, void* out, float* lse, sp_stream_t stream);
+
+/* Waits for `stream`, then reads the device error word that the attention
+ * kernels of the last calls using `workspace` left there (0 = no error;
+ * otherwise a barrier wait ran out of time and that kernel returned early,
+ * its output undefined).  Writes the raw word to *code when code != NULL and
+ * clears it.  Returns SP_OK, SP_ERR_DEVICE_TIMEOUT or SP_ERR_CUDA. */
+sp_status sp_get_device_error(void* workspace, int* code, sp_stream_t stream);
+
+/* Number of kernels the last successful call on this host thread enqueued
+ * (lets a caller count device launches without a profiler). */
+int sp_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SP_GB300_H */
