@@ -1,0 +1,507 @@
+"""Benchmark of the hot path: Ulysses permutation + blockwise ring attention.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one pass of the whole path over one batch of synthetic input.
+For the default workload (ulysses_4k: B=1, S=4096, H=32, d=128, P=4, bf16):
+    seq_to_head(q), seq_to_head(k), seq_to_head(v)      Ulysses all-to-all #1
+    blockwise attention, batch P*B, H/P heads, P ring blocks (online merge)
+    head_to_seq(out)                                     Ulysses all-to-all #2
+For the causal workloads (llama8b_32k, packed_128k, halfmil_512k) a step is
+doc_start from position_ids + causal blockwise attention.
+
+Reported value: attention TFLOP/s over the whole step (algorithmic FLOPs:
+4*d per allowed (query, key) pair per query head), aggregated over ranks.
+L2 (129 MB) is flushed between timed steps by writing a 512 MiB buffer,
+outside the timed events.  The JSON line also carries the dominant kernel's
+roofline, the permutation's bandwidth, the causal Llama-3.1-8B-shaped
+attention rate, an end-to-end number with host buffers, the CPU oracle
+baseline, and the SM clocks sampled during the timed region.
+
+Multi-GPU: every rank runs its own independent replica of the step (the
+head groups / batches of the path are independent; no collective on the data
+path), weak scaling; time = max over ranks.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("causal blockwise-attention TFLOP/s (% BF16 peak); seq↔head permute GB/s")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
+# kernel from the committed ncu capture (None until taken for this kernel).
+NCU_TRAFFIC_BYTES = {}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def attention_flops(cfg, pos):
+    """4*d FLOPs per allowed (query, key) pair per query head."""
+    B, S, Hq, d = cfg["B"], cfg["S"], cfg["Hq"], cfg["d"]
+    if cfg.get("ulysses"):
+        return 4.0 * d * S * S * Hq * B
+    if pos is None:
+        pairs = float(S) * S
+    else:
+        # pairs per document: L(L+1)/2 (position_ids restart per document)
+        pairs = 0.0
+        row = pos[0]
+        starts = np.flatnonzero(np.concatenate([[1], row[1:] != row[:-1] + 1]))
+        ends = np.concatenate([starts[1:], [S]])
+        for a, b in zip(starts, ends):
+            L = float(b - a)
+            pairs += L * (L + 1) / 2
+    return 4.0 * d * pairs * Hq * B
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import sequence_parallelism_gb300 as sp
+    from sequence_parallelism_gb300 import _lib, workloads
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = dict(workloads.CONFIGS[args.workload])
+    B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
+    order = cfg["orders"][-1] if args.order is None else args.order
+    if cfg["dtype"] != "bf16":
+        raise SystemExit("bench.py times the bf16 tensor-core path")
+    q, k, v = workloads.qkv_torch(B, S, Hq, Hkv, d, cfg["seed"] + 7919 * rank, torch.bfloat16, dev)
+    pos_np = workloads.position_ids(cfg)
+    pos = None if pos_np is None else torch.from_numpy(pos_np).to(dev)
+    flops = attention_flops(cfg, pos_np)
+    ulysses = bool(cfg.get("ulysses"))
+    stream = torch.cuda.current_stream()
+
+    if ulysses:
+        G = Hq // P
+        yq = torch.empty((P, B, S, G, d), dtype=torch.bfloat16, device=dev)
+        yk, yv, yo = torch.empty_like(yq), torch.empty_like(yq), torch.empty_like(yq)
+        ylse = torch.empty((P * B, G, S), dtype=torch.float32, device=dev)
+        out = torch.empty_like(q)
+        ws = sp.attention_workspace(P * B, S, False, dev)
+        perm_bytes = 2.0 * 3 * q.numel() * 2  # read + write of q, k, v
+        inv_bytes = 2.0 * q.numel() * 2
+
+        def step(ev=None):
+            n = 0
+            if ev:
+                ev[0].record(stream)
+            for src, dst in ((q, yq), (k, yk), (v, yv)):
+                _lib.sp_ulysses_seq_to_head(src, dst, P)
+                n += _lib.sp_last_launch_count()
+            if ev:
+                ev[1].record(stream)
+            _lib.sp_blockwise_attn_fwd(yq.view(P * B, S, G, d), yk.view(P * B, S, G, d),
+                                       yv.view(P * B, S, G, d), None, P, order, 0.0,
+                                       yo.view(P * B, S, G, d), ylse, ws)
+            n += _lib.sp_last_launch_count()
+            if ev:
+                ev[2].record(stream)
+            _lib.sp_ulysses_head_to_seq(yo, out, P)
+            n += _lib.sp_last_launch_count()
+            if ev:
+                ev[3].record(stream)
+            return n
+    else:
+        out = torch.empty_like(q)
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=dev)
+        ws = sp.attention_workspace(B, S, pos is not None, dev)
+        perm_bytes = inv_bytes = 0.0
+
+        def step(ev=None):
+            if ev:
+                ev[0].record(stream)
+                ev[1].record(stream)
+            _lib.sp_blockwise_attn_fwd(q, k, v, pos, P, order, 0.0, out, lse, ws)
+            n = _lib.sp_last_launch_count()
+            if ev:
+                ev[2].record(stream)
+                ev[3].record(stream)
+            return n
+
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, code = _lib.sp_get_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {code:#x} after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    launches = 0
+    for i in range(args.steps):
+        flush.zero_()  # evict L2 between steps (outside the timed events)
+        launches += step(evs[i])
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    st, code = _lib.sp_get_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {code:#x} in the timed region")
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    perm_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    inv_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    tot_ms = float(sum(step_ms))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    ms_per_step = tot_ms / args.steps
+    value = flops * world * args.steps / (tot_ms * 1e-3) / 1e12
+
+    peaks, peak_kind = load_peaks()
+    attn_mean = statistics.mean(attn_ms)
+    achieved = flops / (attn_mean * 1e-3) / 1e12
+    roofline = {"kernel": "attn_bf16_kernel", "bound": "tensor", "achieved": round(achieved, 1),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "peak_source": f"{peak_kind} bf16 dense (burst)",
+                "traffic": NCU_TRAFFIC_BYTES.get(args.workload),
+                "algorithmic_flops_per_launch": flops}
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v; seeded packed-document position_ids)",
+        "config": {"workload": args.workload, "B": B, "S": S, "Hq": Hq, "Hkv": Hkv, "d": d,
+                   "P": P, "order": order, "causal": pos is not None,
+                   "parallelism": f"replicas{world}" if world > 1 else "single GPU",
+                   "l2": "flushed between timed steps (512 MiB write)"},
+        "roofline": roofline,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if ulysses:
+        perm_mean = statistics.mean(perm_ms)
+        gbs = perm_bytes / (perm_mean * 1e-3) / 1e9
+        inv_gbs = inv_bytes / (statistics.mean(inv_ms) * 1e-3) / 1e9
+        result["permute"] = {
+            "kernel": "permute_kernel (seq_to_head x3, head_to_seq x1)", "bound": "hbm",
+            "seq_to_head_GBps": round(gbs, 1), "head_to_seq_GBps": round(inv_gbs, 1),
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+            "bytes_per_step": perm_bytes + inv_bytes,
+            "note": "L2 flushed before each step; 32 MiB tensors"}
+    result["e2e"] = e2e(args, step_inputs=(q, k, v), out=out, step=step, flops=flops,
+                        world=world, dev=dev)
+    if not args.skip_extra and rank == 0 and world == 1:
+        result["extra"] = extra_measurements(args, peaks)
+    if rank == 0 and world == 1 and not args.skip_cpu:
+        result["cpu_baseline"] = cpu_baseline(cfg, args.workload, order, budget_s=args.cpu_budget)
+    return result
+
+
+def e2e(args, step_inputs, out, step, flops, world, dev):
+    """Same step through the public API with host buffers: pinned H2D of q, k,
+    v and D2H of the output inside the timed region."""
+    import torch
+    stream = torch.cuda.current_stream()
+    hosts = [t.cpu().pin_memory() for t in step_inputs]
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    n = max(3, min(args.steps, 200))
+    for _ in range(3):
+        for h, t in zip(hosts, step_inputs):
+            t.copy_(h, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        for h, t in zip(hosts, step_inputs):
+            t.copy_(h, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in step_inputs)
+    d2h = out.numel() * out.element_size()
+    return {"value": round(flops * world * n / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / n, 4), "steps": n}
+
+
+def extra_measurements(args, peaks):
+    """Causal Llama-3.1-8B-shaped attention (llama8b_32k) and a large-tensor
+    permutation, timed the same way (events, L2 flushed between reps)."""
+    import torch
+
+    import sequence_parallelism_gb300 as sp
+    from sequence_parallelism_gb300 import _lib, workloads
+
+    res = {}
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    if args.workload != "llama8b_32k":
+        cfg = workloads.CONFIGS["llama8b_32k"]
+        B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
+        q, k, v = workloads.qkv_torch(B, S, Hq, Hkv, d, cfg["seed"], torch.bfloat16, "cuda")
+        pos_np = workloads.position_ids(cfg)
+        pos = torch.from_numpy(pos_np).cuda()
+        out = torch.empty_like(q)
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+        ws = sp.attention_workspace(B, S, True)
+        for _ in range(3):
+            _lib.sp_blockwise_attn_fwd(q, k, v, pos, P, "contiguous", 0.0, out, lse, ws)
+        reps = 20
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            _lib.sp_blockwise_attn_fwd(q, k, v, pos, P, "contiguous", 0.0, out, lse, ws)
+            b.record(stream)
+            ms.append((a, b))
+        torch.cuda.synchronize()
+        t = statistics.median([a.elapsed_time(b) for a, b in ms])
+        fl = attention_flops(cfg, pos_np)
+        tf = fl / (t * 1e-3) / 1e12
+        res["llama8b_32k_causal_attention"] = {
+            "ms": round(t, 4), "TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(
+                tf / peaks["bf16_tflops"], 4), "flops": fl, "reps": reps,
+            "note": "doc_start scan + attention kernel, median of reps"}
+        del q, k, v, out
+    x = torch.randn((1, 32768, 32, 128), device="cuda").to(torch.bfloat16)
+    y = torch.empty((8, 1, 32768, 4, 128), dtype=torch.bfloat16, device="cuda")
+    for _ in range(3):
+        _lib.sp_ulysses_seq_to_head(x, y, 8)
+    ms = []
+    for _ in range(20):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        _lib.sp_ulysses_seq_to_head(x, y, 8)
+        b.record(stream)
+        ms.append((a, b))
+    torch.cuda.synchronize()
+    t = statistics.median([a.elapsed_time(b) for a, b in ms])
+    gbs = 2.0 * x.numel() * 2 / (t * 1e-3) / 1e9
+    res["permute_256MiB"] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                             "shape": "[1][32768][32][128] bf16, P=8"}
+    return res
+
+
+# ------------------------------------------------------- CPU oracle leg
+def _oracle_sample(cfg, workload, order, rows):
+    """One bounded sample of the workload through the oracle; returns
+    (algorithmic FLOPs done, seconds)."""
+    import oracle
+    from sequence_parallelism_gb300 import workloads
+
+    B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
+    rng = np.random.default_rng(cfg["seed"])
+    q = rng.standard_normal((B, S, Hq, d)).astype(np.float32)
+    k = rng.standard_normal((B, S, Hkv, d)).astype(np.float32)
+    v = rng.standard_normal((B, S, Hkv, d)).astype(np.float32)
+    pos = workloads.position_ids(cfg)
+    sel = workloads.sample_rows(S, P, rows, cfg["seed"], order)
+    t0 = time.perf_counter()
+    if cfg.get("ulysses"):
+        yq, yk, yv = (oracle.seq_to_head(t, P) for t in (q, k, v))
+        G = Hq // P
+        outs = []
+        for r in range(P):
+            o, _ = oracle.attention_rows(yq[r], yk[r], yv[r], sel, None)
+            outs.append(o)
+        full = np.zeros((P, B, S, G, d))
+        for r in range(P):
+            full[r][:, sel] = outs[r]
+        oracle.head_to_seq(full)
+        fl = 4.0 * d * S * len(sel) * Hq * B
+    else:
+        oracle.attention_rows(q, k, v, sel, pos)
+        seg = oracle.segment_ids(pos)
+        starts = oracle.doc_starts(pos) if S <= 200000 else None
+        if starts is not None:
+            allowed = (sel - starts[0, sel] + 1).astype(np.float64)
+        else:  # plain causal
+            allowed = (sel + 1).astype(np.float64)
+        del seg
+        fl = 4.0 * d * float(allowed.sum()) * Hq * B
+    return fl, time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, workload, order, budget_s=15.0):
+    rows = 8
+    fl, sec = _oracle_sample(cfg, workload, order, rows)
+    # grow the sample to about budget_s of CPU work
+    target = int(rows * budget_s / max(sec, 1e-3))
+    rows = max(rows, min(target, cfg["S"]))
+    fl, sec = _oracle_sample(cfg, workload, order, rows)
+    return {"value": round(fl / sec / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{workload}: {rows} seeded query rows x all heads "
+                      f"(float64 NumPy oracle{', plus full permutations' if cfg.get('ulysses') else ''}),"
+                      f" {sec:.1f} s; BLAS threads = library default (all cores)",
+            "seconds": round(sec, 2)}
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, timed on the host cores: each step one bounded
+    sample of the workload, sized so K + W steps take about two minutes."""
+    if rank != 0:
+        return None
+    from sequence_parallelism_gb300 import workloads
+    cfg = dict(workloads.CONFIGS[args.workload])
+    order = cfg["orders"][-1] if args.order is None else args.order
+    fl1, s1 = _oracle_sample(cfg, args.workload, order, 8)
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    rows = max(1, int(8 * per_step / max(s1, 1e-3)))
+    for _ in range(args.warmup):
+        _oracle_sample(cfg, args.workload, order, rows)
+    tot_fl, tot_s = 0.0, 0.0
+    for _ in range(args.steps):
+        fl, s = _oracle_sample(cfg, args.workload, order, rows)
+        tot_fl += fl
+        tot_s += s
+    value = tot_fl / tot_s / 1e12
+    sample = f"{args.workload}: {rows} seeded query rows x all heads per step (float64 NumPy oracle)"
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot_s * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "order": order},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "kind": "oracle",
+                             "cores": os.cpu_count(), "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="ulysses_4k")
+    ap.add_argument("--order", default=None, choices=[None, "contiguous", "striped"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--skip-extra", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if not os.path.exists(os.path.join(ROOT, "sequence_parallelism_gb300", "libsp_gb300.so")):
+        import __graft_entry__
+        __graft_entry__.build()
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

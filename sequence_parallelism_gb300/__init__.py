@@ -1,0 +1,101 @@
+"""GB300-native blockwise (ring) attention and Ulysses layout permutation.
+
+The compute runs in libsp_gb300.so (hand-written sm_103a CUDA, C ABI in
+include/sp_gb300.h); this package only allocates outputs and workspace with
+torch and calls the C entry points on the current stream.  Importing it
+without the built library raises ImportError -- there is no CPU path.
+
+    seq_to_head(x, P) / head_to_seq(y)         Ulysses redistribution
+    blockwise_attention(q, k, v, P, ...)       ring-order online-softmax attention
+    ring_step(q, k, v, P, step, ...)           one ring step's partial result
+    merge_partials(outs, lses)                 log-sum-exp combine of partials
+    ulysses_attention(q, k, v, P, ...)         permute -> attention -> permute back
+    doc_starts(position_ids)                   O(n) causal-mask carrier
+"""
+
+import torch
+
+from . import _lib
+from ._lib import SPError  # noqa: F401
+
+__all__ = ["seq_to_head", "head_to_seq", "blockwise_attention", "ring_step", "merge_partials",
+           "ulysses_attention", "doc_starts", "attention_workspace", "SPError"]
+
+
+def seq_to_head(x, P, out=None):
+    B, S, H, d = x.shape
+    y = torch.empty((P, B, S, H // P, d), dtype=x.dtype, device=x.device) if out is None else out
+    return _lib.sp_ulysses_seq_to_head(x, y, P)
+
+
+def head_to_seq(y, out=None):
+    P, B, S, G, d = y.shape
+    x = torch.empty((B, S, P * G, d), dtype=y.dtype, device=y.device) if out is None else out
+    return _lib.sp_ulysses_head_to_seq(y, x, P)
+
+
+def attention_workspace(B, S, causal, device=None):
+    n = _lib.sp_blockwise_attn_workspace_bytes(B, S, causal)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _outputs(q, out, lse):
+    B, S, Hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    return out, lse
+
+
+def blockwise_attention(q, k, v, P, order="contiguous", position_ids=None, scale=0.0, out=None,
+                        lse=None, workspace=None):
+    """Exact attention over P ring blocks; returns (out, lse)."""
+    B, S = q.shape[:2]
+    out, lse = _outputs(q, out, lse)
+    if workspace is None:
+        workspace = attention_workspace(B, S, position_ids is not None, q.device)
+    return _lib.sp_blockwise_attn_fwd(q, k, v, position_ids, P, order, scale, out, lse, workspace)
+
+
+def ring_step(q, k, v, P, step, order="contiguous", position_ids=None, scale=0.0, out=None,
+              lse=None, workspace=None):
+    """Partial result of ring step `step` for every query block; (out, lse)."""
+    B, S = q.shape[:2]
+    out, lse = _outputs(q, out, lse)
+    if workspace is None:
+        workspace = attention_workspace(B, S, position_ids is not None, q.device)
+    return _lib.sp_blockwise_attn_step(q, k, v, position_ids, P, order, step, scale, out, lse,
+                                       workspace)
+
+
+def merge_partials(outs, lses, out=None, lse=None):
+    P, B, S, H, d = outs.shape
+    if out is None:
+        out = torch.empty((B, S, H, d), dtype=outs.dtype, device=outs.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=outs.device)
+    return _lib.sp_attn_merge_partials(outs, lses, out, lse)
+
+
+def doc_starts(position_ids):
+    B, S = position_ids.shape
+    ws = torch.empty(_lib.sp_segment_starts_workspace_bytes(B, S), dtype=torch.uint8,
+                     device=position_ids.device)
+    ds = torch.empty_like(position_ids)
+    return _lib.sp_segment_starts(position_ids, ds, ws)
+
+
+def ulysses_attention(q, k, v, P, ring_blocks=None, order="contiguous", scale=0.0):
+    """One Ulysses attention layer simulated on one GPU.
+
+    q [B][S][Hq][d], k/v [B][S][Hkv][d] in sequence-sharded layout: permute to
+    head groups ([P][B][S][H/P][d] = batch P*B), run blockwise attention with
+    `ring_blocks` blocks per head group (default P), permute back.  Non-causal.
+    """
+    B, S, Hq, d = q.shape
+    yq, yk, yv = seq_to_head(q, P), seq_to_head(k, P), seq_to_head(v, P)
+    G, Gk = Hq // P, k.shape[2] // P
+    yo, _ = blockwise_attention(yq.view(P * B, S, G, d), yk.view(P * B, S, Gk, d),
+                                yv.view(P * B, S, Gk, d), ring_blocks or P, order, None, scale)
+    return head_to_seq(yo.view(P, B, S, G, d))

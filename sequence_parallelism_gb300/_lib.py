@@ -1,0 +1,177 @@
+"""ctypes binding of libsp_gb300.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls (include/
+sp_gb300.h), takes torch tensors, passes their device pointers, sizes and
+the current CUDA stream, and raises SPError on any non-OK status.  Nothing is
+computed in Python: if the shared library is missing the import fails -- there
+is no fallback.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsp_gb300.so")
+
+SP_OK, SP_ERR_INVALID_ARG, SP_ERR_UNSUPPORTED, SP_ERR_WORKSPACE, SP_ERR_CUDA, \
+    SP_ERR_DEVICE_TIMEOUT = range(6)
+SP_BF16, SP_F32 = 0, 1
+SP_ORDER_CONTIGUOUS, SP_ORDER_STRIPED = 0, 1
+
+_ORDERS = {"contiguous": SP_ORDER_CONTIGUOUS, "striped": SP_ORDER_STRIPED}
+
+EXPORTS = (
+    "sp_status_string", "sp_ulysses_seq_to_head", "sp_ulysses_head_to_seq",
+    "sp_segment_starts_workspace_bytes", "sp_segment_starts", "sp_blockwise_attn_workspace_bytes",
+    "sp_blockwise_attn_fwd", "sp_blockwise_attn_step", "sp_attn_merge_partials",
+    "sp_get_device_error", "sp_last_launch_count",
+)
+
+
+class SPError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn}: {_lib.sp_status_string(status).decode()}")
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is not built; run sequence_parallelism_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "sp_status_string": (ctypes.c_char_p, [i]),
+        "sp_ulysses_seq_to_head": (i, [vp, vp, i, i, i, i, i, i, vp]),
+        "sp_ulysses_head_to_seq": (i, [vp, vp, i, i, i, i, i, i, vp]),
+        "sp_segment_starts_workspace_bytes": (sz, [i, i]),
+        "sp_segment_starts": (i, [vp, vp, i, i, vp, sz, vp]),
+        "sp_blockwise_attn_workspace_bytes": (sz, [i, i, i]),
+        "sp_blockwise_attn_fwd": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, vp, vp, sz,
+                                      vp]),
+        "sp_blockwise_attn_step": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp,
+                                       sz, vp]),
+        "sp_attn_merge_partials": (i, [vp, vp, i, i, i, i, i, i, vp, vp, vp]),
+        "sp_get_device_error": (i, [vp, ctypes.POINTER(ctypes.c_int), vp]),
+        "sp_last_launch_count": (i, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype(t):
+    if t.dtype == torch.bfloat16:
+        return SP_BF16
+    if t.dtype == torch.float32:
+        return SP_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _check(fn, status):
+    if status != SP_OK:
+        raise SPError(fn, status)
+
+
+def _dense(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def sp_status_string(status):
+    return _lib.sp_status_string(status).decode()
+
+
+def sp_last_launch_count():
+    return _lib.sp_last_launch_count()
+
+
+def sp_ulysses_seq_to_head(x, y, P, stream=None):
+    """x [B][S][H][d] -> y [P][B][S][H/P][d]."""
+    _dense(x, y)
+    B, S, H, d = x.shape
+    _check("sp_ulysses_seq_to_head", _lib.sp_ulysses_seq_to_head(
+        _ptr(x), _ptr(y), B, S, H, d, P, _dtype(x), _stream(stream)))
+    return y
+
+
+def sp_ulysses_head_to_seq(y, x, P, stream=None):
+    """y [P][B][S][H/P][d] -> x [B][S][H][d]."""
+    _dense(x, y)
+    B, S, H, d = x.shape
+    _check("sp_ulysses_head_to_seq", _lib.sp_ulysses_head_to_seq(
+        _ptr(y), _ptr(x), B, S, H, d, P, _dtype(x), _stream(stream)))
+    return x
+
+
+def sp_segment_starts_workspace_bytes(B, S):
+    return _lib.sp_segment_starts_workspace_bytes(B, S)
+
+
+def sp_segment_starts(position_ids, doc_start, workspace, stream=None):
+    _dense(position_ids, doc_start, workspace)
+    B, S = position_ids.shape
+    _check("sp_segment_starts", _lib.sp_segment_starts(
+        _ptr(position_ids), _ptr(doc_start), B, S, _ptr(workspace), workspace.numel()
+        * workspace.element_size(), _stream(stream)))
+    return doc_start
+
+
+def sp_blockwise_attn_workspace_bytes(B, S, causal):
+    return _lib.sp_blockwise_attn_workspace_bytes(B, S, int(bool(causal)))
+
+
+def sp_blockwise_attn_fwd(q, k, v, position_ids, P, order, scale, out, lse, workspace,
+                          stream=None):
+    _dense(q, k, v, position_ids, out, lse, workspace)
+    B, S, Hq, d = q.shape
+    Hkv = k.shape[2]
+    _check("sp_blockwise_attn_fwd", _lib.sp_blockwise_attn_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(position_ids), B, S, Hq, Hkv, d, P, _ORDERS[order],
+        float(scale), _dtype(q), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse
+
+
+def sp_blockwise_attn_step(q, k, v, position_ids, P, order, step, scale, out, lse, workspace,
+                           stream=None):
+    _dense(q, k, v, position_ids, out, lse, workspace)
+    B, S, Hq, d = q.shape
+    Hkv = k.shape[2]
+    _check("sp_blockwise_attn_step", _lib.sp_blockwise_attn_step(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(position_ids), B, S, Hq, Hkv, d, P, _ORDERS[order], step,
+        float(scale), _dtype(q), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse
+
+
+def sp_attn_merge_partials(outs, lses, out, lse, stream=None):
+    """outs [P][B][S][H][d], lses [P][B][H][S] -> out [B][S][H][d], lse [B][H][S]."""
+    _dense(outs, lses, out, lse)
+    P, B, S, H, d = outs.shape
+    _check("sp_attn_merge_partials", _lib.sp_attn_merge_partials(
+        _ptr(outs), _ptr(lses), P, B, S, H, d, _dtype(outs), _ptr(out), _ptr(lse),
+        _stream(stream)))
+    return out, lse
+
+
+def sp_get_device_error(workspace, stream=None):
+    code = ctypes.c_int(0)
+    st = _lib.sp_get_device_error(_ptr(workspace), ctypes.byref(code), _stream(stream))
+    return st, code.value

@@ -1,0 +1,563 @@
+// attn_bf16.cu -- blockwise ring attention on the sm_103a tensor cores.
+//
+// Method ("Ring Attention", "Cómo funciona la atención en anillo"): the
+// sequence is cut into P blocks; query block i stays resident while the
+// key/value blocks arrive in ring order j = (i - s) mod P; each arrival is
+// folded into a running max m, a running sum of exponentiated scores l and a
+// running weighted-value sum O (the cumulative softmax, with the running
+// maximum subtracted as production kernels do), and O / l is written at the
+// end.  The causal mask comes from O(n) position_ids ("Ulysses SPで100万
+// トークン学習", section 3) through the doc_start array: query t may attend
+// key j iff doc_start[t] <= j <= t, so each score row has one contiguous
+// allowed interval per key tile and fully masked tiles are never visited.
+//
+// One CTA = one (batch, q head, query block i, 256 query rows) and keeps its
+// two 128-row Q tiles in shared memory for the whole ring.  Warp roles:
+//   warps 0-3   softmax group 0: one thread per row of Q tile 0
+//   warps 4-7   softmax group 1: one thread per row of Q tile 1
+//   warp  8     TMA producer: Q once, then K_t, V_t into a 4-slot ring
+//   warp  9     TMEM owner + single-thread tcgen05.mma issuer
+// Tensor memory (512 columns x 128 lanes, fp32):
+//   [0,128) S0   [128,256) S1   [256,384) O0   [384,512) O1
+// P (bf16, two per column) overwrites the first 64 columns of its S tile and
+// feeds the PV product straight from TMEM.  The MMA issue order
+//   S0(t+1) after PV0(t), PV1(t) between, S1(t+1) after PV1(t)
+// keeps the tensor pipe busy with one Q tile while the other tile's softmax
+// runs.  O is rescaled in TMEM only when a row's max grows by more than
+// 2^8 (exact after the final division; bf16 P stays far from overflow).
+//
+// Operand layouts (all 128-byte swizzled, as TMA writes them):
+//   Q, K tile: [2 halves of d][128 rows][64 elements]  K-major for S = Q K^T
+//   V tile   : [2 halves of d][128 keys][64 elements]  MN-major B for O += P V
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "attn_common.cuh"
+#include "ptx.cuh"
+
+namespace sp {
+namespace {
+
+using namespace ptx;
+
+constexpr int kD = 128;
+constexpr int kBM = 128;              // rows per Q tile
+constexpr int kBN = 128;              // keys per K/V tile
+constexpr int kQTiles = 2;            // Q tiles per CTA
+constexpr int kRowsPerCta = kBM * kQTiles;
+constexpr int kSlots = 4;             // K/V ring depth
+constexpr int kTileBytes = kBN * kD * 2;          // 32 KiB
+constexpr int kHalfBytes = kTileBytes / 2;        // one 64-column half
+constexpr int kSmemBytes = (kQTiles + kSlots) * kTileBytes;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, true);
+
+// error codes recorded in the workspace error word (which wait gave up)
+enum : int {
+  kErrQFull = 0x101, kErrKvEmpty = 0x102, kErrKvFull = 0x103, kErrSFull = 0x104,
+  kErrPFull = 0x105, kErrOFull = 0x106, kErrDrain = 0x107
+};
+
+struct Tmaps {
+  CUtensorMap q, k, v;
+};
+
+__device__ __forceinline__ long long floor_div(long long a, long long b) {
+  return a >= 0 ? a / b : -((-a + b - 1) / b);
+}
+
+// The part of the ring schedule every role must agree on.
+struct Schedule {
+  int i, P, Lb, S, order, step_begin, step_end;
+  long long hull_lo, hull_hi;  // key-token interval any row of the CTA may use
+
+  // KV tiles [kt0, kt1] of block j that intersect the hull (kt1 < kt0: none)
+  __device__ __forceinline__ void tiles(int s, int& j, int& kt0, int& kt1) const {
+    j = ((i - s) % P + P) % P;
+    long long w_lo, w_hi;
+    if (order == SP_ORDER_STRIPED) {
+      w_lo = -floor_div(-(hull_lo - j), P);  // ceil((lo - j) / P)
+      w_hi = floor_div(hull_hi - j, P);
+    } else {
+      const long long base = static_cast<long long>(j) * Lb;
+      w_lo = hull_lo - base;
+      w_hi = hull_hi - base;
+    }
+    if (w_lo < 0) w_lo = 0;
+    if (w_hi > Lb - 1) w_hi = Lb - 1;
+    if (w_lo > w_hi) {
+      kt0 = 0;
+      kt1 = -1;
+      return;
+    }
+    kt0 = static_cast<int>(w_lo / kBN);
+    kt1 = static_cast<int>(w_hi / kBN);
+  }
+
+  __device__ __forceinline__ int count() const {
+    int n = 0;
+    for (int s = step_begin; s < step_end; ++s) {
+      int j, a, b;
+      tiles(s, j, a, b);
+      n += b - a + 1;
+    }
+    return n;
+  }
+};
+
+struct __align__(8) Barriers {
+  uint64_t q_full;
+  uint64_t kv_full[kSlots];
+  uint64_t kv_empty[kSlots];
+  uint64_t s_full[kQTiles];
+  uint64_t p_full[kQTiles];
+  uint64_t o_full[kQTiles];
+  uint64_t done;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bf16_kernel(const __grid_constant__ Tmaps tm, AttnArgs a, float scale_log2,
+                     int n_pairs) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Barriers bars;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+
+  // 1024-byte alignment for the 128-byte swizzle atoms
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t smem_q = smem_u32(smem);                         // Q0, Q1
+  const uint32_t smem_kv = smem_q + kQTiles * kTileBytes;         // ring slots
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work item: heavy query positions first, heads innermost ----------
+  const int BH = a.B * a.Hq;
+  const int pos = blockIdx.x / BH;
+  const int bh = blockIdx.x % BH;
+  const int b = bh / a.Hq;
+  const int hq = bh % a.Hq;
+  const int kvh = hq / (a.Hq / a.Hkv);
+  const int rev = a.P * n_pairs - 1 - pos;
+  const int i = rev / n_pairs;
+  const int pair = rev % n_pairs;
+  const int Lb = a.S / a.P;
+  const int u0 = pair * kRowsPerCta;  // first local query row of the CTA
+
+  Schedule sch;
+  sch.i = i;
+  sch.P = a.P;
+  sch.Lb = Lb;
+  sch.S = a.S;
+  sch.order = a.order;
+  sch.step_begin = a.step_begin;
+  sch.step_end = a.step_end;
+  {
+    const int u_last = min(u0 + kRowsPerCta, Lb) - 1;
+    const long long t_first = block_token(a.order, a.S, a.P, i, u0);
+    const long long t_last = block_token(a.order, a.S, a.P, i, u_last);
+    if (a.doc_start) {
+      sch.hull_lo = a.doc_start[static_cast<long long>(b) * a.S + t_first];
+      sch.hull_hi = t_last;
+    } else {
+      sch.hull_lo = 0;
+      sch.hull_hi = a.S - 1;
+    }
+  }
+  const int n_tiles = sch.count();
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bars.q_full), 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(smem_u32(&bars.kv_full[s]), 1);
+      mbar_init(smem_u32(&bars.kv_empty[s]), 1);
+    }
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(smem_u32(&bars.s_full[t]), 1);
+      mbar_init(smem_u32(&bars.p_full[t]), kBM);
+      mbar_init(smem_u32(&bars.o_full[t]), 1);
+    }
+    mbar_init(smem_u32(&bars.done), 1);
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  volatile int* abort_flag = &abort_s;
+
+  // coordinates of local row u of block p in the 5-D tensor maps
+  auto coord_rows = [&](int p, int u, int& c2, int& c3) {
+    if (a.order == SP_ORDER_STRIPED) {
+      c2 = p;
+      c3 = u;
+    } else {
+      c2 = u;
+      c3 = p;
+    }
+  };
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tm.q);
+      prefetch_tmap(&tm.k);
+      prefetch_tmap(&tm.v);
+      const uint32_t qf = smem_u32(&bars.q_full);
+      mbar_arrive_expect_tx(qf, kQTiles * kTileBytes);
+      for (int t = 0; t < kQTiles; ++t) {
+        int c2, c3;
+        coord_rows(i, u0 + t * kBM, c2, c3);
+        for (int half = 0; half < 2; ++half)
+          tma_load_5d(smem_q + t * kTileBytes + half * kHalfBytes, &tm.q, qf, half * 64, hq, c2,
+                      c3, b);
+      }
+      int n = 0;  // load index: K_t = 2t, V_t = 2t + 1
+      bool ok = true;
+      for (int s = a.step_begin; s < a.step_end && ok; ++s) {
+        int j, kt0, kt1;
+        sch.tiles(s, j, kt0, kt1);
+        for (int kt = kt0; kt <= kt1 && ok; ++kt) {
+          int c2, c3;
+          coord_rows(j, kt * kBN, c2, c3);
+          for (int kv = 0; kv < 2; ++kv, ++n) {
+            const int slot = n % kSlots;
+            const uint32_t parity = ((n / kSlots) & 1) ^ 1;
+            if (!mbar_wait(smem_u32(&bars.kv_empty[slot]), parity, abort_flag, a.err,
+                           kErrKvEmpty)) {
+              ok = false;
+              break;
+            }
+            const uint32_t full = smem_u32(&bars.kv_full[slot]);
+            mbar_arrive_expect_tx(full, kTileBytes);
+            const CUtensorMap* map = kv == 0 ? &tm.k : &tm.v;
+            for (int half = 0; half < 2; ++half)
+              tma_load_5d(smem_kv + slot * kTileBytes + half * kHalfBytes, map, full, half * 64,
+                          kvh, c2, c3, b);
+          }
+        }
+      }
+      // drain: every copy this CTA started has landed before it may exit
+      mbar_wait(qf, 0, abort_flag, a.err, kErrDrain);
+      for (int m = n - 1; m >= 0 && m >= n - kSlots; --m)
+        mbar_wait(smem_u32(&bars.kv_full[m % kSlots]), (m / kSlots) & 1, abort_flag, a.err,
+                  kErrDrain);
+    }
+  } else if (warp == kMmaWarp) {
+    // --------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abort_flag, a.err, kErrQFull);
+      tc_fence_after();
+      const uint32_t tS[2] = {tmem + 0, tmem + 128};
+      const uint32_t tO[2] = {tmem + 256, tmem + 384};
+      // S_t = Q_t K^T over d = 128: 8 k-steps of 16, 32 bytes apart inside a
+      // 128-byte swizzled row, the second 64 columns in the next half tile.
+      auto issue_s = [&](int t, int load_idx) {
+        const int slot = load_idx % kSlots;
+        const uint32_t qa = smem_q + t * kTileBytes;
+        const uint32_t kb = smem_kv + slot * kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          mma_ss(tS[t], smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
+                 kIdescQK, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&bars.s_full[t]));
+      };
+      // O_t (+)= P_t V: P from TMEM (8 columns = 16 keys per k-step), V
+      // MN-major: 16 keys = 2 swizzle atoms of 8 rows (stride 1024 B), the
+      // two 64-column halves of d 16 KiB apart.
+      auto issue_pv = [&](int t, int it, int slot) {
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint32_t vb = smem_kv + slot * kTileBytes + kk * 16 * 128;
+          mma_ts(tO[t], tS[t] + kk * 8, smem_desc_sw128(vb, kHalfBytes, 1024), kIdescPV,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      if (ok) ok = mbar_wait(smem_u32(&bars.kv_full[0]), 0, abort_flag, a.err, kErrKvFull);
+      tc_fence_after();
+      if (ok) {
+        issue_s(0, 0);
+        issue_s(1, 0);
+        mma_commit(smem_u32(&bars.kv_empty[0]));  // K_0 consumed
+      }
+      for (int it = 0; it < n_tiles && ok; ++it) {
+        const int v_idx = 2 * it + 1, k_next = 2 * it + 2;
+        const int v_slot = v_idx % kSlots, k_slot = k_next % kSlots;
+        if (!mbar_wait(smem_u32(&bars.kv_full[v_slot]), (v_idx / kSlots) & 1, abort_flag, a.err,
+                       kErrKvFull))
+          break;
+        const bool more = it + 1 < n_tiles;
+        if (more && !mbar_wait(smem_u32(&bars.kv_full[k_slot]), (k_next / kSlots) & 1,
+                               abort_flag, a.err, kErrKvFull))
+          break;
+        tc_fence_after();
+        // tile 0: PV then next S
+        if (!mbar_wait(smem_u32(&bars.p_full[0]), it & 1, abort_flag, a.err, kErrPFull)) break;
+        tc_fence_after();
+        issue_pv(0, it, v_slot);
+        if (!more) mma_commit(smem_u32(&bars.o_full[0]));
+        if (more) issue_s(0, k_next);
+        // tile 1
+        if (!mbar_wait(smem_u32(&bars.p_full[1]), it & 1, abort_flag, a.err, kErrPFull)) break;
+        tc_fence_after();
+        issue_pv(1, it, v_slot);
+        mma_commit(smem_u32(&bars.kv_empty[v_slot]));  // V_it consumed
+        if (!more) mma_commit(smem_u32(&bars.o_full[1]));
+        if (more) {
+          issue_s(1, k_next);
+          mma_commit(smem_u32(&bars.kv_empty[k_slot]));  // K_{it+1} consumed
+        }
+      }
+      // every MMA issued has completed before TMEM is released
+      mma_commit(smem_u32(&bars.done));
+      mbar_wait(smem_u32(&bars.done), 0, abort_flag, a.err, kErrDrain);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------- softmax warpgroups
+    const int t = warp >> 2;           // Q tile of this group
+    const int row = threadIdx.x & 127;  // TMEM lane == row of the tile
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * 128;
+    const uint32_t tO = tmem + lane_base + 256 + t * 128;
+    const int u = u0 + t * kBM + row;  // local row in block i
+    const bool row_live = u < Lb;
+    const long long tq = row_live ? block_token(a.order, a.S, a.P, i, u) : 0;
+    long long lo, hi;
+    if (a.doc_start && row_live) {
+      lo = a.doc_start[static_cast<long long>(b) * a.S + tq];
+      hi = tq;
+    } else {
+      lo = 0;
+      hi = a.S - 1;
+    }
+    float m_run = -INFINITY;   // running max (log2 units, scaled)
+    float m_use = -INFINITY;   // exponent base actually applied
+    float l = 0.f;
+    int it = 0;
+    bool ok = true;
+    for (int s = a.step_begin; s < a.step_end && ok; ++s) {
+      int j, kt0, kt1;
+      sch.tiles(s, j, kt0, kt1);
+      for (int kt = kt0; kt <= kt1; ++kt, ++it) {
+        // warp-uniform outcome: the tcgen05.ld below is warp-collective
+        const bool got = mbar_wait(smem_u32(&bars.s_full[t]), it & 1, abort_flag, a.err, kErrSFull);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float x[kBN];
+        {
+          uint32_t r[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            tmem_ld32(tS + c * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(r[e]);
+          }
+        }
+        // allowed columns [c_lo, c_hi] of this tile for this row
+        long long c_lo, c_hi;
+        const long long w_base = static_cast<long long>(kt) * kBN;
+        if (a.order == SP_ORDER_STRIPED) {
+          c_lo = -floor_div(-(lo - j), a.P) - w_base;
+          c_hi = floor_div(hi - j, a.P) - w_base;
+        } else {
+          const long long base = static_cast<long long>(j) * Lb + w_base;
+          c_lo = lo - base;
+          c_hi = hi - base;
+        }
+        const long long c_valid = static_cast<long long>(Lb) - w_base - 1;
+        if (c_hi > c_valid) c_hi = c_valid;
+        if (c_lo > 0 || c_hi < kBN - 1) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c < c_lo || c > c_hi) x[c] = -INFINITY;
+        }
+        float mt = x[0];
+#pragma unroll
+        for (int c = 1; c < kBN; ++c) mt = fmaxf(mt, x[c]);
+        m_run = fmaxf(m_run, mt * scale_log2);
+        float alpha = 1.f;
+        bool rescale = false;
+        if (m_use == -INFINITY) {
+          m_use = m_run;  // first allowed key: O and l are still zero
+        } else if (m_run > m_use + kRescaleThreshold) {
+          alpha = ex2(m_use - m_run);
+          m_use = m_run;
+          rescale = true;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tO + c * 32, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(tO + c * 32, r);
+          }
+        }
+        const float base = (m_use == -INFINITY) ? 0.f : m_use;
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          x[c] = ex2(fmaf(x[c], scale_log2, -base));
+          sum += x[c];
+        }
+        l = l * alpha + sum;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = pack_bf16(x[c * 64 + 2 * e], x[c * 64 + 2 * e + 1]);
+          tmem_st32(tS + c * 32, r);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.p_full[t]));
+      }
+    }
+    // ------------------------------------------------------------ epilogue
+    const bool have = n_tiles > 0 && ok;
+    if (have) {
+      const bool got = mbar_wait(smem_u32(&bars.o_full[t]), 0, abort_flag, a.err, kErrOFull);
+      if (!__all_sync(0xffffffffu, got)) ok = false;
+    }
+    tc_fence_after();
+    const bool any = have && ok && l > 0.f;
+    const float inv = any ? 1.f / l : 0.f;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+    uint4* orow = reinterpret_cast<uint4*>(
+        out + ((static_cast<long long>(b) * a.S + tq) * a.Hq + hq) * kD);
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t r[32];
+      if (have && ok) {
+        tmem_ld32(tO + c * 32, r);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) r[e] = 0u;
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        pk[e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+      if (row_live) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          orow[c * 4 + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+      }
+    }
+    if (row_live && a.lse)
+      a.lse[(static_cast<long long>(b) * a.Hq + hq) * a.S + tq] =
+          any ? (m_use + lg2(l)) * 0.69314718055994530942f : -INFINITY;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// [B][S][H][128] bf16 viewed as 5-D (d, H, rows-in-block, block, B) for the
+// contiguous order or (d, H, block, rows-in-block, B) for the striped order,
+// box = 64 columns x 1 head x 128 rows, 128-byte swizzle.  Rows past the end
+// of a block are out of bounds and read as zeros.
+bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int P, int order) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t Lb = static_cast<cuuint64_t>(S / P);
+  const cuuint64_t row = static_cast<cuuint64_t>(H) * kD * 2;  // bytes per token
+  cuuint64_t dims[5], strides[4];
+  cuuint32_t box[5], estr[5] = {1, 1, 1, 1, 1};
+  dims[0] = kD;
+  dims[1] = H;
+  dims[4] = B;
+  strides[0] = kD * 2;
+  strides[3] = static_cast<cuuint64_t>(S) * row;
+  box[0] = 64;
+  box[1] = 1;
+  box[4] = 1;
+  if (order == SP_ORDER_STRIPED) {
+    dims[2] = P;
+    dims[3] = Lb;
+    strides[1] = row;
+    strides[2] = row * P;
+    box[2] = 1;
+    box[3] = kBN;
+  } else {
+    dims[2] = Lb;
+    dims[3] = P;
+    strides[1] = row;
+    strides[2] = row * Lb;
+    box[2] = kBN;
+    box[3] = 1;
+  }
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
+  Tmaps tm;
+  if (!make_map(&tm.q, a.q, a.B, a.S, a.Hq, a.P, a.order) ||
+      !make_map(&tm.k, a.k, a.B, a.S, a.Hkv, a.P, a.order) ||
+      !make_map(&tm.v, a.v, a.B, a.S, a.Hkv, a.P, a.order))
+    return -1;
+  const int Lb = a.S / a.P;
+  const int n_pairs = (Lb + kRowsPerCta - 1) / kRowsPerCta;
+  const long long blocks = static_cast<long long>(a.B) * a.Hq * a.P * n_pairs;
+  const size_t smem = kSmemBytes + 1024;
+  if (cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return -1;
+  const float scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  attn_bf16_kernel<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(tm, a, scale_log2,
+                                                                            n_pairs);
+  return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+}  // namespace sp

@@ -1,0 +1,37 @@
+// attn_common.cuh -- what the attention entry points hand to the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace sp {
+
+// One blockwise-attention launch.  Ring steps [step_begin, step_end) are
+// visited for every query block i: key/value block j = (i - s) mod P.
+struct AttnArgs {
+  const void* q;               // [B][S][Hq][d]
+  const void* k;               // [B][S][Hkv][d]
+  const void* v;               // [B][S][Hkv][d]
+  const int32_t* doc_start;    // [B][S] or nullptr (non-causal)
+  void* out;                   // [B][S][Hq][d]
+  float* lse;                  // [B][Hq][S] or nullptr
+  int* err;                    // device error word
+  int B, S, Hq, Hkv, d, P;
+  int order;                   // sp_block_order
+  int step_begin, step_end;
+  float scale;                 // multiplies q.k (natural-log domain)
+};
+
+// Both return the number of kernels launched, or -1 on a CUDA error.
+int launch_attn_f32(const AttnArgs& a, cudaStream_t stream);
+int launch_attn_bf16(const AttnArgs& a, cudaStream_t stream);
+
+// Token index of local row u of block p (both orders).
+__host__ __device__ __forceinline__ long long block_token(int order, int S, int P, int p,
+                                                          long long u) {
+  return order == SP_ORDER_STRIPED ? u * P + p : static_cast<long long>(p) * (S / P) + u;
+}
+
+}  // namespace sp

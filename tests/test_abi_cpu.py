@@ -1,0 +1,119 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/sp_gb300.h declares, sizes its workspace, and rejects bad arguments
+on the host before touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sp_gb300.h")
+LIB = os.path.join(ROOT, "sequence_parallelism_gb300", "libsp_gb300.so")
+
+SP_OK, SP_ERR_INVALID_ARG, SP_ERR_UNSUPPORTED, SP_ERR_WORKSPACE = 0, 1, 2, 3
+FAKE = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
+FAKE_WS = ctypes.c_void_p(0x20000)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(LIB):
+        import __graft_entry__
+        __graft_entry__.build()
+    from sequence_parallelism_gb300 import _lib
+    return _lib._lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sp_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("sp_ulysses_seq_to_head", "sp_ulysses_head_to_seq", "sp_blockwise_attn_fwd",
+              "sp_attn_merge_partials", "sp_blockwise_attn_step", "sp_segment_starts"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_every_export(lib):
+    from sequence_parallelism_gb300 import _lib
+    assert set(_lib.EXPORTS) == set(declared_functions())
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.sp_status_string(s).decode().startswith("SP_")
+
+
+def test_workspace_sizes(lib):
+    assert lib.sp_blockwise_attn_workspace_bytes(1, 4096, 0) == 256
+    n = lib.sp_blockwise_attn_workspace_bytes(2, 1000, 1)
+    assert n >= 256 + 2 * 1000 * 4 and n % 256 == 0
+    assert lib.sp_blockwise_attn_workspace_bytes(0, 10, 1) == 0
+    assert lib.sp_segment_starts_workspace_bytes(1, 524288) >= 512 * 4
+
+
+def _permute(lib, fn, x, y, B, S, H, d, P, dt=0):
+    return getattr(lib, fn)(x, y, B, S, H, d, P, dt, None)
+
+
+@pytest.mark.parametrize("fn", ["sp_ulysses_seq_to_head", "sp_ulysses_head_to_seq"])
+def test_permute_rejects_bad_arguments(lib, fn):
+    assert _permute(lib, fn, None, FAKE, 1, 8, 4, 16, 2) == SP_ERR_INVALID_ARG
+    assert _permute(lib, fn, FAKE, None, 1, 8, 4, 16, 2) == SP_ERR_INVALID_ARG
+    assert _permute(lib, fn, FAKE, FAKE, 1, 9, 4, 16, 2) == SP_ERR_INVALID_ARG   # S % P
+    assert _permute(lib, fn, FAKE, FAKE, 1, 8, 6, 16, 4) == SP_ERR_INVALID_ARG   # H % P
+    assert _permute(lib, fn, FAKE, FAKE, 0, 8, 4, 16, 2) == SP_ERR_INVALID_ARG
+    assert _permute(lib, fn, FAKE, FAKE, 1, 8, 4, 16, 0) == SP_ERR_INVALID_ARG
+    assert _permute(lib, fn, FAKE, FAKE, 1, 8, 4, 16, 2, dt=7) == SP_ERR_INVALID_ARG
+    assert lib.sp_last_launch_count() == 0
+
+
+def _attn(lib, q=FAKE, k=FAKE, v=FAKE, pos=None, B=1, S=256, Hq=4, Hkv=2, d=128, P=2, order=0,
+          scale=0.0, dt=0, out=FAKE, ws=FAKE_WS, wsb=1 << 20, step=None):
+    if step is None:
+        return lib.sp_blockwise_attn_fwd(q, k, v, pos, B, S, Hq, Hkv, d, P, order, scale, dt, out,
+                                         None, ws, wsb, None)
+    return lib.sp_blockwise_attn_step(q, k, v, pos, B, S, Hq, Hkv, d, P, order, step, scale, dt,
+                                      out, None, ws, wsb, None)
+
+
+def test_attention_rejects_bad_arguments(lib):
+    assert _attn(lib, q=None) == SP_ERR_INVALID_ARG
+    assert _attn(lib, out=None) == SP_ERR_INVALID_ARG
+    assert _attn(lib, S=255) == SP_ERR_INVALID_ARG            # S % P
+    assert _attn(lib, Hq=6, Hkv=4) == SP_ERR_INVALID_ARG      # Hq % Hkv
+    assert _attn(lib, order=2) == SP_ERR_INVALID_ARG
+    assert _attn(lib, dt=5) == SP_ERR_INVALID_ARG
+    assert _attn(lib, P=0) == SP_ERR_INVALID_ARG
+    assert _attn(lib, scale=float("nan")) == SP_ERR_INVALID_ARG
+    assert _attn(lib, d=64) == SP_ERR_UNSUPPORTED              # bf16 needs d == 128
+    assert _attn(lib, d=512, dt=1) == SP_ERR_UNSUPPORTED       # f32 d <= 256
+    assert _attn(lib, q=ctypes.c_void_p(0x10008)) == SP_ERR_INVALID_ARG  # TMA alignment
+    assert _attn(lib, ws=None) == SP_ERR_WORKSPACE
+    assert _attn(lib, ws=ctypes.c_void_p(0x20010)) == SP_ERR_WORKSPACE  # 256-byte alignment
+    assert _attn(lib, pos=FAKE, wsb=256) == SP_ERR_WORKSPACE           # causal needs doc_start
+    assert _attn(lib, step=2) == SP_ERR_INVALID_ARG
+    assert _attn(lib, step=-1) == SP_ERR_INVALID_ARG
+    assert lib.sp_last_launch_count() == 0
+
+
+def test_merge_and_segments_reject_bad_arguments(lib):
+    m = lib.sp_attn_merge_partials
+    assert m(None, FAKE, 2, 1, 8, 2, 16, 0, FAKE, None, None) == SP_ERR_INVALID_ARG
+    assert m(FAKE, FAKE, 0, 1, 8, 2, 16, 0, FAKE, None, None) == SP_ERR_INVALID_ARG
+    assert m(FAKE, FAKE, 2, 1, 8, 2, 16, 9, FAKE, None, None) == SP_ERR_INVALID_ARG
+    s = lib.sp_segment_starts
+    assert s(None, FAKE, 1, 8, FAKE_WS, 1 << 12, None) == SP_ERR_INVALID_ARG
+    assert s(FAKE, FAKE, 1, 8, None, 1 << 12, None) == SP_ERR_WORKSPACE
+    assert s(FAKE, FAKE, 1, 8, FAKE_WS, 0, None) == SP_ERR_WORKSPACE
+    assert lib.sp_get_device_error(None, None, None) == SP_ERR_INVALID_ARG

@@ -1,0 +1,171 @@
+"""GPU parity of blockwise attention (fp32 CUDA-core and bf16 tcgen05 paths),
+of single ring steps and of the partial merge, against the float64 oracle on
+the same seeded inputs.  Sizes span several 128-row tiles, ragged tails,
+GQA, packed documents with length-1 documents, P from 1 to 16, both block
+orders."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import check_attention, np32, torch_dtype
+from sequence_parallelism_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sp():
+    import sequence_parallelism_gb300 as m
+    return m
+
+
+def _positions(kind, B, S, seed):
+    if kind == "none":
+        return None
+    if kind == "causal":
+        return np.tile(np.arange(S, dtype=np.int32), (B, 1))
+    rows = []
+    for b in range(B):  # packed documents, a few of length 1, not tile-aligned
+        rng = np.random.default_rng(seed + b)
+        cuts = np.sort(rng.choice(np.arange(1, S), 6, replace=False))
+        cuts = np.unique(np.concatenate([cuts, [cuts[0] + 1, S - 1]]))
+        lengths = np.diff(np.concatenate([[0], cuts, [S]]))
+        rows.append(workloads.position_ids_from_lengths(lengths))
+    return np.stack(rows).astype(np.int32)
+
+
+def _run(sp, dtype, B, S, Hq, Hkv, d, P, order, pos_kind, seed):
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, d, seed, dtype)
+    pos = _positions(pos_kind, B, S, seed)
+    tpos = None if pos is None else torch.from_numpy(pos).cuda()
+    out, lse = sp.blockwise_attention(q, k, v, P, order, tpos)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.full_attention(np32(q), np32(k), np32(v), pos)
+    return check_attention(np32(out), lse.cpu().numpy(), ref_out, ref_lse, dtype,
+                           f"{dtype} S={S} P={P} {order} {pos_kind}")
+
+
+def test_ring_tiny_f32(sp):
+    """The Ring Attention page's example: 4 blocks of 8 tokens, d = 16, fp32,
+    matches full attention within 1e-5 (the page's allclose tolerance)."""
+    qn, kn, vn = workloads.ring_tiny_arrays()
+    as4 = lambda a: torch.from_numpy(a)[None, :, None, :].contiguous().cuda()
+    q, k, v = as4(qn), as4(kn), as4(vn)
+    out, lse = sp.blockwise_attention(q, k, v, 4, "contiguous")
+    torch.cuda.synchronize()
+    as4n = lambda a: a.astype(np.float64)[None, :, None, :]
+    ref_out, ref_lse = oracle.full_attention(as4n(qn), as4n(kn), as4n(vn))
+    check_attention(np32(out), lse.cpu().numpy(), ref_out, ref_lse, "f32", "ring_tiny")
+    assert np.abs(np32(out) - ref_out).max() <= 1e-5
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,d,P,order,pos", [
+    (1, 32, 1, 1, 16, 1, "contiguous", "none"),
+    (2, 96, 4, 2, 64, 3, "contiguous", "causal"),
+    (2, 96, 4, 2, 64, 3, "striped", "packed"),
+    (1, 200, 3, 1, 100, 4, "striped", "causal"),
+    (1, 160, 2, 2, 256, 8, "contiguous", "packed"),
+    (1, 64, 2, 1, 7, 16, "striped", "none"),
+])
+def test_f32_parity(sp, B, S, Hq, Hkv, d, P, order, pos):
+    _run(sp, "f32", B, S, Hq, Hkv, d, P, order, pos, 100 + S)
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,P,order,pos", [
+    (1, 128, 1, 1, 1, "contiguous", "none"),      # one tile
+    (1, 1024, 2, 2, 1, "contiguous", "none"),     # 4 Q tiles, 8 KV tiles
+    (2, 1000, 4, 2, 2, "contiguous", "none"),     # ragged tail (500 rows per block), GQA
+    (1, 1200, 4, 1, 4, "striped", "none"),        # MQA, striped, ragged
+    (1, 2048, 4, 2, 4, "contiguous", "causal"),
+    (1, 2048, 4, 2, 4, "striped", "causal"),
+    (2, 1536, 2, 1, 2, "contiguous", "packed"),
+    (2, 1536, 2, 1, 3, "striped", "packed"),
+    (1, 4096, 2, 2, 16, "striped", "causal"),
+    (1, 4096, 2, 2, 16, "contiguous", "causal"),
+    (1, 768, 3, 3, 8, "contiguous", "packed"),    # blocks of 96 rows (< one tile)
+])
+def test_bf16_parity(sp, B, S, Hq, Hkv, P, order, pos):
+    _run(sp, "bf16", B, S, Hq, Hkv, 128, P, order, pos, 200 + S + P)
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 32)])
+@pytest.mark.parametrize("order", ["contiguous", "striped"])
+def test_ring_steps_merge_to_full(sp, dtype, d, order):
+    """Each ring step alone matches the oracle's per-step partial (rows with
+    no key in that block give 0 / -inf), and merging the P partials on the
+    GPU reproduces full attention."""
+    B, S, Hq, Hkv, P = 1, 1024, 2, 1, 4
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 300, dtype)
+    pos = _positions("packed", B, S, 300)
+    tpos = torch.from_numpy(pos).cuda()
+    qn, kn, vn = np32(q), np32(k), np32(v)
+    outs = torch.empty((P, B, S, Hq, d), dtype=torch_dtype(dtype), device="cuda")
+    lses = torch.empty((P, B, Hq, S), dtype=torch.float32, device="cuda")
+    for s in range(P):
+        sp.ring_step(q, k, v, P, s, order, tpos, out=outs[s], lse=lses[s])
+        torch.cuda.synchronize()
+        ro, rl = oracle.ring_partial(qn, kn, vn, P, s, order, pos)
+        check_attention(np32(outs[s]), lses[s].cpu().numpy(), ro, rl, dtype, f"step {s}")
+    out, lse = sp.merge_partials(outs, lses)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.full_attention(qn, kn, vn, pos)
+    check_attention(np32(out), lse.cpu().numpy(), ref_out, ref_lse, dtype, "merged")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_merge_partials_parity(sp, dtype):
+    P, B, S, H, d = 5, 2, 37, 3, 48
+    g = torch.Generator(device="cuda")
+    g.manual_seed(77)
+    outs = torch.randn((P, B, S, H, d), generator=g, device="cuda").to(torch_dtype(dtype))
+    lses = torch.randn((P, B, H, S), generator=g, device="cuda") * 3
+    lses[1, :, :, :5] = float("-inf")   # empty partials get weight 0
+    lses[:, 1, 2, 7] = float("-inf")    # a row with nothing at all
+    out, lse = sp.merge_partials(outs, lses)
+    torch.cuda.synchronize()
+    ro, rl = oracle.merge_partials(np32(outs).astype(np.float64), lses.cpu().numpy())
+    tol = 1e-5 if dtype == "f32" else 1e-2
+    assert np.abs(np32(out) - ro).max() <= tol
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isfinite(lse.cpu().numpy()), fin)
+    assert np.abs(lse.cpu().numpy()[fin] - rl[fin]).max() <= 1e-5
+    assert (np32(out)[1, 7, 2] == 0).all()
+
+
+def test_constant_values_give_ones(sp):
+    """v = 1: every softmax row sums to one (bf16 P rounding is the only
+    error)."""
+    B, S, Hq, Hkv = 1, 2048, 2, 1
+    q, k, _ = workloads.small_case(B, S, Hq, Hkv, 128, 400, "bf16")
+    v = torch.ones((B, S, Hkv, 128), dtype=torch.bfloat16, device="cuda")
+    pos = torch.from_numpy(_positions("packed", B, S, 400)).cuda()
+    out, _ = sp.blockwise_attention(q, k, v, 4, "striped", pos)
+    torch.cuda.synchronize()
+    assert np.abs(np32(out) - 1.0).max() <= 1e-2
+
+
+def test_zero_query_closed_form(sp):
+    """q = 0: out = mean of the allowed values, lse = ln(position + 1)."""
+    B, S, Hq, Hkv = 1, 1536, 2, 2
+    _, k, v = workloads.small_case(B, S, Hq, Hkv, 128, 401, "bf16")
+    q = torch.zeros((B, S, Hq, 128), dtype=torch.bfloat16, device="cuda")
+    pos = _positions("packed", B, S, 401)
+    out, lse = sp.blockwise_attention(q, k, v, 2, "contiguous", torch.from_numpy(pos).cuda())
+    torch.cuda.synchronize()
+    expect = np.log(pos[0].astype(np.float64) + 1.0)
+    assert np.abs(lse.cpu().numpy()[0] - expect[None, :]).max() <= 1e-3
+    ref_out, _ = oracle.full_attention(np32(q), np32(k), np32(v), pos)
+    assert np.abs(np32(out) - ref_out).max() <= 2e-2
+
+
+def test_no_device_error_reported(sp):
+    B, S = 1, 1024
+    q, k, v = workloads.small_case(B, S, 2, 2, 128, 402, "bf16")
+    ws = sp.attention_workspace(B, S, False)
+    sp.blockwise_attention(q, k, v, 2, "contiguous", workspace=ws)
+    from sequence_parallelism_gb300 import _lib
+    st, code = _lib.sp_get_device_error(ws)
+    assert st == 0 and code == 0
+    assert _lib.sp_last_launch_count() == 1

@@ -1,0 +1,105 @@
+"""GPU parity of the Ulysses permutation and of doc_start: bit-exact against
+the oracle's index loops / segment reading, through the C ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import npi
+from sequence_parallelism_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sp():
+    import sequence_parallelism_gb300 as m
+    return m
+
+
+def _rand_tensor(shape, dtype, seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    if dtype == torch.bfloat16 or dtype == torch.float32:
+        return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(dtype)
+    raise ValueError(dtype)
+
+
+@pytest.mark.parametrize("B,S,H,d,P,dtype", [
+    (1, 64, 8, 128, 4, torch.bfloat16),
+    (2, 42, 6, 16, 3, torch.float32),
+    (1, 12, 4, 3, 2, torch.bfloat16),     # 2-byte chunks: scalar path
+    (1, 10, 5, 7, 5, torch.float32),      # one head per group, 4-byte path
+    (3, 16, 16, 64, 1, torch.bfloat16),   # P = 1: plain reshape
+    (1, 32, 16, 128, 16, torch.bfloat16),  # P = H
+])
+def test_permutation_bit_exact(sp, B, S, H, d, P, dtype):
+    x = _rand_tensor((B, S, H, d), dtype, 11 + P)
+    y = sp.seq_to_head(x, P)
+    torch.cuda.synchronize()
+    bits = torch.int16 if dtype == torch.bfloat16 else torch.int32
+    ref = oracle.seq_to_head(npi(x.view(bits)), P)
+    assert np.array_equal(npi(y.view(bits)), ref)
+    back = sp.head_to_seq(y)
+    torch.cuda.synchronize()
+    assert torch.equal(back.view(bits), x.view(bits))
+    assert np.array_equal(npi(back.view(bits)), oracle.head_to_seq(ref))
+
+
+def test_permutation_full_size_ulysses(sp):
+    """ulysses_4k: q, k, v [1][4096][32][128] bf16, P = 4."""
+    cfg = workloads.CONFIGS["ulysses_4k"]
+    q, k, v = workloads.qkv_torch(cfg["B"], cfg["S"], cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["seed"],
+                                  torch.bfloat16, "cuda")
+    for t in (q, k, v):
+        y = sp.seq_to_head(t, cfg["P"])
+        torch.cuda.synchronize()
+        assert np.array_equal(npi(y.view(torch.int16)),
+                              oracle.seq_to_head(npi(t.view(torch.int16)), cfg["P"]))
+        assert torch.equal(sp.head_to_seq(y).view(torch.int16), t.view(torch.int16))
+
+
+def test_permutation_large_tensor_roundtrip(sp):
+    """A 256 MiB tensor (the llama8b_32k q shape) round-trips bit-exactly and
+    lands in the head-sharded slots the index formula names."""
+    x = _rand_tensor((1, 32768, 32, 128), torch.bfloat16, 5)
+    y = sp.seq_to_head(x, 8)
+    back = sp.head_to_seq(y)
+    torch.cuda.synchronize()
+    assert torch.equal(back.view(torch.int16), x.view(torch.int16))
+    rng = np.random.default_rng(3)
+    for _ in range(64):
+        r, t, hl = int(rng.integers(8)), int(rng.integers(32768)), int(rng.integers(4))
+        assert torch.equal(y[r, 0, t, hl].view(torch.int16), x[0, t, r * 4 + hl].view(torch.int16))
+
+
+def _doc_start_ref(pos):
+    return oracle.doc_starts(pos).astype(np.int32)
+
+
+@pytest.mark.parametrize("lengths", [[1], [5, 1, 7], [1023, 1, 1025, 2047], [3000, 1, 1, 96]])
+def test_doc_start_bit_exact(sp, lengths):
+    pos = np.stack([workloads.position_ids_from_lengths(lengths),
+                    workloads.position_ids_from_lengths(lengths[::-1])])
+    ds = sp.doc_starts(torch.from_numpy(pos).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(npi(ds), _doc_start_ref(pos))
+
+
+def test_doc_start_irregular_positions(sp):
+    rng = np.random.default_rng(9)
+    pos = rng.integers(0, 5, size=(3, 5000)).astype(np.int32)  # many restarts and repeats
+    pos[1] = np.arange(5000, dtype=np.int32) + 17               # one doc not starting at 0
+    ds = sp.doc_starts(torch.from_numpy(pos).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(npi(ds), _doc_start_ref(pos))
+
+
+@pytest.mark.parametrize("name", ["packed_128k", "halfmil_512k"])
+def test_doc_start_full_size(sp, name):
+    cfg = workloads.CONFIGS[name]
+    pos = workloads.position_ids(cfg)
+    ds = sp.doc_starts(torch.from_numpy(pos).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(npi(ds), _doc_start_ref(pos))
