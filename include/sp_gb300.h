@@ -176,6 +176,33 @@ sp_status sp_blockwise_attn_step(const void* q, const void* k, const void* v,
                                  void* out, float* lse, void* workspace, size_t workspace_bytes,
                                  sp_stream_t stream);
 
+/* sp_blockwise_attn_fwd without a workspace argument, for callers that
+ * cannot allocate device memory (code that must not call cudaMalloc, such as
+ * a host callback or a plugin hook, or a framework whose allocator only hands
+ * out the caller's own tensors).  The pages describe no such variant: it has
+ * no counterpart there.
+ *
+ * Same arguments, layouts, results and errors as sp_blockwise_attn_fwd,
+ * minus workspace / workspace_bytes.  The workspace is a fixed 5 MiB array
+ * with static storage on the device, held by every GPU that loads the
+ * library until the process exits.  Any non-causal call fits; a causal call
+ * needs sp_blockwise_attn_workspace_bytes(B, S, 1) <= 5 MiB, which holds for
+ * every B*S <= 1,048,576 tokens; larger requests return SP_ERR_WORKSPACE and
+ * launch nothing.  Allocates nothing (no cudaMalloc / cudaFree, no
+ * allocating library call).
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before capturing the stream into a CUDA graph.  All calls on a device share
+ * the array, which keeps the last call's contents (each call clears its error
+ * word and rewrites doc_start in full): calls whose kernels overlap on the
+ * GPU race on it.  The device error word of this variant cannot be read
+ * back. */
+sp_status sp_blockwise_attn_fwd_noalloc(const void* q, const void* k, const void* v,
+                                        const int32_t* position_ids, int B, int S, int Hq,
+                                        int Hkv, int d, int P, sp_block_order order, float scale,
+                                        sp_dtype dtype, void* out, float* lse, sp_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Merge of per-block partial results (the cross-device combine of ring
  * attention, "Ring Attention", "Cómo funciona la atención en anillo").

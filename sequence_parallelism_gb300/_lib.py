@@ -25,7 +25,8 @@ _ORDERS = {"contiguous": SP_ORDER_CONTIGUOUS, "striped": SP_ORDER_STRIPED}
 EXPORTS = (
     "sp_status_string", "sp_ulysses_seq_to_head", "sp_ulysses_head_to_seq",
     "sp_segment_starts_workspace_bytes", "sp_segment_starts", "sp_blockwise_attn_workspace_bytes",
-    "sp_blockwise_attn_fwd", "sp_blockwise_attn_step", "sp_attn_merge_partials",
+    "sp_blockwise_attn_fwd", "sp_blockwise_attn_step", "sp_blockwise_attn_fwd_noalloc",
+    "sp_attn_merge_partials",
     "sp_get_device_error", "sp_last_launch_count",
 )
 
@@ -52,6 +53,8 @@ def _load():
                                       vp]),
         "sp_blockwise_attn_step": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp,
                                        sz, vp]),
+        "sp_blockwise_attn_fwd_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, vp,
+                                              vp]),
         "sp_attn_merge_partials": (i, [vp, vp, i, i, i, i, i, i, vp, vp, vp]),
         "sp_get_device_error": (i, [vp, ctypes.POINTER(ctypes.c_int), vp]),
         "sp_last_launch_count": (i, []),
@@ -146,6 +149,18 @@ def sp_blockwise_attn_fwd(q, k, v, position_ids, P, order, scale, out, lse, work
         _ptr(q), _ptr(k), _ptr(v), _ptr(position_ids), B, S, Hq, Hkv, d, P, _ORDERS[order],
         float(scale), _dtype(q), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse
+
+
+def sp_blockwise_attn_fwd_noalloc(q, k, v, position_ids, P, order, scale, out, lse, stream=None):
+    """sp_blockwise_attn_fwd with the library's built-in device scratch, for
+    callers that cannot allocate device memory (no workspace argument)."""
+    _dense(q, k, v, position_ids, out, lse)
+    B, S, Hq, d = q.shape
+    Hkv = k.shape[2]
+    _check("sp_blockwise_attn_fwd_noalloc", _lib.sp_blockwise_attn_fwd_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(position_ids), B, S, Hq, Hkv, d, P, _ORDERS[order],
+        float(scale), _dtype(q), _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse
 
 
