@@ -1,6 +1,6 @@
 """Compile the CUDA library in-tree for sm_103a.
 
-    python -m sequence_parallelism_gb300.build
+    python sequence_parallelism_gb300/build.py     (or __graft_entry__.build())
 
 Every translation unit under csrc/ is compiled by nvcc in parallel into
 _build/, then linked into sequence_parallelism_gb300/libsp_gb300.so (CUDA
