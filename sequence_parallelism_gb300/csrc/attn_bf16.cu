@@ -264,17 +264,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t tS[2] = {tmem + 0, tmem + 128};
       const uint32_t tO[2] = {tmem + 256, tmem + 384};
+      // Descriptors are built once; a k-step only adds its byte offset >> 4
+      // to the start-address field (all addresses stay below 256 KiB, so the
+      // 14-bit field never carries).
+      const uint64_t dq0 = smem_desc_sw128(smem_q, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(smem_kv, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(smem_kv, kHalfBytes, 1024);
       // S_t = Q_t K^T over d = 128: 8 k-steps of 16, 32 bytes apart inside a
       // 128-byte swizzled row, the second 64 columns in the next half tile.
       auto issue_s = [&](int t, int load_idx) {
-        const int slot = load_idx % kSlots;
-        const uint32_t qa = smem_q + t * kTileBytes;
-        const uint32_t kb = smem_kv + slot * kTileBytes;
+        const uint64_t qa = dq0 + ((t * kTileBytes) >> 4);
+        const uint64_t kb = dk0 + (((load_idx % kSlots) * kTileBytes) >> 4);
+        const uint32_t d = tmem + t * 128;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_ss(tS[t], smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
-                 kIdescQK, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_ss(d, qa + off, kb + off, kIdescQK, kk > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&bars.s_full[t]));
       };
@@ -282,12 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // MN-major: 16 keys = 2 swizzle atoms of 8 rows (stride 1024 B), the
       // two 64-column halves of d 16 KiB apart.
       auto issue_pv = [&](int t, int it, int slot) {
+        const uint64_t vb = dv0 + ((slot * kTileBytes) >> 4);
+        const uint32_t d = tmem + 256 + t * 128;
+        const uint32_t pa = tmem + t * 128;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t vb = smem_kv + slot * kTileBytes + kk * 16 * 128;
-          mma_ts(tO[t], tS[t] + kk * 8, smem_desc_sw128(vb, kHalfBytes, 1024), kIdescPV,
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(d, pa + kk * 8, vb + ((kk * 16 * 128) >> 4), kIdescPV,
                  (it > 0 || kk > 0) ? 1u : 0u);
-        }
       };
       if (ok) ok = mbar_wait(smem_u32(&bars.kv_full[0]), 0, abort_flag, a.err, kErrKvFull);
       tc_fence_after();
@@ -329,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(smem_u32(&bars.done), 0, abort_flag, a.err, kErrDrain);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 2 * 4) {
     // ------------------------------------------------- softmax warpgroups
     const int t = warp >> 2;           // Q tile of this group
     const int row = threadIdx.x & 127;  // TMEM lane == row of the tile
@@ -363,38 +369,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        float x[kBN];
-        {
-          uint32_t r[32];
+        // the whole score row: four 32-column loads in flight, one wait
+        uint32_t x[kBN];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            tmem_ld32(tS + c * 32, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(r[e]);
-          }
-        }
+        for (int c = 0; c < 4; ++c) tmem_ld32_at(tS + c * 32, x, c * 32);
+        tmem_wait_ld();
         // allowed columns [c_lo, c_hi] of this tile for this row
-        long long c_lo, c_hi;
-        const long long w_base = static_cast<long long>(kt) * kBN;
-        if (a.order == SP_ORDER_STRIPED) {
-          c_lo = -floor_div(-(lo - j), a.P) - w_base;
-          c_hi = floor_div(hi - j, a.P) - w_base;
-        } else {
-          const long long base = static_cast<long long>(j) * Lb + w_base;
-          c_lo = lo - base;
-          c_hi = hi - base;
+        int c_lo, c_hi;
+        {
+          long long lo_c, hi_c;
+          const long long w_base = static_cast<long long>(kt) * kBN;
+          if (a.order == SP_ORDER_STRIPED) {
+            lo_c = -floor_div(-(lo - j), a.P) - w_base;
+            hi_c = floor_div(hi - j, a.P) - w_base;
+          } else {
+            const long long base = static_cast<long long>(j) * Lb + w_base;
+            lo_c = lo - base;
+            hi_c = hi - base;
+          }
+          const long long c_valid = static_cast<long long>(Lb) - w_base - 1;
+          if (hi_c > c_valid) hi_c = c_valid;
+          c_lo = static_cast<int>(lo_c < 0 ? 0 : (lo_c > kBN ? kBN : lo_c));
+          c_hi = static_cast<int>(hi_c < -1 ? -1 : (hi_c > kBN - 1 ? kBN - 1 : hi_c));
         }
-        const long long c_valid = static_cast<long long>(Lb) - w_base - 1;
-        if (c_hi > c_valid) c_hi = c_valid;
         if (c_lo > 0 || c_hi < kBN - 1) {
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
-            if (c < c_lo || c > c_hi) x[c] = -INFINITY;
+            if (c < c_lo || c > c_hi) x[c] = 0xff800000u;  // -inf
         }
-        float mt = x[0];
+        // row max: 8 independent chains of 3-input max
+        float mx[8];
 #pragma unroll
-        for (int c = 1; c < kBN; ++c) mt = fmaxf(mt, x[c]);
+        for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(x[k]);
+#pragma unroll
+        for (int c = 8; c < kBN - 8; c += 16) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mx[k] = fmax3(mx[k], __uint_as_float(x[c + k]), __uint_as_float(x[c + 8 + k]));
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(x[kBN - 8 + k]));
+        const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                               fmaxf(mx[6], mx[7]));
         m_run = fmaxf(m_run, mt * scale_log2);
         float alpha = 1.f;
         bool rescale = false;
@@ -405,6 +421,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_use = m_run;
           rescale = true;
         }
+        const float nbase = (m_use == -INFINITY) ? 0.f : -m_use;
+        // p = 2^(s * scale_log2 - base), two lanes per FFMA; 4 pair sums
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < kBN; c += 2) {
+          float e0, e1;
+          ffma2(e0, e1, __uint_as_float(x[c]), __uint_as_float(x[c + 1]), scale_log2, scale_log2,
+                nbase, nbase);
+          e0 = ex2(e0);
+          e1 = ex2(e1);
+          const int k = (c >> 1) & 3;
+          fadd2(sa[k], sb[k], sa[k], sb[k], e0, e1);
+          x[c >> 1] = pack_bf16(e0, e1);  // P row, packed in place (c/2 <= c)
+        }
+        l = l * alpha + ((sa[0] + sb[0]) + (sa[1] + sb[1])) + ((sa[2] + sb[2]) + (sa[3] + sb[3]));
+        tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+        // O *= alpha in TMEM (after the scores are dead, to keep registers
+        // free); the PV MMA that adds this tile waits for p_full below.
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -415,21 +450,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
             tmem_st32(tO + c * 32, r);
           }
-        }
-        const float base = (m_use == -INFINITY) ? 0.f : m_use;
-        float sum = 0.f;
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          x[c] = ex2(fmaf(x[c], scale_log2, -base));
-          sum += x[c];
-        }
-        l = l * alpha + sum;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t r[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = pack_bf16(x[c * 64 + 2 * e], x[c * 64 + 2 * e + 1]);
-          tmem_st32(tS + c * 32, r);
         }
         tmem_wait_st();
         tc_fence_before();
