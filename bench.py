@@ -41,7 +41,7 @@ METRIC = ("causal blockwise-attention TFLOP/s (% BF16 peak); seq↔head permute 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # kernel from the committed ncu capture (None until taken for this kernel).
-NCU_TRAFFIC_BYTES = {}
+NCU_TRAFFIC_BYTES = {"ulysses_4k": 239.64e6, "llama8b_32k": 2095.89e6}
 
 
 def load_peaks():
@@ -377,56 +377,62 @@ def extra_measurements(args, peaks):
 
 
 # ------------------------------------------------------- CPU oracle leg
-def _oracle_sample(cfg, workload, order, rows):
-    """One bounded sample of the workload through the oracle; returns
-    (algorithmic FLOPs done, seconds)."""
-    import oracle
+def _oracle_inputs(cfg):
     from sequence_parallelism_gb300 import workloads
-
-    B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
+    B, S, Hq, Hkv, d = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d"))
     rng = np.random.default_rng(cfg["seed"])
     q = rng.standard_normal((B, S, Hq, d)).astype(np.float32)
     k = rng.standard_normal((B, S, Hkv, d)).astype(np.float32)
     v = rng.standard_normal((B, S, Hkv, d)).astype(np.float32)
-    pos = workloads.position_ids(cfg)
+    return q, k, v, workloads.position_ids(cfg)
+
+
+def _oracle_sample(cfg, order, rows, inputs):
+    """One bounded sample of the workload through the oracle (inputs drawn
+    beforehand); returns (algorithmic FLOPs done, seconds)."""
+    import oracle
+    from sequence_parallelism_gb300 import workloads
+
+    B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
+    q, k, v, pos = inputs
     sel = workloads.sample_rows(S, P, rows, cfg["seed"], order)
     t0 = time.perf_counter()
     if cfg.get("ulysses"):
         yq, yk, yv = (oracle.seq_to_head(t, P) for t in (q, k, v))
         G = Hq // P
-        outs = []
-        for r in range(P):
-            o, _ = oracle.attention_rows(yq[r], yk[r], yv[r], sel, None)
-            outs.append(o)
         full = np.zeros((P, B, S, G, d))
         for r in range(P):
-            full[r][:, sel] = outs[r]
+            o, _ = oracle.attention_rows(yq[r], yk[r], yv[r], sel, None)
+            full[r][:, sel] = o
         oracle.head_to_seq(full)
         fl = 4.0 * d * S * len(sel) * Hq * B
     else:
         oracle.attention_rows(q, k, v, sel, pos)
-        seg = oracle.segment_ids(pos)
-        starts = oracle.doc_starts(pos) if S <= 200000 else None
-        if starts is not None:
-            allowed = (sel - starts[0, sel] + 1).astype(np.float64)
-        else:  # plain causal
-            allowed = (sel + 1).astype(np.float64)
-        del seg
-        fl = 4.0 * d * float(allowed.sum()) * Hq * B
+        sec = time.perf_counter() - t0
+        starts = oracle.doc_starts(pos[:, :int(sel.max()) + 1])
+        allowed = (sel - starts[0, sel] + 1).astype(np.float64)
+        return 4.0 * d * float(allowed.sum()) * Hq * B, sec
     return fl, time.perf_counter() - t0
 
 
+def _calibrated_rows(cfg, order, inputs, seconds):
+    """Rows whose oracle time is about `seconds`: t(rows) = a + b * rows from
+    two small samples."""
+    _, t1 = _oracle_sample(cfg, order, 8, inputs)
+    _, t2 = _oracle_sample(cfg, order, 40, inputs)
+    b = max((t2 - t1) / 32.0, 1e-6)
+    a = max(t1 - 8 * b, 0.0)
+    return int(max(1, min(cfg["S"], (seconds - a) / b)))
+
+
 def cpu_baseline(cfg, workload, order, budget_s=15.0):
-    rows = 8
-    fl, sec = _oracle_sample(cfg, workload, order, rows)
-    # grow the sample to about budget_s of CPU work
-    target = int(rows * budget_s / max(sec, 1e-3))
-    rows = max(rows, min(target, cfg["S"]))
-    fl, sec = _oracle_sample(cfg, workload, order, rows)
+    inputs = _oracle_inputs(cfg)
+    rows = _calibrated_rows(cfg, order, inputs, budget_s)
+    fl, sec = _oracle_sample(cfg, order, rows, inputs)
     return {"value": round(fl / sec / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
             "kind": "oracle",
             "sample": f"{workload}: {rows} seeded query rows x all heads "
-                      f"(float64 NumPy oracle{', plus full permutations' if cfg.get('ulysses') else ''}),"
+                      f"(float64 NumPy oracle{', plus full q/k/v/out permutations' if cfg.get('ulysses') else ''}),"
                       f" {sec:.1f} s; BLAS threads = library default (all cores)",
             "seconds": round(sec, 2)}
 
@@ -439,14 +445,14 @@ def run_reference(args, rank, world):
     from sequence_parallelism_gb300 import workloads
     cfg = dict(workloads.CONFIGS[args.workload])
     order = cfg["orders"][-1] if args.order is None else args.order
-    fl1, s1 = _oracle_sample(cfg, args.workload, order, 8)
+    inputs = _oracle_inputs(cfg)
     per_step = 120.0 / max(1, args.steps + args.warmup)
-    rows = max(1, int(8 * per_step / max(s1, 1e-3)))
+    rows = _calibrated_rows(cfg, order, inputs, per_step)
     for _ in range(args.warmup):
-        _oracle_sample(cfg, args.workload, order, rows)
+        _oracle_sample(cfg, order, rows, inputs)
     tot_fl, tot_s = 0.0, 0.0
     for _ in range(args.steps):
-        fl, s = _oracle_sample(cfg, args.workload, order, rows)
+        fl, s = _oracle_sample(cfg, order, rows, inputs)
         tot_fl += fl
         tot_s += s
     value = tot_fl / tot_s / 1e12
@@ -472,7 +478,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-extra", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
