@@ -70,24 +70,25 @@ struct Tmaps {
   CUtensorMap q, k, v;
 };
 
-__device__ __forceinline__ long long floor_div(long long a, long long b) {
+// Token indices fit in int (S is an int), so the schedule works in 32 bits.
+__device__ __forceinline__ int floor_div(int a, int b) {
   return a >= 0 ? a / b : -((-a + b - 1) / b);
 }
 
 // The part of the ring schedule every role must agree on.
 struct Schedule {
   int i, P, Lb, S, order, step_begin, step_end;
-  long long hull_lo, hull_hi;  // key-token interval any row of the CTA may use
+  int hull_lo, hull_hi;  // key-token interval any row of the CTA may use
 
   // KV tiles [kt0, kt1] of block j that intersect the hull (kt1 < kt0: none)
   __device__ __forceinline__ void tiles(int s, int& j, int& kt0, int& kt1) const {
     j = ((i - s) % P + P) % P;
-    long long w_lo, w_hi;
+    int w_lo, w_hi;
     if (order == SP_ORDER_STRIPED) {
       w_lo = -floor_div(-(hull_lo - j), P);  // ceil((lo - j) / P)
       w_hi = floor_div(hull_hi - j, P);
     } else {
-      const long long base = static_cast<long long>(j) * Lb;
+      const int base = j * Lb;
       w_lo = hull_lo - base;
       w_hi = hull_hi - base;
     }
@@ -163,8 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   sch.step_end = a.step_end;
   {
     const int u_last = min(u0 + kRowsPerCta, Lb) - 1;
-    const long long t_first = block_token(a.order, a.S, a.P, i, u0);
-    const long long t_last = block_token(a.order, a.S, a.P, i, u_last);
+    const int t_first = static_cast<int>(block_token(a.order, a.S, a.P, i, u0));
+    const int t_last = static_cast<int>(block_token(a.order, a.S, a.P, i, u_last));
     if (a.doc_start) {
       sch.hull_lo = a.doc_start[static_cast<long long>(b) * a.S + t_first];
       sch.hull_hi = t_last;
@@ -344,8 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_base + 256 + t * 128;
     const int u = u0 + t * kBM + row;  // local row in block i
     const bool row_live = u < Lb;
-    const long long tq = row_live ? block_token(a.order, a.S, a.P, i, u) : 0;
-    long long lo, hi;
+    const int tq = row_live ? static_cast<int>(block_token(a.order, a.S, a.P, i, u)) : 0;
+    int lo, hi;
     if (a.doc_start && row_live) {
       lo = a.doc_start[static_cast<long long>(b) * a.S + tq];
       hi = tq;
@@ -377,20 +378,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // allowed columns [c_lo, c_hi] of this tile for this row
         int c_lo, c_hi;
         {
-          long long lo_c, hi_c;
-          const long long w_base = static_cast<long long>(kt) * kBN;
+          int lo_c, hi_c;
+          const int w_base = kt * kBN;
           if (a.order == SP_ORDER_STRIPED) {
             lo_c = -floor_div(-(lo - j), a.P) - w_base;
             hi_c = floor_div(hi - j, a.P) - w_base;
           } else {
-            const long long base = static_cast<long long>(j) * Lb + w_base;
+            const int base = j * Lb + w_base;
             lo_c = lo - base;
             hi_c = hi - base;
           }
-          const long long c_valid = static_cast<long long>(Lb) - w_base - 1;
+          const int c_valid = Lb - w_base - 1;
           if (hi_c > c_valid) hi_c = c_valid;
-          c_lo = static_cast<int>(lo_c < 0 ? 0 : (lo_c > kBN ? kBN : lo_c));
-          c_hi = static_cast<int>(hi_c < -1 ? -1 : (hi_c > kBN - 1 ? kBN - 1 : hi_c));
+          c_lo = lo_c < 0 ? 0 : (lo_c > kBN ? kBN : lo_c);
+          c_hi = hi_c < -1 ? -1 : (hi_c > kBN - 1 ? kBN - 1 : hi_c);
         }
         if (c_lo > 0 || c_hi < kBN - 1) {
 #pragma unroll
