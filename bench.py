@@ -72,6 +72,28 @@ def attention_flops(cfg, pos):
     return 4.0 * d * pairs * Hq * B
 
 
+# ------------------------------------------------------ multi-rank logic
+def rank_seed(seed, rank):
+    """Each rank draws its own replica of the workload (weak scaling)."""
+    return seed + 7919 * rank
+
+
+def max_over_ranks(value, world, device=None):
+    """Slowest rank's value (the job takes as long as its slowest rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step, world, steps, max_ms):
+    """Whole-job throughput: every rank's FLOPs over the slowest rank's time."""
+    return flops_per_step * world * steps / (max_ms * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -137,7 +159,8 @@ def run_ours(args, rank, world, local_rank):
     order = cfg["orders"][-1] if args.order is None else args.order
     if cfg["dtype"] != "bf16":
         raise SystemExit("bench.py times the bf16 tensor-core path")
-    q, k, v = workloads.qkv_torch(B, S, Hq, Hkv, d, cfg["seed"] + 7919 * rank, torch.bfloat16, dev)
+    q, k, v = workloads.qkv_torch(B, S, Hq, Hkv, d, rank_seed(cfg["seed"], rank), torch.bfloat16,
+                                  dev)
     pos_np = workloads.position_ids(cfg)
     pos = None if pos_np is None else torch.from_numpy(pos_np).to(dev)
     flops = attention_flops(cfg, pos_np)
@@ -228,14 +251,9 @@ def run_ours(args, rank, world, local_rank):
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
     perm_ms = [e[0].elapsed_time(e[1]) for e in evs]
     inv_ms = [e[2].elapsed_time(e[3]) for e in evs]
-    tot_ms = float(sum(step_ms))
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([tot_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = max_over_ranks(float(sum(step_ms)), world, dev)
     ms_per_step = tot_ms / args.steps
-    value = flops * world * args.steps / (tot_ms * 1e-3) / 1e12
+    value = job_tflops(flops, world, args.steps, tot_ms)
 
     peaks, peak_kind = load_peaks()
     attn_mean = statistics.mean(attn_ms)
@@ -303,15 +321,10 @@ def e2e(args, step_inputs, out, step, flops, world, dev):
         hout.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     h2d = sum(t.numel() * t.element_size() for t in step_inputs)
     d2h = out.numel() * out.element_size()
-    return {"value": round(flops * world * n / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    return {"value": round(job_tflops(flops, world, n, ms), 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(ms / n, 4), "steps": n}
 

@@ -176,6 +176,35 @@ sp_status sp_blockwise_attn_step(const void* q, const void* k, const void* v,
                                  void* out, float* lse, void* workspace, size_t workspace_bytes,
                                  sp_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Ulysses + Ring hybrid, for fewer heads than devices.
+ *
+ * Ulysses needs num_heads >= sp_size ("Ulysses SP: entrenar modelos con
+ * millones de tokens", "Comparación práctica: Ulysses vs Ring Attention");
+ * "Ulysses SPで100万トークン学習" section 6 points to a Ulysses + Ring hybrid
+ * when GQA/MQA leaves too few heads.  With P = P_u * P_r simulated devices:
+ *   1. sp_ulysses_seq_to_head of q, k, v with P_u head groups;
+ *   2. blockwise ring attention with P_r blocks inside every head group
+ *      (batch P_u * B; every group uses the same B rows of position_ids);
+ *   3. sp_ulysses_head_to_seq of the output.
+ * q [B][S][Hq][d], k/v [B][S][Hkv][d], out [B][S][Hq][d] (sequence-sharded
+ * layout in and out); lse (may be NULL) in the head-sharded layout
+ * [P_u][B][Hq/P_u][S] float32 -- what each Ulysses group holds.
+ * Requires S % P_u == 0, S % P_r == 0, Hq % P_u == 0, Hkv % P_u == 0,
+ * Hq % Hkv == 0 (SP_ERR_INVALID_ARG otherwise); the dtype/d support of
+ * sp_blockwise_attn_fwd.  workspace: at least
+ * sp_ulysses_ring_attn_workspace_bytes(...) bytes, 256-byte aligned (it holds
+ * the head-sharded copies of q, k, v and of the output, and the attention
+ * workspace).
+ * ------------------------------------------------------------------------ */
+size_t sp_ulysses_ring_attn_workspace_bytes(int B, int S, int Hq, int Hkv, int d, int causal,
+                                            sp_dtype dtype);
+sp_status sp_ulysses_ring_attn_fwd(const void* q, const void* k, const void* v,
+                                   const int32_t* position_ids, int B, int S, int Hq, int Hkv,
+                                   int d, int P_u, int P_r, sp_block_order order, float scale,
+                                   sp_dtype dtype, void* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, sp_stream_t stream);
+
 /* sp_blockwise_attn_fwd without a workspace argument, for callers that
  * cannot allocate device memory (code that must not call cudaMalloc, such as
  * a host callback or a plugin hook, or a framework whose allocator only hands

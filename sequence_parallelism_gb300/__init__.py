@@ -10,6 +10,7 @@ without the built library raises ImportError -- there is no CPU path.
     ring_step(q, k, v, P, step, ...)           one ring step's partial result
     merge_partials(outs, lses)                 log-sum-exp combine of partials
     ulysses_attention(q, k, v, P, ...)         permute -> attention -> permute back
+    ulysses_ring_attention(q, k, v, P_u, P_r)  Ulysses + Ring hybrid (heads < devices)
     doc_starts(position_ids)                   O(n) causal-mask carrier
 """
 
@@ -19,7 +20,8 @@ from . import _lib
 from ._lib import SPError  # noqa: F401
 
 __all__ = ["seq_to_head", "head_to_seq", "blockwise_attention", "ring_step", "merge_partials",
-           "ulysses_attention", "doc_starts", "attention_workspace", "SPError"]
+           "ulysses_attention", "ulysses_ring_attention", "doc_starts", "attention_workspace",
+           "SPError"]
 
 
 def seq_to_head(x, P, out=None):
@@ -86,16 +88,41 @@ def doc_starts(position_ids):
     return _lib.sp_segment_starts(position_ids, ds, ws)
 
 
-def ulysses_attention(q, k, v, P, ring_blocks=None, order="contiguous", scale=0.0):
+def ulysses_attention(q, k, v, P, ring_blocks=None, order="contiguous", scale=0.0, fused=False):
     """One Ulysses attention layer simulated on one GPU.
 
     q [B][S][Hq][d], k/v [B][S][Hkv][d] in sequence-sharded layout: permute to
     head groups ([P][B][S][H/P][d] = batch P*B), run blockwise attention with
     `ring_blocks` blocks per head group (default P), permute back.  Non-causal.
+
+    fused=True skips both permutations: on one GPU, attention on the
+    sequence-sharded tensors computes every head group's result in place and
+    writes the output already in sequence-sharded layout (bit-identical).
     """
     B, S, Hq, d = q.shape
+    if fused:
+        out, _ = blockwise_attention(q, k, v, ring_blocks or P, order, None, scale)
+        return out
     yq, yk, yv = seq_to_head(q, P), seq_to_head(k, P), seq_to_head(v, P)
     G, Gk = Hq // P, k.shape[2] // P
     yo, _ = blockwise_attention(yq.view(P * B, S, G, d), yk.view(P * B, S, Gk, d),
                                 yv.view(P * B, S, Gk, d), ring_blocks or P, order, None, scale)
     return head_to_seq(yo.view(P, B, S, G, d))
+
+
+def ulysses_ring_attention(q, k, v, P_u, P_r, order="contiguous", position_ids=None, scale=0.0,
+                           out=None, lse=None, workspace=None):
+    """Ulysses + Ring hybrid: P_u head groups x P_r ring blocks; returns
+    (out [B][S][Hq][d], lse [P_u][B][Hq/P_u][S])."""
+    B, S, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((P_u, B, Hq // P_u, S), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = _lib.sp_ulysses_ring_attn_workspace_bytes(B, S, Hq, Hkv, d, position_ids is not None,
+                                                      _lib._dtype(q))
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    return _lib.sp_ulysses_ring_attn_fwd(q, k, v, position_ids, P_u, P_r, order, scale, out, lse,
+                                         workspace)

@@ -26,6 +26,7 @@ EXPORTS = (
     "sp_status_string", "sp_ulysses_seq_to_head", "sp_ulysses_head_to_seq",
     "sp_segment_starts_workspace_bytes", "sp_segment_starts", "sp_blockwise_attn_workspace_bytes",
     "sp_blockwise_attn_fwd", "sp_blockwise_attn_step", "sp_blockwise_attn_fwd_noalloc",
+    "sp_ulysses_ring_attn_workspace_bytes", "sp_ulysses_ring_attn_fwd",
     "sp_attn_merge_partials",
     "sp_get_device_error", "sp_last_launch_count",
 )
@@ -55,6 +56,9 @@ def _load():
                                        sz, vp]),
         "sp_blockwise_attn_fwd_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, vp,
                                               vp]),
+        "sp_ulysses_ring_attn_workspace_bytes": (sz, [i, i, i, i, i, i, i]),
+        "sp_ulysses_ring_attn_fwd": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp,
+                                         sz, vp]),
         "sp_attn_merge_partials": (i, [vp, vp, i, i, i, i, i, i, vp, vp, vp]),
         "sp_get_device_error": (i, [vp, ctypes.POINTER(ctypes.c_int), vp]),
         "sp_last_launch_count": (i, []),
@@ -172,6 +176,24 @@ def sp_blockwise_attn_step(q, k, v, position_ids, P, order, step, scale, out, ls
     _check("sp_blockwise_attn_step", _lib.sp_blockwise_attn_step(
         _ptr(q), _ptr(k), _ptr(v), _ptr(position_ids), B, S, Hq, Hkv, d, P, _ORDERS[order], step,
         float(scale), _dtype(q), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse
+
+
+def sp_ulysses_ring_attn_workspace_bytes(B, S, Hq, Hkv, d, causal, dtype):
+    return _lib.sp_ulysses_ring_attn_workspace_bytes(B, S, Hq, Hkv, d, int(bool(causal)), dtype)
+
+
+def sp_ulysses_ring_attn_fwd(q, k, v, position_ids, P_u, P_r, order, scale, out, lse, workspace,
+                             stream=None):
+    """Ulysses (P_u head groups) + ring (P_r blocks) hybrid; lse in the
+    head-sharded layout [P_u][B][Hq/P_u][S]."""
+    _dense(q, k, v, position_ids, out, lse, workspace)
+    B, S, Hq, d = q.shape
+    Hkv = k.shape[2]
+    _check("sp_ulysses_ring_attn_fwd", _lib.sp_ulysses_ring_attn_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(position_ids), B, S, Hq, Hkv, d, P_u, P_r,
+        _ORDERS[order], float(scale), _dtype(q), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse
 

@@ -4,7 +4,8 @@
 //
 // Workspace layout (256-byte aligned, caller-owned):
 //   [0, 256)                   error word (int32) + reserved
-//   [256, 256 + B*S*4)         doc_start [B][S] int32     (causal only)
+//   [256, 256 + R*S*4)         doc_start [R][S] int32     (causal only; R rows of
+//                              position_ids, R = B except in the Ulysses+Ring call)
 //   [.., + scan scratch)       per-chunk maxima of the doc_start scan
 #include <cuda_runtime.h>
 #include <math.h>
@@ -33,10 +34,12 @@ size_t doc_start_bytes(int B, int S) {
   return round_up(static_cast<size_t>(B) * static_cast<size_t>(S) * sizeof(int32_t), 256);
 }
 
-sp_status attn(const void* q, const void* k, const void* v, const int32_t* position_ids, int B,
-               int S, int Hq, int Hkv, int d, int P, sp_block_order order, int step_begin,
-               int step_end, float scale, sp_dtype dtype, void* out, float* lse, void* workspace,
-               size_t workspace_bytes, sp_stream_t stream) {
+}  // namespace
+
+sp_status attn(const void* q, const void* k, const void* v, const int32_t* position_ids,
+               int pos_rows, int B, int S, int Hq, int Hkv, int d, int P, sp_block_order order,
+               int step_begin, int step_end, float scale, sp_dtype dtype, void* out, float* lse,
+               void* workspace, size_t workspace_bytes, sp_stream_t stream) {
   g_last_launches = 0;
   if (!q || !k || !v || !out) return SP_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || d < 1 || P < 1) return SP_ERR_INVALID_ARG;
@@ -54,9 +57,10 @@ sp_status attn(const void* q, const void* k, const void* v, const int32_t* posit
     const long long pairs = (S / P + 255) / 256;
     if (static_cast<long long>(B) * Hq * P * pairs > 0x7fffffffLL) return SP_ERR_UNSUPPORTED;
   }
+  if (pos_rows < 1 || B % pos_rows != 0) return SP_ERR_INVALID_ARG;
   const int causal = position_ids != nullptr;
   if (!workspace || !aligned(workspace, 256) ||
-      workspace_bytes < sp_blockwise_attn_workspace_bytes(B, S, causal))
+      workspace_bytes < sp_blockwise_attn_workspace_bytes(pos_rows, S, causal))
     return SP_ERR_WORKSPACE;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -67,8 +71,8 @@ sp_status attn(const void* q, const void* k, const void* v, const int32_t* posit
   if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return SP_ERR_CUDA;
   if (causal) {
     doc_start = reinterpret_cast<int32_t*>(ws + kWsHeaderBytes);
-    void* scan = ws + kWsHeaderBytes + doc_start_bytes(B, S);
-    const int n = launch_segment_starts(position_ids, doc_start, B, S, scan, st);
+    void* scan = ws + kWsHeaderBytes + doc_start_bytes(pos_rows, S);
+    const int n = launch_segment_starts(position_ids, doc_start, pos_rows, S, scan, st);
     if (n < 0) return SP_ERR_CUDA;
     launches += n;
   }
@@ -81,6 +85,7 @@ sp_status attn(const void* q, const void* k, const void* v, const int32_t* posit
   a.lse = lse;
   a.err = err;
   a.B = B;
+  a.pos_rows = pos_rows;
   a.S = S;
   a.Hq = Hq;
   a.Hkv = Hkv;
@@ -96,7 +101,6 @@ sp_status attn(const void* q, const void* k, const void* v, const int32_t* posit
   return SP_OK;
 }
 
-}  // namespace
 }  // namespace sp
 
 extern "C" const char* sp_status_string(sp_status s) {
@@ -124,8 +128,8 @@ extern "C" sp_status sp_blockwise_attn_fwd(const void* q, const void* k, const v
                                            float scale, sp_dtype dtype, void* out, float* lse,
                                            void* workspace, size_t workspace_bytes,
                                            sp_stream_t stream) {
-  return sp::attn(q, k, v, position_ids, B, S, Hq, Hkv, d, P, order, 0, P, scale, dtype, out, lse,
-                  workspace, workspace_bytes, stream);
+  return sp::attn(q, k, v, position_ids, B, B, S, Hq, Hkv, d, P, order, 0, P, scale, dtype, out,
+                  lse, workspace, workspace_bytes, stream);
 }
 
 extern "C" sp_status sp_blockwise_attn_step(const void* q, const void* k, const void* v,
@@ -136,8 +140,8 @@ extern "C" sp_status sp_blockwise_attn_step(const void* q, const void* k, const 
                                             sp_stream_t stream) {
   sp::g_last_launches = 0;
   if (step < 0 || step >= P) return SP_ERR_INVALID_ARG;
-  return sp::attn(q, k, v, position_ids, B, S, Hq, Hkv, d, P, order, step, step + 1, scale, dtype,
-                  out, lse, workspace, workspace_bytes, stream);
+  return sp::attn(q, k, v, position_ids, B, B, S, Hq, Hkv, d, P, order, step, step + 1, scale,
+                  dtype, out, lse, workspace, workspace_bytes, stream);
 }
 
 extern "C" sp_status sp_get_device_error(void* workspace, int* code, sp_stream_t stream) {

@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t_first = static_cast<int>(block_token(a.order, a.S, a.P, i, u0));
     const int t_last = static_cast<int>(block_token(a.order, a.S, a.P, i, u_last));
     if (a.doc_start) {
-      sch.hull_lo = a.doc_start[static_cast<long long>(b) * a.S + t_first];
+      sch.hull_lo = a.doc_start[static_cast<long long>(b % a.pos_rows) * a.S + t_first];
       sch.hull_hi = t_last;
     } else {
       sch.hull_lo = 0;
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tq = row_live ? static_cast<int>(block_token(a.order, a.S, a.P, i, u)) : 0;
     int lo, hi;
     if (a.doc_start && row_live) {
-      lo = a.doc_start[static_cast<long long>(b) * a.S + tq];
+      lo = a.doc_start[static_cast<long long>(b % a.pos_rows) * a.S + tq];
       hi = tq;
     } else {
       lo = 0;

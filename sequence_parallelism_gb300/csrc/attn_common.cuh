@@ -14,15 +14,25 @@ struct AttnArgs {
   const void* q;               // [B][S][Hq][d]
   const void* k;               // [B][S][Hkv][d]
   const void* v;               // [B][S][Hkv][d]
-  const int32_t* doc_start;    // [B][S] or nullptr (non-causal)
+  const int32_t* doc_start;    // [pos_rows][S] or nullptr (non-causal)
   void* out;                   // [B][S][Hq][d]
   float* lse;                  // [B][Hq][S] or nullptr
   int* err;                    // device error word
   int B, S, Hq, Hkv, d, P;
+  int pos_rows;                // batch b reads doc_start row b % pos_rows
   int order;                   // sp_block_order
   int step_begin, step_end;
   float scale;                 // multiplies q.k (natural-log domain)
 };
+
+// Validates and runs one blockwise-attention call (doc_start scan when
+// position_ids != NULL, then the f32 or bf16 kernel).  position_ids has
+// pos_rows rows; attention batch b reads row b % pos_rows (pos_rows divides B).
+// Sets g_last_launches.
+sp_status attn(const void* q, const void* k, const void* v, const int32_t* position_ids,
+               int pos_rows, int B, int S, int Hq, int Hkv, int d, int P, sp_block_order order,
+               int step_begin, int step_end, float scale, sp_dtype dtype, void* out, float* lse,
+               void* workspace, size_t workspace_bytes, sp_stream_t stream);
 
 // Both return the number of kernels launched, or -1 on a CUDA error.
 int launch_attn_f32(const AttnArgs& a, cudaStream_t stream);

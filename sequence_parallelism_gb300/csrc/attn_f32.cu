@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(AttnArgs a, int n
     live[rr] = u < Lb;
     const long long t = live[rr] ? block_token(a.order, a.S, a.P, i, u) : 0;
     if (a.doc_start) {
-      lo[rr] = live[rr] ? a.doc_start[static_cast<long long>(b) * a.S + t] : 0;
+      lo[rr] = live[rr] ? a.doc_start[static_cast<long long>(b % a.pos_rows) * a.S + t] : 0;
       hi[rr] = t;
     } else {
       lo[rr] = 0;
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(AttnArgs a, int n
       const long long u = static_cast<long long>(tile) * kRows + r;
       if (u >= Lb) break;
       const long long t = block_token(a.order, a.S, a.P, i, u);
-      const long long l0 = a.doc_start ? a.doc_start[static_cast<long long>(b) * a.S + t] : 0;
+      const long long l0 = a.doc_start ? a.doc_start[static_cast<long long>(b % a.pos_rows) * a.S + t] : 0;
       const long long h0 = a.doc_start ? t : a.S - 1;
       hl = l0 < hl ? l0 : hl;
       hh = h0 > hh ? h0 : hh;

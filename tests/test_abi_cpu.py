@@ -117,3 +117,21 @@ def test_merge_and_segments_reject_bad_arguments(lib):
     assert s(FAKE, FAKE, 1, 8, None, 1 << 12, None) == SP_ERR_WORKSPACE
     assert s(FAKE, FAKE, 1, 8, FAKE_WS, 0, None) == SP_ERR_WORKSPACE
     assert lib.sp_get_device_error(None, None, None) == SP_ERR_INVALID_ARG
+
+
+def test_hybrid_rejects_bad_arguments(lib):
+    f = lib.sp_ulysses_ring_attn_fwd
+    ws = lib.sp_ulysses_ring_attn_workspace_bytes(1, 64, 8, 8, 128, 0, 0)
+    assert ws >= 4 * 64 * 8 * 128 * 2
+    args = lambda **kw: dict(dict(q=FAKE, k=FAKE, v=FAKE, pos=None, B=1, S=64, Hq=8, Hkv=8, d=128,
+                                  Pu=4, Pr=2, order=0, scale=0.0, dt=0, out=FAKE, ws=FAKE_WS,
+                                  wsb=1 << 30), **kw)
+    call = lambda a: f(a["q"], a["k"], a["v"], a["pos"], a["B"], a["S"], a["Hq"], a["Hkv"], a["d"],
+                       a["Pu"], a["Pr"], a["order"], a["scale"], a["dt"], a["out"], None, a["ws"],
+                       a["wsb"], None)
+    assert call(args(q=None)) == SP_ERR_INVALID_ARG
+    assert call(args(Hkv=2, Pu=4)) == SP_ERR_INVALID_ARG     # Hkv % P_u
+    assert call(args(S=66, Pr=4)) == SP_ERR_INVALID_ARG      # S % P_r
+    assert call(args(Pu=0)) == SP_ERR_INVALID_ARG
+    assert call(args(wsb=1024)) == SP_ERR_WORKSPACE
+    assert lib.sp_last_launch_count() == 0

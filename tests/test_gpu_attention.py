@@ -169,3 +169,35 @@ def test_no_device_error_reported(sp):
     st, code = _lib.sp_get_device_error(ws)
     assert st == 0 and code == 0
     assert _lib.sp_last_launch_count() == 1
+
+
+def test_fused_ulysses_is_bit_identical_to_permuted_pipeline(sp):
+    """On one GPU, attention on the sequence-sharded tensors computes every
+    Ulysses head group in place: same result, bit for bit, with no
+    permutation traffic."""
+    B, S, H, P = 1, 2048, 8, 4
+    q, k, v = workloads.small_case(B, S, H, H, 128, 500, "bf16")
+    piped = sp.ulysses_attention(q, k, v, P)
+    fused = sp.ulysses_attention(q, k, v, P, fused=True)
+    torch.cuda.synchronize()
+    assert torch.equal(piped.view(torch.int16), fused.view(torch.int16))
+    ref, _ = oracle.full_attention(np32(q), np32(k), np32(v))
+    check_attention(np32(fused), np.zeros((B, H, S)), ref, np.zeros((B, H, S)), "bf16", "fused")
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,P_u,P_r,order,pos", [
+    (1, 2048, 4, 4, 4, 2, "striped", "causal"),     # one head per Ulysses group
+    (2, 1536, 4, 2, 2, 3, "contiguous", "packed"),  # GQA inside each group
+    (1, 1024, 2, 2, 2, 4, "striped", "none"),
+])
+def test_ulysses_ring_hybrid_parity(sp, B, S, Hq, Hkv, P_u, P_r, order, pos):
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, 128, 600 + S, "bf16")
+    pos_np = _positions(pos, B, S, 600)
+    tpos = None if pos_np is None else torch.from_numpy(pos_np).cuda()
+    out, lse = sp.ulysses_ring_attention(q, k, v, P_u, P_r, order, tpos)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.full_attention(np32(q), np32(k), np32(v), pos_np)
+    G = Hq // P_u
+    lse_nat = lse.permute(1, 0, 2, 3).reshape(B, Hq, S).cpu().numpy()  # [P_u][B][G][S] -> [B][H][S]
+    check_attention(np32(out), lse_nat, ref_out, ref_lse, "bf16", f"hybrid {P_u}x{P_r} {order}")
+    assert G >= 1

@@ -81,3 +81,19 @@ def test_causal_full_size(sp, name, order):
     del out, lse
     ref_out, ref_lse = oracle_rows(np32(q), np32(k), np32(v), rows, pos)
     check_attention(got_out, got_lse, ref_out, ref_lse, "bf16", f"{name} {order}")
+
+
+def test_halfmil_ulysses_ring_hybrid(sp):
+    """halfmil_512k has 8 heads for P = 16 devices (Ulysses alone would need
+    16 heads): 8 Ulysses head groups x 2 striped ring blocks."""
+    cfg = workloads.CONFIGS["halfmil_512k"]
+    q, k, v = _inputs(cfg)
+    pos = workloads.position_ids(cfg)
+    out, lse = sp.ulysses_ring_attention(q, k, v, 8, 2, "striped", torch.from_numpy(pos).cuda())
+    torch.cuda.synchronize()
+    rows = workloads.sample_rows(cfg["S"], 2, 512, cfg["seed"] + 1, "striped")
+    got_out = np32(out[:, rows])
+    got_lse = lse.permute(1, 0, 2, 3).reshape(1, cfg["Hq"], cfg["S"])[:, :, rows].cpu().numpy()
+    del out, lse
+    ref_out, ref_lse = oracle_rows(np32(q), np32(k), np32(v), rows, pos)
+    check_attention(got_out, got_lse, ref_out, ref_lse, "bf16", "halfmil hybrid 8x2")
