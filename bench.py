@@ -41,7 +41,7 @@ METRIC = ("causal blockwise-attention TFLOP/s (% BF16 peak); seq↔head permute 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # kernel from the committed ncu capture (None until taken for this kernel).
-NCU_TRAFFIC_BYTES = {"ulysses_4k": 239.64e6, "llama8b_32k": 2095.89e6}
+NCU_TRAFFIC_BYTES = {}
 
 
 def load_peaks():

@@ -149,7 +149,12 @@ sp_status sp_segment_starts(const int32_t* position_ids, int32_t* doc_start, int
  * workspace: device scratch of at least
  * sp_blockwise_attn_workspace_bytes(B, S, position_ids != NULL) bytes,
  * 256-byte aligned; it holds the device error word and the doc_start
- * array.  Its contents need not be initialised.
+ * array.  Its contents need not be initialised.  A non-causal bf16 call given
+ * sp_blockwise_attn_split_workspace_bytes(...) bytes (about 21 MiB more) may
+ * also split the items of its last, partly filled wave of CTAs into pieces
+ * whose fp32 partial results are merged by their log-sum-exp (the ring's
+ * partial combine), so that the last wave fills the GPU; the result is the
+ * same up to rounding.
  *
  * Errors: SP_ERR_INVALID_ARG (NULL q/k/v/out, size < 1, S % P != 0,
  * Hq % Hkv != 0, bad order or dtype), SP_ERR_UNSUPPORTED (d outside the
@@ -158,6 +163,7 @@ sp_status sp_segment_starts(const int32_t* position_ids, int32_t* doc_start, int
  * by sp_get_device_error.
  * ------------------------------------------------------------------------ */
 size_t sp_blockwise_attn_workspace_bytes(int B, int S, int causal);
+size_t sp_blockwise_attn_split_workspace_bytes(int B, int S, int causal);
 sp_status sp_blockwise_attn_fwd(const void* q, const void* k, const void* v,
                                 const int32_t* position_ids, int B, int S, int Hq, int Hkv, int d,
                                 int P, sp_block_order order, float scale, sp_dtype dtype, void* out,

@@ -36,8 +36,13 @@ def head_to_seq(y, out=None):
     return _lib.sp_ulysses_head_to_seq(y, x, P)
 
 
-def attention_workspace(B, S, causal, device=None):
-    n = _lib.sp_blockwise_attn_workspace_bytes(B, S, causal)
+def attention_workspace(B, S, causal, device=None, minimal=False):
+    """Workspace for the attention calls; by default large enough for the
+    tail split of non-causal calls (minimal=True: the required minimum)."""
+    if minimal:
+        n = _lib.sp_blockwise_attn_workspace_bytes(B, S, causal)
+    else:
+        n = _lib.sp_blockwise_attn_split_workspace_bytes(B, S, causal)
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
 
 

@@ -25,6 +25,7 @@ _ORDERS = {"contiguous": SP_ORDER_CONTIGUOUS, "striped": SP_ORDER_STRIPED}
 EXPORTS = (
     "sp_status_string", "sp_ulysses_seq_to_head", "sp_ulysses_head_to_seq",
     "sp_segment_starts_workspace_bytes", "sp_segment_starts", "sp_blockwise_attn_workspace_bytes",
+    "sp_blockwise_attn_split_workspace_bytes",
     "sp_blockwise_attn_fwd", "sp_blockwise_attn_step", "sp_blockwise_attn_fwd_noalloc",
     "sp_ulysses_ring_attn_workspace_bytes", "sp_ulysses_ring_attn_fwd",
     "sp_attn_merge_partials",
@@ -50,6 +51,7 @@ def _load():
         "sp_segment_starts_workspace_bytes": (sz, [i, i]),
         "sp_segment_starts": (i, [vp, vp, i, i, vp, sz, vp]),
         "sp_blockwise_attn_workspace_bytes": (sz, [i, i, i]),
+        "sp_blockwise_attn_split_workspace_bytes": (sz, [i, i, i]),
         "sp_blockwise_attn_fwd": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, vp, vp, sz,
                                       vp]),
         "sp_blockwise_attn_step": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp,
@@ -142,6 +144,10 @@ def sp_segment_starts(position_ids, doc_start, workspace, stream=None):
 
 def sp_blockwise_attn_workspace_bytes(B, S, causal):
     return _lib.sp_blockwise_attn_workspace_bytes(B, S, int(bool(causal)))
+
+
+def sp_blockwise_attn_split_workspace_bytes(B, S, causal):
+    return _lib.sp_blockwise_attn_split_workspace_bytes(B, S, int(bool(causal)))
 
 
 def sp_blockwise_attn_fwd(q, k, v, position_ids, P, order, scale, out, lse, workspace,

@@ -95,6 +95,12 @@ sp_status attn(const void* q, const void* k, const void* v, const int32_t* posit
   a.step_begin = step_begin;
   a.step_end = step_end;
   a.scale = scale > 0.f ? scale : static_cast<float>(1.0 / sqrt(static_cast<double>(d)));
+  a.scratch = nullptr;
+  a.scratch_bytes = 0;
+  if (!causal && workspace_bytes > kWsHeaderBytes) {
+    a.scratch = ws + kWsHeaderBytes;
+    a.scratch_bytes = workspace_bytes - kWsHeaderBytes;
+  }
   const int n = dtype == SP_BF16 ? launch_attn_bf16(a, st) : launch_attn_f32(a, st);
   if (n < 0) return SP_ERR_CUDA;
   g_last_launches = launches + n;
@@ -120,6 +126,12 @@ extern "C" size_t sp_blockwise_attn_workspace_bytes(int B, int S, int causal) {
   size_t n = sp::kWsHeaderBytes;
   if (causal) n += sp::doc_start_bytes(B, S) + sp::segment_scratch_bytes(B, S);
   return n;
+}
+
+extern "C" size_t sp_blockwise_attn_split_workspace_bytes(int B, int S, int causal) {
+  const size_t n = sp_blockwise_attn_workspace_bytes(B, S, causal);
+  if (n == 0 || causal) return n;
+  return n + sp::kSplitScratchBytes;
 }
 
 extern "C" sp_status sp_blockwise_attn_fwd(const void* q, const void* k, const void* v,

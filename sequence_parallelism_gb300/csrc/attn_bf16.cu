@@ -75,10 +75,14 @@ __device__ __forceinline__ int floor_div(int a, int b) {
   return a >= 0 ? a / b : -((-a + b - 1) / b);
 }
 
-// The part of the ring schedule every role must agree on.
+// The part of the ring schedule every role must agree on.  Tiles are
+// numbered in visiting order (ring step, then key tile); a CTA processes the
+// window [t_lo, t_hi) of that sequence (the whole sequence unless the item is
+// split across several CTAs).
 struct Schedule {
   int i, P, Lb, S, order, step_begin, step_end;
   int hull_lo, hull_hi;  // key-token interval any row of the CTA may use
+  int t_lo, t_hi;
 
   // KV tiles [kt0, kt1] of block j that intersect the hull (kt1 < kt0: none)
   __device__ __forceinline__ void tiles(int s, int& j, int& kt0, int& kt1) const {
@@ -103,7 +107,8 @@ struct Schedule {
     kt1 = static_cast<int>(w_hi / kBN);
   }
 
-  __device__ __forceinline__ int count() const {
+  // total number of tiles in the item's sequence
+  __device__ __forceinline__ int total() const {
     int n = 0;
     for (int s = step_begin; s < step_end; ++s) {
       int j, a, b;
@@ -113,6 +118,21 @@ struct Schedule {
     return n;
   }
 };
+
+// Work item of linear index L: heavy query positions first (the causal work
+// of a query block grows with its position), heads innermost so that the
+// query heads sharing a key/value head run side by side.
+__device__ __forceinline__ void item_coords(int L, const AttnArgs& a, int n_pairs, int& b, int& hq,
+                                            int& i, int& pair) {
+  const int BH = a.B * a.Hq;
+  const int pos = L / BH;
+  const int bh = L % BH;
+  b = bh / a.Hq;
+  hq = bh % a.Hq;
+  const int rev = a.P * n_pairs - 1 - pos;
+  i = rev / n_pairs;
+  pair = rev % n_pairs;
+}
 
 struct __align__(8) Barriers {
   uint64_t q_full;
@@ -125,8 +145,9 @@ struct __align__(8) Barriers {
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bf16_kernel(const __grid_constant__ Tmaps tm, AttnArgs a, float scale_log2,
-                     int n_pairs) {
+    attn_bf16_kernel(const __grid_constant__ Tmaps tm, AttnArgs a, float scale_log2, int n_pairs,
+                     int n_whole, int split_k, float* __restrict__ part_o,
+                     float* __restrict__ part_lse) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Barriers bars;
   __shared__ uint32_t tmem_base_s;
@@ -141,16 +162,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work item: heavy query positions first, heads innermost ----------
-  const int BH = a.B * a.Hq;
-  const int pos = blockIdx.x / BH;
-  const int bh = blockIdx.x % BH;
-  const int b = bh / a.Hq;
-  const int hq = bh % a.Hq;
+  // ---- work item: CTAs [0, n_whole) run whole items; the CTAs after them
+  // run split_k pieces (tile windows) of each remaining item and write fp32
+  // partials that merge_split_kernel combines.  Scheduled last, the pieces
+  // fill the final wave of the launch.
+  const int cta = static_cast<int>(blockIdx.x);
+  const bool whole = cta < n_whole;
+  const int split = whole ? 1 : split_k;
+  const int sidx = whole ? 0 : cta - n_whole;  // index among the pieces
+  int b, hq, i, pair;
+  item_coords(whole ? cta : n_whole + sidx / split_k, a, n_pairs, b, hq, i, pair);
+  const int piece = whole ? 0 : sidx % split_k;
   const int kvh = hq / (a.Hq / a.Hkv);
-  const int rev = a.P * n_pairs - 1 - pos;
-  const int i = rev / n_pairs;
-  const int pair = rev % n_pairs;
   const int Lb = a.S / a.P;
   const int u0 = pair * kRowsPerCta;  // first local query row of the CTA
 
@@ -174,7 +197,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       sch.hull_hi = a.S - 1;
     }
   }
-  const int n_tiles = sch.count();
+  {
+    const int tot = sch.total();
+    sch.t_lo = static_cast<int>(static_cast<long long>(tot) * piece / split);
+    sch.t_hi = static_cast<int>(static_cast<long long>(tot) * (piece + 1) / split);
+  }
+  const int n_tiles = sch.t_hi - sch.t_lo;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars.q_full), 1);
@@ -227,12 +255,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_5d(smem_q + t * kTileBytes + half * kHalfBytes, &tm.q, qf, half * 64, hq, c2,
                       c3, b);
       }
-      int n = 0;  // load index: K_t = 2t, V_t = 2t + 1
+      int n = 0;   // load index: K_t = 2t, V_t = 2t + 1
+      int ft = 0;  // position in the item's tile sequence
       bool ok = true;
-      for (int s = a.step_begin; s < a.step_end && ok; ++s) {
+      for (int s = a.step_begin; s < a.step_end && ok && ft < sch.t_hi; ++s) {
         int j, kt0, kt1;
         sch.tiles(s, j, kt0, kt1);
-        for (int kt = kt0; kt <= kt1 && ok; ++kt) {
+        for (int kt = kt0; kt <= kt1 && ok; ++kt, ++ft) {
+          if (ft < sch.t_lo) continue;
+          if (ft >= sch.t_hi) break;
           int c2, c3;
           coord_rows(j, kt * kBN, c2, c3);
           for (int kv = 0; kv < 2; ++kv, ++n) {
@@ -357,12 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY;   // running max (log2 units, scaled)
     float m_use = -INFINITY;   // exponent base actually applied
     float l = 0.f;
-    int it = 0;
+    int it = 0;  // tiles processed by this CTA
+    int ft = 0;  // position in the item's tile sequence
     bool ok = true;
-    for (int s = a.step_begin; s < a.step_end && ok; ++s) {
+    for (int s = a.step_begin; s < a.step_end && ok && ft < sch.t_hi; ++s) {
       int j, kt0, kt1;
       sch.tiles(s, j, kt0, kt1);
-      for (int kt = kt0; kt <= kt1; ++kt, ++it) {
+      for (int kt = kt0; kt <= kt1; ++kt, ++ft) {
+        if (ft < sch.t_lo) continue;
+        if (ft >= sch.t_hi) break;
         // warp-uniform outcome: the tcgen05.ld below is warp-collective
         const bool got = mbar_wait(smem_u32(&bars.s_full[t]), it & 1, abort_flag, a.err, kErrSFull);
         if (!__all_sync(0xffffffffu, got)) {
@@ -455,6 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.p_full[t]));
+        ++it;
       }
     }
     // ------------------------------------------------------------ epilogue
@@ -466,32 +501,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const bool any = have && ok && l > 0.f;
     const float inv = any ? 1.f / l : 0.f;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-    uint4* orow = reinterpret_cast<uint4*>(
-        out + ((static_cast<long long>(b) * a.S + tq) * a.Hq + hq) * kD);
+    const float row_lse = any ? (m_use + lg2(l)) * 0.69314718055994530942f : -INFINITY;
+    if (split > 1) {
+      // one piece of a split item: normalized partial O and its lse (fp32),
+      // combined afterwards by merge_split_kernel
+      const long long prow = static_cast<long long>(sidx) * kRowsPerCta + t * kBM + row;
+      float4* po = reinterpret_cast<float4*>(part_o + prow * kD);
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      uint32_t r[32];
-      if (have && ok) {
-        tmem_ld32(tO + c * 32, r);
-        tmem_wait_ld();
-      } else {
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        if (have && ok) {
+          tmem_ld32(tO + c * 32, r);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) r[e] = 0u;
+          for (int e = 0; e < 32; ++e) r[e] = 0u;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          po[c * 8 + e] =
+              make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
+                          __uint_as_float(r[4 * e + 2]) * inv, __uint_as_float(r[4 * e + 3]) * inv);
       }
-      uint32_t pk[16];
+      part_lse[prow] = row_lse;
+    } else {
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+      uint4* orow = reinterpret_cast<uint4*>(
+          out + ((static_cast<long long>(b) * a.S + tq) * a.Hq + hq) * kD);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        if (have && ok) {
+          tmem_ld32(tO + c * 32, r);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
-        pk[e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
-      if (row_live) {
+          for (int e = 0; e < 32; ++e) r[e] = 0u;
+        }
+        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          orow[c * 4 + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+        if (row_live) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            orow[c * 4 + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
       }
+      if (row_live && a.lse) a.lse[(static_cast<long long>(b) * a.Hq + hq) * a.S + tq] = row_lse;
     }
-    if (row_live && a.lse)
-      a.lse[(static_cast<long long>(b) * a.Hq + hq) * a.S + tq] =
-          any ? (m_use + lg2(l)) * 0.69314718055994530942f : -INFINITY;
   }
 
   tc_fence_before();
@@ -500,6 +558,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// Combines the pieces of split items: for every row, the `split` partial
+// results (each normalized by its own sum, with its own lse) are merged by
+// their log-sum-exp weights -- the same combine ring attention applies to
+// per-device partials ("Ring Attention", "Cómo funciona la atención en
+// anillo").  One warp per row of an item; lane c handles columns 4c..4c+3.
+__global__ void __launch_bounds__(256) merge_split_kernel(AttnArgs a, int n_pairs, int item_base,
+                                                          int split, const float* __restrict__ part_o,
+                                                          const float* __restrict__ part_lse) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int x = blockIdx.x / (kRowsPerCta / 8);            // split item
+  const int r = (blockIdx.x % (kRowsPerCta / 8)) * 8 + warp;  // row within the item
+  int b, hq, i, pair;
+  item_coords(item_base + x, a, n_pairs, b, hq, i, pair);
+  const int Lb = a.S / a.P;
+  const int u = pair * kRowsPerCta + r;
+  if (u >= Lb) return;
+  const long long tq = block_token(a.order, a.S, a.P, i, u);
+  float m = -INFINITY;
+  for (int p = 0; p < split; ++p)
+    m = fmaxf(m, part_lse[(static_cast<long long>(x) * split + p) * kRowsPerCta + r]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  if (m != -INFINITY) {
+    for (int p = 0; p < split; ++p) {
+      const long long prow = (static_cast<long long>(x) * split + p) * kRowsPerCta + r;
+      const float lp = part_lse[prow];
+      if (lp == -INFINITY) continue;
+      const float w = expf(lp - m);
+      wsum += w;
+      const float4 o = reinterpret_cast<const float4*>(part_o + prow * kD)[lane];
+      acc.x = fmaf(w, o.x, acc.x);
+      acc.y = fmaf(w, o.y, acc.y);
+      acc.z = fmaf(w, o.z, acc.z);
+      acc.w = fmaf(w, o.w, acc.w);
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+  uint2* orow = reinterpret_cast<uint2*>(out + ((static_cast<long long>(b) * a.S + tq) * a.Hq + hq) * kD);
+  orow[lane] = make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
+  if (a.lse && lane == 0)
+    a.lse[(static_cast<long long>(b) * a.Hq + hq) * a.S + tq] =
+        wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
 // ------------------------------------------------------------------ host
@@ -570,15 +673,43 @@ int launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
     return -1;
   const int Lb = a.S / a.P;
   const int n_pairs = (Lb + kRowsPerCta - 1) / kRowsPerCta;
-  const long long blocks = static_cast<long long>(a.B) * a.Hq * a.P * n_pairs;
+  const long long items = static_cast<long long>(a.B) * a.Hq * a.P * n_pairs;
   const size_t smem = kSmemBytes + 1024;
   if (cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return -1;
   const float scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-  attn_bf16_kernel<<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(tm, a, scale_log2,
-                                                                            n_pairs);
-  return cudaGetLastError() == cudaSuccess ? 1 : -1;
+
+  // Tail split (non-causal only, where every item has the same tile count):
+  // the items of the last, partly filled wave are cut into `split` pieces
+  // along their ring-ordered tile sequence so that the wave fills the GPU;
+  // the pieces write fp32 partials that merge_split_kernel combines.
+  const long long G = device_sm_count();
+  const long long rem = items % G;
+  const long long full = items - rem;
+  int split = 1;
+  if (!a.doc_start && a.scratch && rem > 0) {
+    const long long tiles = static_cast<long long>(a.step_end - a.step_begin) *
+                            ((Lb + kBN - 1) / kBN);
+    long long k = G / rem;
+    if (k > tiles) k = tiles;
+    if (k > 32) k = 32;
+    if (rem * k > kMaxSplitPieces) k = kMaxSplitPieces / rem;
+    const size_t need = static_cast<size_t>(rem * k) * kRowsPerCta * (kD + 1) * sizeof(float);
+    if (k >= 2 && need <= a.scratch_bytes) split = static_cast<int>(k);
+  }
+  if (split == 1) {
+    attn_bf16_kernel<<<static_cast<unsigned>(items), kThreads, smem, stream>>>(
+        tm, a, scale_log2, n_pairs, static_cast<int>(items), 1, nullptr, nullptr);
+    return cudaGetLastError() == cudaSuccess ? 1 : -1;
+  }
+  float* part_o = static_cast<float*>(a.scratch);
+  float* part_lse = part_o + static_cast<size_t>(rem * split) * kRowsPerCta * kD;
+  attn_bf16_kernel<<<static_cast<unsigned>(full + rem * split), kThreads, smem, stream>>>(
+      tm, a, scale_log2, n_pairs, static_cast<int>(full), split, part_o, part_lse);
+  merge_split_kernel<<<static_cast<unsigned>(rem * (kRowsPerCta / 8)), 256, 0, stream>>>(
+      a, n_pairs, static_cast<int>(full), split, part_o, part_lse);
+  return cudaGetLastError() == cudaSuccess ? 2 : -1;
 }
 
 }  // namespace sp

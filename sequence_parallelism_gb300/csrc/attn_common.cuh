@@ -23,7 +23,15 @@ struct AttnArgs {
   int order;                   // sp_block_order
   int step_begin, step_end;
   float scale;                 // multiplies q.k (natural-log domain)
+  void* scratch;               // optional workspace beyond the minimum (256-aligned)
+  size_t scratch_bytes;
 };
+
+// Scratch that lets a non-causal bf16 call split the items of its last,
+// partly filled wave (fp32 partial rows for at most kMaxSplitPieces CTAs).
+constexpr int kMaxSplitPieces = 160;
+constexpr size_t kSplitScratchBytes =
+    static_cast<size_t>(kMaxSplitPieces) * 256 * (128 + 1) * sizeof(float);
 
 // Validates and runs one blockwise-attention call (doc_start scan when
 // position_ids != NULL, then the f32 or bf16 kernel).  position_ids has

@@ -23,7 +23,7 @@ struct HybridLayout {
 HybridLayout hybrid_layout(int B, int S, int Hq, int Hkv, int d, int causal, sp_dtype dtype) {
   HybridLayout L;
   const size_t es = dtype_size(dtype);
-  L.attn = round_up(sp_blockwise_attn_workspace_bytes(B, S, causal), 256);
+  L.attn = round_up(sp_blockwise_attn_split_workspace_bytes(B, S, causal), 256);
   L.yq = round_up(static_cast<size_t>(B) * S * Hq * d * es, 256);
   L.ykv = round_up(static_cast<size_t>(B) * S * Hkv * d * es, 256);
   L.total = L.attn + 2 * L.yq + 2 * L.ykv;

@@ -163,7 +163,7 @@ def test_zero_query_closed_form(sp):
 def test_no_device_error_reported(sp):
     B, S = 1, 1024
     q, k, v = workloads.small_case(B, S, 2, 2, 128, 402, "bf16")
-    ws = sp.attention_workspace(B, S, False)
+    ws = sp.attention_workspace(B, S, False, minimal=True)
     sp.blockwise_attention(q, k, v, 2, "contiguous", workspace=ws)
     from sequence_parallelism_gb300 import _lib
     st, code = _lib.sp_get_device_error(ws)
@@ -201,3 +201,25 @@ def test_ulysses_ring_hybrid_parity(sp, B, S, Hq, Hkv, P_u, P_r, order, pos):
     lse_nat = lse.permute(1, 0, 2, 3).reshape(B, Hq, S).cpu().numpy()  # [P_u][B][G][S] -> [B][H][S]
     check_attention(np32(out), lse_nat, ref_out, ref_lse, "bf16", f"hybrid {P_u}x{P_r} {order}")
     assert G >= 1
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,P,order", [
+    (2, 1000, 4, 2, 2, "contiguous"),   # 8 items: every item split into pieces
+    (1, 4096, 10, 5, 4, "striped"),     # 160 items: a full wave plus 8 split items
+])
+def test_tail_split_and_single_launch_agree_with_oracle(sp, B, S, Hq, Hkv, P, order):
+    """Non-causal calls with the larger workspace split the items of their
+    last wave and merge fp32 partials; with the minimal workspace every item
+    runs whole in one launch.  Both match the oracle."""
+    from sequence_parallelism_gb300 import _lib
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, 128, 700 + S, "bf16")
+    ref_out, ref_lse = oracle.full_attention(np32(q), np32(k), np32(v))
+    launches = {}
+    for minimal in (True, False):
+        ws = sp.attention_workspace(B, S, False, minimal=minimal)
+        out, lse = sp.blockwise_attention(q, k, v, P, order, workspace=ws)
+        launches[minimal] = _lib.sp_last_launch_count()
+        torch.cuda.synchronize()
+        check_attention(np32(out), lse.cpu().numpy(), ref_out, ref_lse, "bf16",
+                        f"minimal={minimal}")
+    assert launches[True] == 1 and launches[False] >= 2
