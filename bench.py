@@ -181,9 +181,8 @@ def run_ours(args, rank, world, local_rank):
             n = 0
             if ev:
                 ev[0].record(stream)
-            for src, dst in ((q, yq), (k, yk), (v, yv)):
-                _lib.sp_ulysses_seq_to_head(src, dst, P)
-                n += _lib.sp_last_launch_count()
+            _lib.sp_ulysses_seq_to_head_qkv(q, k, v, yq, yk, yv, P)
+            n += _lib.sp_last_launch_count()
             if ev:
                 ev[1].record(stream)
             _lib.sp_blockwise_attn_fwd(yq.view(P * B, S, G, d), yk.view(P * B, S, G, d),
@@ -284,7 +283,8 @@ def run_ours(args, rank, world, local_rank):
         gbs = perm_bytes / (perm_mean * 1e-3) / 1e9
         inv_gbs = inv_bytes / (statistics.mean(inv_ms) * 1e-3) / 1e9
         result["permute"] = {
-            "kernel": "permute_kernel (seq_to_head x3, head_to_seq x1)", "bound": "hbm",
+            "kernel": "permute_kernel (seq_to_head of q,k,v in one launch; head_to_seq)",
+            "bound": "hbm",
             "seq_to_head_GBps": round(gbs, 1), "head_to_seq_GBps": round(inv_gbs, 1),
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
             "bytes_per_step": perm_bytes + inv_bytes,

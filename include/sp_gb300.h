@@ -100,6 +100,14 @@ sp_status sp_ulysses_seq_to_head(const void* x, void* y, int B, int S, int H, in
 sp_status sp_ulysses_head_to_seq(const void* y, void* x, int B, int S, int H, int d, int P,
                                  sp_dtype dtype, sp_stream_t stream);
 
+/* sp_ulysses_seq_to_head for the q, k and v of one layer in a single launch:
+ * q [B][S][Hq][d] -> yq [P][B][S][Hq/P][d], k, v [B][S][Hkv][d] ->
+ * yk, yv [P][B][S][Hkv/P][d].  Same results and errors as three
+ * sp_ulysses_seq_to_head calls (also SP_ERR_INVALID_ARG if Hkv % P != 0). */
+sp_status sp_ulysses_seq_to_head_qkv(const void* q, const void* k, const void* v, void* yq,
+                                     void* yk, void* yv, int B, int S, int Hq, int Hkv, int d,
+                                     int P, sp_dtype dtype, sp_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Document starts from position_ids (the O(n) causal-mask carrier,
  * "Ulysses SPで100万トークン学習", section 3).

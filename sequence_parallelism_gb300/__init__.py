@@ -108,8 +108,11 @@ def ulysses_attention(q, k, v, P, ring_blocks=None, order="contiguous", scale=0.
     if fused:
         out, _ = blockwise_attention(q, k, v, ring_blocks or P, order, None, scale)
         return out
-    yq, yk, yv = seq_to_head(q, P), seq_to_head(k, P), seq_to_head(v, P)
     G, Gk = Hq // P, k.shape[2] // P
+    yq = torch.empty((P, B, S, G, d), dtype=q.dtype, device=q.device)
+    yk = torch.empty((P, B, S, Gk, d), dtype=k.dtype, device=k.device)
+    yv = torch.empty_like(yk)
+    _lib.sp_ulysses_seq_to_head_qkv(q, k, v, yq, yk, yv, P)
     yo, _ = blockwise_attention(yq.view(P * B, S, G, d), yk.view(P * B, S, Gk, d),
                                 yv.view(P * B, S, Gk, d), ring_blocks or P, order, None, scale)
     return head_to_seq(yo.view(P, B, S, G, d))

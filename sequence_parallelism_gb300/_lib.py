@@ -24,6 +24,7 @@ _ORDERS = {"contiguous": SP_ORDER_CONTIGUOUS, "striped": SP_ORDER_STRIPED}
 
 EXPORTS = (
     "sp_status_string", "sp_ulysses_seq_to_head", "sp_ulysses_head_to_seq",
+    "sp_ulysses_seq_to_head_qkv",
     "sp_segment_starts_workspace_bytes", "sp_segment_starts", "sp_blockwise_attn_workspace_bytes",
     "sp_blockwise_attn_split_workspace_bytes",
     "sp_blockwise_attn_fwd", "sp_blockwise_attn_step", "sp_blockwise_attn_fwd_noalloc",
@@ -48,6 +49,7 @@ def _load():
         "sp_status_string": (ctypes.c_char_p, [i]),
         "sp_ulysses_seq_to_head": (i, [vp, vp, i, i, i, i, i, i, vp]),
         "sp_ulysses_head_to_seq": (i, [vp, vp, i, i, i, i, i, i, vp]),
+        "sp_ulysses_seq_to_head_qkv": (i, [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, vp]),
         "sp_segment_starts_workspace_bytes": (sz, [i, i]),
         "sp_segment_starts": (i, [vp, vp, i, i, vp, sz, vp]),
         "sp_blockwise_attn_workspace_bytes": (sz, [i, i, i]),
@@ -127,6 +129,17 @@ def sp_ulysses_head_to_seq(y, x, P, stream=None):
     _check("sp_ulysses_head_to_seq", _lib.sp_ulysses_head_to_seq(
         _ptr(y), _ptr(x), B, S, H, d, P, _dtype(x), _stream(stream)))
     return x
+
+
+def sp_ulysses_seq_to_head_qkv(q, k, v, yq, yk, yv, P, stream=None):
+    """q [B][S][Hq][d], k/v [B][S][Hkv][d] -> head-sharded yq, yk, yv (one launch)."""
+    _dense(q, k, v, yq, yk, yv)
+    B, S, Hq, d = q.shape
+    Hkv = k.shape[2]
+    _check("sp_ulysses_seq_to_head_qkv", _lib.sp_ulysses_seq_to_head_qkv(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(yq), _ptr(yk), _ptr(yv), B, S, Hq, Hkv, d, P, _dtype(q),
+        _stream(stream)))
+    return yq, yk, yv
 
 
 def sp_segment_starts_workspace_bytes(B, S):

@@ -65,11 +65,8 @@ extern "C" sp_status sp_ulysses_ring_attn_fwd(const void* q, const void* k, cons
   int launches = 0;
   sp_status st;
   // Ulysses all-to-all #1 (sequence shards -> P_u head groups)
-  if ((st = sp_ulysses_seq_to_head(q, yq, B, S, Hq, d, P_u, dtype, stream)) != SP_OK) return st;
-  launches += sp::g_last_launches;
-  if ((st = sp_ulysses_seq_to_head(k, yk, B, S, Hkv, d, P_u, dtype, stream)) != SP_OK) return st;
-  launches += sp::g_last_launches;
-  if ((st = sp_ulysses_seq_to_head(v, yv, B, S, Hkv, d, P_u, dtype, stream)) != SP_OK) return st;
+  st = sp_ulysses_seq_to_head_qkv(q, k, v, yq, yk, yv, B, S, Hq, Hkv, d, P_u, dtype, stream);
+  if (st != SP_OK) return st;
   launches += sp::g_last_launches;
   // ring attention over P_r blocks inside every head group (batch P_u * B);
   // all groups share the B rows of position_ids

@@ -135,3 +135,11 @@ def test_hybrid_rejects_bad_arguments(lib):
     assert call(args(Pu=0)) == SP_ERR_INVALID_ARG
     assert call(args(wsb=1024)) == SP_ERR_WORKSPACE
     assert lib.sp_last_launch_count() == 0
+
+
+def test_qkv_permutation_rejects_bad_arguments(lib):
+    f = lib.sp_ulysses_seq_to_head_qkv
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 8, 8, 6, 16, 4, 0, None) == SP_ERR_INVALID_ARG
+    assert f(FAKE, None, FAKE, FAKE, FAKE, FAKE, 1, 8, 8, 4, 16, 4, 0, None) == SP_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 9, 8, 4, 16, 4, 0, None) == SP_ERR_INVALID_ARG
+    assert lib.sp_last_launch_count() == 0

@@ -103,3 +103,24 @@ def test_doc_start_full_size(sp, name):
     ds = sp.doc_starts(torch.from_numpy(pos).cuda())
     torch.cuda.synchronize()
     assert np.array_equal(npi(ds), _doc_start_ref(pos))
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,d,P,dtype", [
+    (1, 4096, 32, 8, 128, 4, torch.bfloat16),   # GQA shapes, 16-byte path
+    (2, 24, 6, 3, 4, 3, torch.bfloat16),        # 8-byte chunks
+    (1, 10, 4, 2, 3, 2, torch.float32),         # 12-byte chunks: 4-byte path
+])
+def test_qkv_permutation_one_launch_bit_exact(sp, B, S, Hq, Hkv, d, P, dtype):
+    from sequence_parallelism_gb300 import _lib
+    q = _rand_tensor((B, S, Hq, d), dtype, 31)
+    k = _rand_tensor((B, S, Hkv, d), dtype, 32)
+    v = _rand_tensor((B, S, Hkv, d), dtype, 33)
+    yq = torch.empty((P, B, S, Hq // P, d), dtype=dtype, device="cuda")
+    yk = torch.empty((P, B, S, Hkv // P, d), dtype=dtype, device="cuda")
+    yv = torch.empty_like(yk)
+    _lib.sp_ulysses_seq_to_head_qkv(q, k, v, yq, yk, yv, P)
+    assert _lib.sp_last_launch_count() == 1
+    torch.cuda.synchronize()
+    bits = torch.int16 if dtype == torch.bfloat16 else torch.int32
+    for x, y in ((q, yq), (k, yk), (v, yv)):
+        assert np.array_equal(npi(y.view(bits)), oracle.seq_to_head(npi(x.view(bits)), P))
