@@ -269,6 +269,15 @@ sp_status sp_attn_merge_partials(const void* outs, const float* lses, int P, int
  * clears it.  Returns SP_OK, SP_ERR_DEVICE_TIMEOUT or SP_ERR_CUDA. */
 sp_status sp_get_device_error(void* workspace, int* code, sp_stream_t stream);
 
+/* Check of the device-side failure path: launches one thread that waits, with
+ * the same bounded wait the attention kernel uses, on a barrier that nothing
+ * ever completes, limited to timeout_us microseconds (1 .. 1e6).  The kernel
+ * then records its timeout code in the workspace error word and returns, so
+ * sp_get_device_error(workspace, ...) reports SP_ERR_DEVICE_TIMEOUT and the
+ * context stays usable.  workspace: >= 256 bytes, 256-byte aligned.  No
+ * counterpart on the pages (they name no failure detection for the kernel). */
+sp_status sp_check_barrier_timeout(void* workspace, int timeout_us, sp_stream_t stream);
+
 /* Number of kernels the last successful call on this host thread enqueued
  * (lets a caller count device launches without a profiler). */
 int sp_last_launch_count(void);

@@ -30,7 +30,7 @@ EXPORTS = (
     "sp_blockwise_attn_fwd", "sp_blockwise_attn_step", "sp_blockwise_attn_fwd_noalloc",
     "sp_ulysses_ring_attn_workspace_bytes", "sp_ulysses_ring_attn_fwd",
     "sp_attn_merge_partials",
-    "sp_get_device_error", "sp_last_launch_count",
+    "sp_get_device_error", "sp_check_barrier_timeout", "sp_last_launch_count",
 )
 
 
@@ -65,6 +65,7 @@ def _load():
                                          sz, vp]),
         "sp_attn_merge_partials": (i, [vp, vp, i, i, i, i, i, i, vp, vp, vp]),
         "sp_get_device_error": (i, [vp, ctypes.POINTER(ctypes.c_int), vp]),
+        "sp_check_barrier_timeout": (i, [vp, i, vp]),
         "sp_last_launch_count": (i, []),
     }
     for name, (res, args) in sig.items():
@@ -231,3 +232,9 @@ def sp_get_device_error(workspace, stream=None):
     code = ctypes.c_int(0)
     st = _lib.sp_get_device_error(_ptr(workspace), ctypes.byref(code), _stream(stream))
     return st, code.value
+
+
+def sp_check_barrier_timeout(workspace, timeout_us, stream=None):
+    _dense(workspace)
+    _check("sp_check_barrier_timeout", _lib.sp_check_barrier_timeout(
+        _ptr(workspace), int(timeout_us), _stream(stream)))

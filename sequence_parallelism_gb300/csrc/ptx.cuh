@@ -76,21 +76,25 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 
 // Bounded wait for the phase with the given parity to complete.
 // abort_flag: CTA-shared flag; err: global error word; code: what to record.
+// Two limits: wall time (timeout_ns of %globaltimer) and, as a second guard
+// in case the timer misbehaves, a cap on the number of polling rounds.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int* abort_flag, int* err, int code) {
+                                          volatile int* abort_flag, int* err, int code,
+                                          uint64_t timeout_ns = SP_WAIT_TIMEOUT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  while (true) {
+  const uint32_t sleep_ns = timeout_ns < 4000000ull ? 1000u : 1000000u;
+#pragma unroll 1
+  for (uint32_t round = 0; round < (1u << 26); ++round) {
 #pragma unroll 1
     for (int i = 0; i < 4; ++i)
-      if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+      if (mbar_try_wait_sleep(bar, parity, sleep_ns)) return true;
     if (*abort_flag) return false;
-    if (globaltimer() - t0 > SP_WAIT_TIMEOUT_NS) {
-      *abort_flag = 1;
-      if (err) atomicExch(err, code);
-      return false;
-    }
+    if (globaltimer() - t0 > timeout_ns) break;
   }
+  *abort_flag = 1;
+  if (err) atomicExch(err, code);
+  return false;
 }
 
 // -------------------------------------------------------------------- TMA

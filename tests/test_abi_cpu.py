@@ -143,3 +143,11 @@ def test_qkv_permutation_rejects_bad_arguments(lib):
     assert f(FAKE, None, FAKE, FAKE, FAKE, FAKE, 1, 8, 8, 4, 16, 4, 0, None) == SP_ERR_INVALID_ARG
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 9, 8, 4, 16, 4, 0, None) == SP_ERR_INVALID_ARG
     assert lib.sp_last_launch_count() == 0
+
+
+def test_barrier_check_rejects_bad_arguments(lib):
+    f = lib.sp_check_barrier_timeout
+    assert f(None, 1000, None) == SP_ERR_WORKSPACE
+    assert f(ctypes.c_void_p(0x20010), 1000, None) == SP_ERR_WORKSPACE
+    assert f(FAKE_WS, 0, None) == SP_ERR_INVALID_ARG
+    assert f(FAKE_WS, 2000000, None) == SP_ERR_INVALID_ARG

@@ -223,3 +223,17 @@ def test_tail_split_and_single_launch_agree_with_oracle(sp, B, S, Hq, Hkv, P, or
         check_attention(np32(out), lse.cpu().numpy(), ref_out, ref_lse, "bf16",
                         f"minimal={minimal}")
     assert launches[True] == 1 and launches[False] >= 2
+
+
+def test_barrier_timeout_is_reported_and_context_survives(sp):
+    """A wait that can never complete ends after its limit with the timeout
+    code in the workspace error word (SP_ERR_DEVICE_TIMEOUT), and the
+    context keeps working: no fault, no hang."""
+    from sequence_parallelism_gb300 import _lib
+    ws = sp.attention_workspace(1, 1024, False, minimal=True)
+    _lib.sp_check_barrier_timeout(ws, 20000)  # 20 ms
+    st, code = _lib.sp_get_device_error(ws)
+    assert st == _lib.SP_ERR_DEVICE_TIMEOUT and code == 0x1F0
+    st, code = _lib.sp_get_device_error(ws)     # reading clears the word
+    assert st == 0 and code == 0
+    _run(sp, "bf16", 1, 1024, 2, 2, 128, 2, "contiguous", "causal", 901)
