@@ -38,6 +38,9 @@ Readings of points the pages leave open (all listed in the design doc):
   head-sharded tensor is laid out [P][B][S][H/P][d];
 * a query row with no allowed key has out = 0 and lse = -inf.
 
+attention_backward adds the gradients of that definition (the pages print no
+backward formulas; they are the derivatives of the forward).
+
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 (worked example of the Ring Attention page, closed forms, a library routine,
 brute force and invariants); none is "parity unpinned".
@@ -45,6 +48,7 @@ brute force and invariants); none is "parity unpinned".
 
 from .attention import (  # noqa: F401
     allowed_mask,
+    attention_backward,
     attention_rows,
     blockwise_ring_attention,
     block_tokens,

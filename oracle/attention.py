@@ -316,3 +316,51 @@ def ring_unstabilised_f32(q, k, v, n_blocks):
             den += e.sum(axis=1, keepdims=True)
         outs.append(num / den)
     return np.concatenate(outs, axis=0)
+
+
+def attention_backward(q, k, v, dout, position_ids=None, scale=None):
+    """Gradients of out = softmax(scale * Q K^T + mask) V with respect to q,
+    k, v for an upstream gradient dout (same layout as out).
+
+    The pages' use case is training ("Ulysses SP: entrenar modelos con
+    millones de tokens"; the ring keeps running sums per block, "Ring
+    Attention", "Cómo funciona la atención en anillo") but they print no
+    backward formulas; these are the derivatives of the definition:
+        P  = softmax(S) over the allowed keys,   S = scale * Q K^T
+        dV = P^T dO
+        dP = dO V^T
+        dS = P * (dP - D),   D_i = sum_c dO[i, c] * O[i, c]  (= sum_j P_ij dP_ij)
+        dQ = scale * dS K,   dK = scale * dS^T Q
+    GQA: the query heads of a group add into their shared key/value head.
+    Rows with no allowed key contribute nothing.  Full score matrices per
+    head: small sizes only.  Returns dq, dk, dv in float64.
+    """
+    B, S, Hq, Hkv, d = _check_shapes(q, k, v)
+    g = Hq // Hkv
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    allowed = allowed_mask(position_ids, B, S)
+    dq = np.zeros(q.shape)
+    dk = np.zeros(k.shape)
+    dv = np.zeros(v.shape)
+    for b in range(B):
+        for h in range(Hq):
+            kvh = h // g
+            qh = np.asarray(q[b, :, h, :], dtype=np.float64)
+            kh = np.asarray(k[b, :, kvh, :], dtype=np.float64)
+            vh = np.asarray(v[b, :, kvh, :], dtype=np.float64)
+            doh = np.asarray(dout[b, :, h, :], dtype=np.float64)
+            s = np.where(allowed[b], scale * (qh @ kh.T), NEG_INF)
+            m = s.max(axis=1)
+            live = np.isfinite(m)
+            w = np.where(allowed[b], np.exp(s - np.where(live, m, 0.0)[:, None]), 0.0)
+            l = w.sum(axis=1)
+            p = np.zeros_like(w)
+            p[live] = w[live] / l[live, None]
+            o = p @ vh
+            dv[b, :, kvh, :] += p.T @ doh
+            dp = doh @ vh.T
+            D = (doh * o).sum(axis=1)
+            ds = p * (dp - D[:, None])
+            dq[b, :, h, :] = scale * (ds @ kh)
+            dk[b, :, kvh, :] += scale * (ds.T @ qh)
+    return dq, dk, dv
