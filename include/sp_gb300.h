@@ -247,6 +247,32 @@ sp_status sp_blockwise_attn_fwd_noalloc(const void* q, const void* k, const void
                                         sp_dtype dtype, void* out, float* lse, sp_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Blockwise attention, backward (the pages train with sequence parallelism;
+ * these are the derivatives of the forward above).
+ *
+ *   P  = exp(scale * Q K^T - lse)  on the allowed pairs (lse from the forward)
+ *   dV = P^T dO
+ *   dS = P * (dO V^T - D),  D_t = sum_c dO[t][c] * O[t][c]
+ *   dQ = scale * dS K,   dK = scale * dS^T Q      (GQA: summed over the group)
+ *
+ * q, out, dout, dq [B][S][Hq][d]; k, v, dk, dv [B][S][Hkv][d] in `dtype`;
+ * lse [B][Hq][S] float32 as written by sp_blockwise_attn_fwd for the same q,
+ * k, v, position_ids and scale.  dQ visits the key/value blocks in ring order
+ * j = (i - s) mod P; dK/dV visit the query blocks in the order block j meets
+ * them on the ring, i = (j + s) mod P.  float32 accumulation; bf16 outputs
+ * rounded to nearest-even.  Supported: SP_BF16 with d == 128, SP_F32 with
+ * d <= 256.  workspace: sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq,
+ * position_ids != NULL) bytes, 256-byte aligned.  Errors as for
+ * sp_blockwise_attn_fwd.
+ * ------------------------------------------------------------------------ */
+size_t sp_blockwise_attn_bwd_workspace_bytes(int B, int S, int Hq, int causal);
+sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                                const void* dout, const float* lse, const int32_t* position_ids,
+                                int B, int S, int Hq, int Hkv, int d, int P, sp_block_order order,
+                                float scale, sp_dtype dtype, void* dq, void* dk, void* dv,
+                                void* workspace, size_t workspace_bytes, sp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Merge of per-block partial results (the cross-device combine of ring
  * attention, "Ring Attention", "Cómo funciona la atención en anillo").
  *

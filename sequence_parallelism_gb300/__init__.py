@@ -11,6 +11,7 @@ without the built library raises ImportError -- there is no CPU path.
     merge_partials(outs, lses)                 log-sum-exp combine of partials
     ulysses_attention(q, k, v, P, ...)         permute -> attention -> permute back
     ulysses_ring_attention(q, k, v, P_u, P_r)  Ulysses + Ring hybrid (heads < devices)
+    blockwise_attention_backward(...)          dq, dk, dv from out, dout and lse
     doc_starts(position_ids)                   O(n) causal-mask carrier
 """
 
@@ -20,7 +21,8 @@ from . import _lib
 from ._lib import SPError  # noqa: F401
 
 __all__ = ["seq_to_head", "head_to_seq", "blockwise_attention", "ring_step", "merge_partials",
-           "ulysses_attention", "ulysses_ring_attention", "doc_starts", "attention_workspace",
+           "ulysses_attention", "ulysses_ring_attention", "blockwise_attention_backward",
+           "doc_starts", "attention_workspace",
            "SPError"]
 
 
@@ -74,6 +76,18 @@ def ring_step(q, k, v, P, step, order="contiguous", position_ids=None, scale=0.0
         workspace = attention_workspace(B, S, position_ids is not None, q.device)
     return _lib.sp_blockwise_attn_step(q, k, v, position_ids, P, order, step, scale, out, lse,
                                        workspace)
+
+
+def blockwise_attention_backward(q, k, v, out, dout, lse, P, order="contiguous",
+                                 position_ids=None, scale=0.0, workspace=None):
+    """Gradients (dq, dk, dv) of blockwise attention; lse from the forward."""
+    B, S, Hq, d = q.shape
+    if workspace is None:
+        n = _lib.sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, position_ids is not None)
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    return _lib.sp_blockwise_attn_bwd(q, k, v, out, dout, lse, position_ids, P, order, scale, dq,
+                                      dk, dv, workspace)
 
 
 def merge_partials(outs, lses, out=None, lse=None):

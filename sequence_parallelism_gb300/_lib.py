@@ -29,6 +29,7 @@ EXPORTS = (
     "sp_blockwise_attn_split_workspace_bytes",
     "sp_blockwise_attn_fwd", "sp_blockwise_attn_step", "sp_blockwise_attn_fwd_noalloc",
     "sp_ulysses_ring_attn_workspace_bytes", "sp_ulysses_ring_attn_fwd",
+    "sp_blockwise_attn_bwd_workspace_bytes", "sp_blockwise_attn_bwd",
     "sp_attn_merge_partials",
     "sp_get_device_error", "sp_check_barrier_timeout", "sp_last_launch_count",
 )
@@ -63,6 +64,9 @@ def _load():
         "sp_ulysses_ring_attn_workspace_bytes": (sz, [i, i, i, i, i, i, i]),
         "sp_ulysses_ring_attn_fwd": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp,
                                          sz, vp]),
+        "sp_blockwise_attn_bwd_workspace_bytes": (sz, [i, i, i, i]),
+        "sp_blockwise_attn_bwd": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp,
+                                      vp, vp, vp, sz, vp]),
         "sp_attn_merge_partials": (i, [vp, vp, i, i, i, i, i, i, vp, vp, vp]),
         "sp_get_device_error": (i, [vp, ctypes.POINTER(ctypes.c_int), vp]),
         "sp_check_barrier_timeout": (i, [vp, i, vp]),
@@ -216,6 +220,22 @@ def sp_ulysses_ring_attn_fwd(q, k, v, position_ids, P_u, P_r, order, scale, out,
         _ORDERS[order], float(scale), _dtype(q), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse
+
+
+def sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, causal):
+    return _lib.sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, int(bool(causal)))
+
+
+def sp_blockwise_attn_bwd(q, k, v, out, dout, lse, position_ids, P, order, scale, dq, dk, dv,
+                          workspace, stream=None):
+    _dense(q, k, v, out, dout, lse, position_ids, dq, dk, dv, workspace)
+    B, S, Hq, d = q.shape
+    Hkv = k.shape[2]
+    _check("sp_blockwise_attn_bwd", _lib.sp_blockwise_attn_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(position_ids), B, S,
+        Hq, Hkv, d, P, _ORDERS[order], float(scale), _dtype(q), _ptr(dq), _ptr(dk), _ptr(dv),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dq, dk, dv
 
 
 def sp_attn_merge_partials(outs, lses, out, lse, stream=None):

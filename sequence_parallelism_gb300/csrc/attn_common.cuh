@@ -33,6 +33,27 @@ constexpr int kMaxSplitPieces = 160;
 constexpr size_t kSplitScratchBytes =
     static_cast<size_t>(kMaxSplitPieces) * 256 * (128 + 1) * sizeof(float);
 
+// One backward call: gradients of blockwise attention.
+struct BwdArgs {
+  const void* q;               // [B][S][Hq][d]
+  const void* k;               // [B][S][Hkv][d]
+  const void* v;               // [B][S][Hkv][d]
+  const void* out;             // [B][S][Hq][d]  forward output
+  const void* dout;            // [B][S][Hq][d]  upstream gradient
+  const float* lse;            // [B][Hq][S]     forward log-sum-exp (natural)
+  const int32_t* doc_start;    // [pos_rows][S] or nullptr (non-causal)
+  float* Dsum;                 // [B][Hq][S] scratch: rowsum(dout * out)
+  void* dq;                    // [B][S][Hq][d]
+  void* dk;                    // [B][S][Hkv][d]
+  void* dv;                    // [B][S][Hkv][d]
+  int* err;
+  int B, S, Hq, Hkv, d, P, pos_rows, order;
+  sp_dtype dtype;
+  float scale;
+};
+
+int launch_attn_bwd_simt(const BwdArgs& a, cudaStream_t stream);
+
 // Validates and runs one blockwise-attention call (doc_start scan when
 // position_ids != NULL, then the f32 or bf16 kernel).  position_ids has
 // pos_rows rows; attention batch b reads row b % pos_rows (pos_rows divides B).

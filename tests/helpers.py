@@ -47,3 +47,21 @@ def check_attention(out, lse, ref_out, ref_lse, dtype, what=""):
 
 def torch_dtype(name):
     return torch.bfloat16 if name == "bf16" else torch.float32
+
+
+# Gradients: errors normalised by max(1, max |ref|) of each tensor (gradient
+# magnitudes grow with the number of contributing rows).  bf16 storage with
+# fp32 accumulation: max <= 2e-2, mean <= 2e-3; fp32: max <= 1e-4 (sums of up
+# to S fp32 products).
+GRAD_BF16_MAX, GRAD_BF16_MEAN, GRAD_F32_MAX = 2e-2, 2e-3, 1e-4
+
+
+def check_grad(got, ref, dtype, what=""):
+    scale = max(1.0, float(np.abs(ref).max()))
+    err = np.abs(got.astype(np.float64) - ref) / scale
+    if dtype == "bf16":
+        assert err.max() <= GRAD_BF16_MAX, f"{what}: max rel err {err.max():.3e}"
+        assert err.mean() <= GRAD_BF16_MEAN, f"{what}: mean rel err {err.mean():.3e}"
+    else:
+        assert err.max() <= GRAD_F32_MAX, f"{what}: max rel err {err.max():.3e}"
+    return float(err.max()), float(err.mean())

@@ -1,0 +1,57 @@
+"""GPU parity of the attention backward (dq, dk, dv) against the float64
+oracle's derivatives, through the C ABI.  The kernel takes out and lse from
+our forward, as a training step would."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import check_grad, np32
+from sequence_parallelism_gb300 import workloads
+from test_gpu_attention import _positions
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sp():
+    import sequence_parallelism_gb300 as m
+    return m
+
+
+def _run_bwd(sp, dtype, B, S, Hq, Hkv, d, P, order, pos_kind, seed):
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, d, seed, dtype)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed + 1)
+    dout = torch.randn(q.shape, generator=g, device="cuda").to(q.dtype)
+    pos = _positions(pos_kind, B, S, seed)
+    tpos = None if pos is None else torch.from_numpy(pos).cuda()
+    out, lse = sp.blockwise_attention(q, k, v, P, order, tpos)
+    dq, dk, dv = sp.blockwise_attention_backward(q, k, v, out, dout, lse, P, order, tpos)
+    torch.cuda.synchronize()
+    rq, rk, rv = oracle.attention_backward(np32(q), np32(k), np32(v), np32(dout), pos)
+    tag = f"{dtype} S={S} P={P} {order} {pos_kind}"
+    check_grad(np32(dq), rq, dtype, "dq " + tag)
+    check_grad(np32(dk), rk, dtype, "dk " + tag)
+    check_grad(np32(dv), rv, dtype, "dv " + tag)
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,d,P,order,pos", [
+    (1, 32, 1, 1, 16, 4, "contiguous", "none"),     # the Ring Attention page's shape
+    (1, 96, 4, 2, 64, 3, "contiguous", "causal"),
+    (2, 64, 2, 1, 32, 4, "striped", "packed"),
+    (1, 80, 2, 2, 100, 2, "striped", "causal"),
+])
+def test_backward_f32(sp, B, S, Hq, Hkv, d, P, order, pos):
+    _run_bwd(sp, "f32", B, S, Hq, Hkv, d, P, order, pos, 800 + S)
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,P,order,pos", [
+    (1, 512, 4, 2, 2, "contiguous", "causal"),
+    (1, 768, 2, 2, 4, "striped", "packed"),
+    (2, 256, 2, 1, 1, "contiguous", "none"),
+    (1, 1000, 2, 1, 2, "striped", "none"),          # ragged blocks of 500
+])
+def test_backward_bf16(sp, B, S, Hq, Hkv, P, order, pos):
+    _run_bwd(sp, "bf16", B, S, Hq, Hkv, 128, P, order, pos, 850 + S)
