@@ -36,6 +36,7 @@
 
 #include "attn_common.cuh"
 #include "ptx.cuh"
+#include "tmap.cuh"
 
 namespace sp {
 namespace {
@@ -294,8 +295,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_tiles > 0) {
       bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abort_flag, a.err, kErrQFull);
       tc_fence_after();
-      const uint32_t tS[2] = {tmem + 0, tmem + 128};
-      const uint32_t tO[2] = {tmem + 256, tmem + 384};
       // Descriptors are built once; a k-step only adds its byte offset >> 4
       // to the start-address field (all addresses stay below 256 KiB, so the
       // 14-bit field never carries).
@@ -606,70 +605,13 @@ __global__ void __launch_bounds__(256) merge_split_kernel(AttnArgs a, int n_pair
 }
 
 // ------------------------------------------------------------------ host
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<EncodeTiledFn>(p);
-  }();
-  return fn;
-}
-
-// [B][S][H][128] bf16 viewed as 5-D (d, H, rows-in-block, block, B) for the
-// contiguous order or (d, H, block, rows-in-block, B) for the striped order,
-// box = 64 columns x 1 head x 128 rows, 128-byte swizzle.  Rows past the end
-// of a block are out of bounds and read as zeros.
-bool make_map(CUtensorMap* m, const void* base, int B, int S, int H, int P, int order) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t Lb = static_cast<cuuint64_t>(S / P);
-  const cuuint64_t row = static_cast<cuuint64_t>(H) * kD * 2;  // bytes per token
-  cuuint64_t dims[5], strides[4];
-  cuuint32_t box[5], estr[5] = {1, 1, 1, 1, 1};
-  dims[0] = kD;
-  dims[1] = H;
-  dims[4] = B;
-  strides[0] = kD * 2;
-  strides[3] = static_cast<cuuint64_t>(S) * row;
-  box[0] = 64;
-  box[1] = 1;
-  box[4] = 1;
-  if (order == SP_ORDER_STRIPED) {
-    dims[2] = P;
-    dims[3] = Lb;
-    strides[1] = row;
-    strides[2] = row * P;
-    box[2] = 1;
-    box[3] = kBN;
-  } else {
-    dims[2] = Lb;
-    dims[3] = P;
-    strides[1] = row;
-    strides[2] = row * Lb;
-    box[2] = kBN;
-    box[3] = 1;
-  }
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 int launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
   Tmaps tm;
-  if (!make_map(&tm.q, a.q, a.B, a.S, a.Hq, a.P, a.order) ||
-      !make_map(&tm.k, a.k, a.B, a.S, a.Hkv, a.P, a.order) ||
-      !make_map(&tm.v, a.v, a.B, a.S, a.Hkv, a.P, a.order))
+  if (!tmap::make_map(&tm.q, a.q, a.B, a.S, a.Hq, a.P, a.order) ||
+      !tmap::make_map(&tm.k, a.k, a.B, a.S, a.Hkv, a.P, a.order) ||
+      !tmap::make_map(&tm.v, a.v, a.B, a.S, a.Hkv, a.P, a.order))
     return -1;
   const int Lb = a.S / a.P;
   const int n_pairs = (Lb + kRowsPerCta - 1) / kRowsPerCta;
