@@ -260,10 +260,12 @@ sp_status sp_blockwise_attn_fwd_noalloc(const void* q, const void* k, const void
  * k, v, position_ids and scale.  dQ visits the key/value blocks in ring order
  * j = (i - s) mod P; dK/dV visit the query blocks in the order block j meets
  * them on the ring, i = (j + s) mod P.  float32 accumulation; bf16 outputs
- * rounded to nearest-even.  Supported: SP_BF16 with d == 128, SP_F32 with
- * d <= 256.  workspace: sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq,
- * position_ids != NULL) bytes, 256-byte aligned.  Errors as for
- * sp_blockwise_attn_fwd.
+ * rounded to nearest-even.  Supported: SP_BF16 with d == 128 (tensor cores:
+ * P and dS are rounded to bf16 before they enter the dV, dQ and dK products;
+ * every tensor pointer 16-byte aligned, else SP_ERR_INVALID_ARG), SP_F32
+ * with d <= 256 (CUDA cores, float32 throughout).  workspace:
+ * sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, position_ids != NULL)
+ * bytes, 256-byte aligned.  Errors as for sp_blockwise_attn_fwd.
  * ------------------------------------------------------------------------ */
 size_t sp_blockwise_attn_bwd_workspace_bytes(int B, int S, int Hq, int causal);
 sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const void* v, const void* out,

@@ -39,16 +39,22 @@ Readings of points the pages leave open (all listed in the design doc):
 * a query row with no allowed key has out = 0 and lse = -inf.
 
 attention_backward adds the gradients of that definition (the pages print no
-backward formulas; they are the derivatives of the forward).
+backward formulas; they are the derivatives of the forward);
+attention_backward_rows and attention_backward_keys give the same gradients
+for sampled query rows (dq) and sampled key rows (dk, dv) at full sequence
+lengths.
 
-Parity status: every function here is pinned by ``tests/test_oracle.py``
-(worked example of the Ring Attention page, closed forms, a library routine,
-brute force and invariants); none is "parity unpinned".
+Parity status: every function here is pinned by ``tests/test_oracle.py`` and
+``tests/test_oracle_backward.py`` (worked example of the Ring Attention page,
+closed forms, a library routine, float64 autograd, finite differences, brute
+force and invariants); none is "parity unpinned".
 """
 
 from .attention import (  # noqa: F401
     allowed_mask,
     attention_backward,
+    attention_backward_keys,
+    attention_backward_rows,
     attention_rows,
     blockwise_ring_attention,
     block_tokens,

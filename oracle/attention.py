@@ -364,3 +364,108 @@ def attention_backward(q, k, v, dout, position_ids=None, scale=None):
             dq[b, :, h, :] = scale * (ds @ kh)
             dk[b, :, kvh, :] += scale * (ds.T @ qh)
     return dq, dk, dv
+
+
+def attention_backward_rows(q, k, v, dout, rows, position_ids=None, scale=None,
+                            max_chunk_elems=1 << 24):
+    """dq for the given query tokens only, every query head.
+
+    The same derivatives as attention_backward, restricted to one query row
+    t at a time: p = softmax of row t over its allowed keys, o = p V,
+    D = dO_t . o, dS = p * (dO_t V^T - D), dq_t = scale * dS K.  A row needs
+    only its own scores, so this runs at full sequence lengths.  Returns
+    [B][R][Hq][d] in float64 for R = len(rows).
+    """
+    B, S, Hq, Hkv, d = _check_shapes(q, k, v)
+    g = Hq // Hkv
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    rows = np.asarray(rows, dtype=np.int64)
+    R = rows.shape[0]
+    dq = np.zeros((B, R, Hq, d))
+    seg = None if position_ids is None else segment_ids(position_ids)
+    step = max(1, max_chunk_elems // max(S, 1))
+    for b in range(B):
+        for h in range(Hq):
+            kvh = h // g
+            for c0 in range(0, R, step):
+                sel = rows[c0:c0 + step]
+                kmax = S if seg is None else int(sel.max()) + 1
+                keys = np.asarray(k[b, :kmax, kvh, :], dtype=np.float64)
+                vals = np.asarray(v[b, :kmax, kvh, :], dtype=np.float64)
+                if seg is None:
+                    allowed = np.ones((sel.shape[0], kmax), dtype=bool)
+                else:
+                    j = np.arange(kmax)
+                    allowed = (seg[b, :kmax][None, :] == seg[b, sel][:, None]) & (
+                        j[None, :] <= sel[:, None])
+                qr = np.asarray(q[b, sel, h, :], dtype=np.float64)
+                dor = np.asarray(dout[b, sel, h, :], dtype=np.float64)
+                o, lse = _softmax_attend(qr, keys, vals, allowed, scale)
+                live = np.isfinite(lse)
+                s = np.where(allowed, scale * (qr @ keys.T), NEG_INF)
+                p = np.where(allowed & live[:, None],
+                             np.exp(s - np.where(live, lse, 0.0)[:, None]), 0.0)
+                D = (dor * o).sum(axis=1)
+                ds = p * (dor @ vals.T - D[:, None])
+                dq[b, c0:c0 + sel.shape[0], h, :] = scale * (ds @ keys)
+    return dq
+
+
+def attention_backward_keys(q, k, v, dout, keys, position_ids=None, scale=None, kv_heads=None,
+                            max_chunk_elems=1 << 24):
+    """dk and dv for the given key tokens only.
+
+    dv_j = sum_t P_tj dO_t and dk_j = scale * sum_t dS_tj q_t over every
+    query t allowed to see key j, in every query head of j's group.  Each
+    such query enters with its full softmax statistics (lse_t and o_t over
+    all its allowed keys, from attention_rows), then only the score columns
+    of the sampled keys are formed.  kv_heads restricts the key/value heads
+    computed (the others stay zero).  Returns dk, dv [B][J][Hkv][d] in
+    float64 for J = len(keys).
+    """
+    B, S, Hq, Hkv, d = _check_shapes(q, k, v)
+    g = Hq // Hkv
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    keys = np.asarray(keys, dtype=np.int64)
+    J = keys.shape[0]
+    dk = np.zeros((B, J, Hkv, d))
+    dv = np.zeros((B, J, Hkv, v.shape[3]))
+    heads = range(Hkv) if kv_heads is None else kv_heads
+    seg = None if position_ids is None else segment_ids(position_ids)
+    for b in range(B):
+        # queries that see at least one sampled key
+        if seg is None:
+            qset = np.arange(S)
+        else:
+            t = np.arange(S)
+            seen = np.zeros(S, dtype=bool)
+            for j in keys:
+                seen |= (t >= j) & (seg[b] == seg[b, j])
+            qset = np.nonzero(seen)[0]
+        if qset.shape[0] == 0:
+            continue
+        for kvh in heads:
+            kj = np.asarray(k[b, keys, kvh, :], dtype=np.float64)
+            vj = np.asarray(v[b, keys, kvh, :], dtype=np.float64)
+            for h in range(kvh * g, (kvh + 1) * g):
+                o, lse = attention_rows(q[b:b + 1, :, h:h + 1], k[b:b + 1, :, kvh:kvh + 1],
+                                        v[b:b + 1, :, kvh:kvh + 1], qset,
+                                        None if position_ids is None
+                                        else position_ids[b:b + 1], scale, max_chunk_elems)
+                o, lse = o[0, :, 0, :], lse[0, 0, :]
+                qr = np.asarray(q[b, qset, h, :], dtype=np.float64)
+                dor = np.asarray(dout[b, qset, h, :], dtype=np.float64)
+                if seg is None:
+                    allowed = np.ones((qset.shape[0], J), dtype=bool)
+                else:
+                    allowed = (seg[b, qset][:, None] == seg[b, keys][None, :]) & (
+                        keys[None, :] <= qset[:, None])
+                live = np.isfinite(lse)
+                s = scale * (qr @ kj.T)
+                p = np.where(allowed & live[:, None],
+                             np.exp(s - np.where(live, lse, 0.0)[:, None]), 0.0)
+                D = (dor * o).sum(axis=1)
+                ds = p * (dor @ vj.T - D[:, None])
+                dv[b, :, kvh, :] += p.T @ dor
+                dk[b, :, kvh, :] += scale * (ds.T @ qr)
+    return dk, dv

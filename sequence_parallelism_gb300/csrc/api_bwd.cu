@@ -53,6 +53,11 @@ extern "C" sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const v
   if (d > 256) return SP_ERR_UNSUPPORTED;
   if (dtype == SP_BF16 && d != 128) return SP_ERR_UNSUPPORTED;
   if (B > 65535 || Hq > 65535) return SP_ERR_UNSUPPORTED;
+  if (dtype == SP_BF16) {  // TMA bases and 16-byte vector accesses
+    const void* ptrs[8] = {q, k, v, out, dout, dq, dk, dv};
+    for (const void* p : ptrs)
+      if (!sp::aligned(p, 16)) return SP_ERR_INVALID_ARG;
+  }
   const int causal = position_ids != nullptr;
   const sp::BwdLayout L = sp::bwd_layout(B, S, Hq, causal);
   if (!workspace || !sp::aligned(workspace, 256) || workspace_bytes < L.total)
@@ -92,7 +97,7 @@ extern "C" sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const v
     launches += n;
     a.doc_start = doc;
   }
-  const int n = sp::launch_attn_bwd_simt(a, st);
+  const int n = dtype == SP_BF16 ? sp::launch_attn_bwd_bf16(a, st) : sp::launch_attn_bwd_simt(a, st);
   if (n < 0) return SP_ERR_CUDA;
   sp::g_last_launches = launches + n;
   return SP_OK;

@@ -1,0 +1,795 @@
+// attn_bwd_bf16.cu -- backward of blockwise ring attention on the sm_103a
+// tensor cores (bf16 operands, fp32 accumulation in TMEM, d = 128).
+//
+// The gradients are the derivatives of the forward (the pages train with
+// sequence parallelism -- "Ulysses SP: entrenar modelos con millones de
+// tokens" -- but print no backward):
+//   P = exp(scale * Q K^T - lse), dP = dO V^T, dS = P * (dP - D),
+//   dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO,
+// D_t = sum_c dO[t, c] O[t, c] (computed by the rowsum kernel first).
+//
+// Two kernels, no atomics:
+//  * dQ: query-stationary.  One CTA keeps a 128-row Q tile and its dO tile in
+//    shared memory and walks the key/value blocks in ring order
+//    j = (i - s) mod P ("Ring Attention", "Cómo funciona la atención en
+//    anillo").  Per key tile: S = Q K^T and dP = dO V^T (SS MMAs), dS from
+//    P and dP in the elementwise warps, dQ += dS K with dS read from TMEM.
+//  * dK/dV: key-stationary.  One CTA keeps a 128-key K tile and V tile and
+//    walks, for every query head of the GQA group, the query blocks in the
+//    order its key block meets them on the ring, i = (j + s) mod P.  Per query
+//    tile: S^T = K Q^T and dP^T = V dO^T, then P^T and dS^T, then
+//    dV += P^T dO and dK += dS^T Q with P^T / dS^T read from TMEM.
+// Warp roles as in the forward: 4 elementwise warps (one thread per TMEM
+// lane = tile row), a TMA producer warp and an MMA warp (TMEM owner).  Every
+// barrier wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "attn_common.cuh"
+#include "ptx.cuh"
+#include "tmap.cuh"
+
+namespace sp {
+namespace {
+
+using namespace ptx;
+
+constexpr int kD = 128;
+constexpr int kT = 128;                      // rows per tile (queries or keys)
+constexpr int kSlots = 4;                    // streamed tile ring depth
+constexpr int kTileBytes = kT * kD * 2;      // 32 KiB
+constexpr int kHalfBytes = kTileBytes / 2;   // one 64-column half
+constexpr int kSmemBytes = (2 + kSlots) * kTileBytes;
+constexpr int kThreads = 192;                // 4 elementwise warps + TMA + MMA
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+constexpr uint32_t kIdescKmaj = idesc_bf16_f32(kT, kT, false);  // both operands K-major
+constexpr uint32_t kIdescBmn = idesc_bf16_f32(kT, kD, true);    // B MN-major
+
+enum : int {
+  kErrBwdQFull = 0x201, kErrBwdKvEmpty = 0x202, kErrBwdKvFull = 0x203, kErrBwdSFull = 0x204,
+  kErrBwdSFree = 0x205, kErrBwdDsFull = 0x206, kErrBwdOut = 0x207, kErrBwdDrain = 0x208
+};
+
+struct BwdMaps {
+  CUtensorMap q, k, v, dout;
+};
+
+__device__ __forceinline__ int floor_div_i(int a, int b) {
+  return a >= 0 ? a / b : -((-a + b - 1) / b);
+}
+
+// Tiles [kt0, kt1] of `rows` local rows of block j that hold a token of the
+// interval [lo, hi] (kt1 < kt0: none); local row w of block j holds token
+// block_token(order, S, P, j, w).
+__device__ __forceinline__ void block_tiles(int order, int S, int P, int j, int lo, int hi,
+                                            int rows, int& kt0, int& kt1) {
+  const int Lb = S / P;
+  int w_lo, w_hi;
+  if (order == SP_ORDER_STRIPED) {
+    w_lo = -floor_div_i(-(lo - j), P);
+    w_hi = floor_div_i(hi - j, P);
+  } else {
+    w_lo = lo - j * Lb;
+    w_hi = hi - j * Lb;
+  }
+  if (w_lo < 0) w_lo = 0;
+  if (w_hi > Lb - 1) w_hi = Lb - 1;
+  if (w_lo > w_hi) {
+    kt0 = 0;
+    kt1 = -1;
+    return;
+  }
+  kt0 = w_lo / rows;
+  kt1 = w_hi / rows;
+}
+
+// Allowed local columns [c_lo, c_hi] (clamped to [0, 127] / [-1, 127]) of
+// tile kt of block j for a row whose allowed token interval is [lo, hi].
+__device__ __forceinline__ void col_bounds(int order, int S, int P, int j, int kt, int lo, int hi,
+                                           int& c_lo, int& c_hi) {
+  const int Lb = S / P;
+  const int w_base = kt * kT;
+  int a, b;
+  if (order == SP_ORDER_STRIPED) {
+    a = -floor_div_i(-(lo - j), P) - w_base;
+    b = floor_div_i(hi - j, P) - w_base;
+  } else {
+    a = lo - j * Lb - w_base;
+    b = hi - j * Lb - w_base;
+  }
+  const int valid = Lb - w_base - 1;
+  if (b > valid) b = valid;
+  c_lo = a < 0 ? 0 : (a > kT ? kT : a);
+  c_hi = b < -1 ? -1 : (b > kT - 1 ? kT - 1 : b);
+}
+
+// One tile of rows from local row u of block p, head h: two 64-column boxes,
+// the second `half` bytes after the first.
+__device__ __forceinline__ void row_tma(uint32_t dst, const CUtensorMap* map, uint32_t bar, int h,
+                                        int order, int p, int u, int b, int half = kHalfBytes) {
+  const int c2 = order == SP_ORDER_STRIPED ? p : u;
+  const int c3 = order == SP_ORDER_STRIPED ? u : p;
+  tma_load_5d(dst, map, bar, 0, h, c2, c3, b);
+  tma_load_5d(dst + half, map, bar, 64, h, c2, c3, b);
+}
+
+// K-major bf16 tile of 128 columns (two 64-column halves `half` bytes apart,
+// 128-byte swizzle): descriptor of k-step kk (16 columns).
+__device__ __forceinline__ uint64_t kmaj_desc(uint64_t base, int kk, int half = kHalfBytes) {
+  return base + ((((kk >> 2) * half) + (kk & 3) * 32) >> 4);
+}
+
+// ------------------------------------------------------------------ dQ
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ BwdMaps tm, BwdArgs a, int n_tiles_q) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t q_full, s_full, s_free, dq_full, done;
+  __shared__ uint64_t ds_full[2];  // per dS buffer
+  __shared__ uint64_t kv_full[kSlots], kv_empty[kSlots];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sq = smem_u32(smem), sdo = sq + kTileBytes, skv = sq + 2 * kTileBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // work item: heavy query positions first, heads innermost
+  const int BH = a.B * a.Hq;
+  const int pos = blockIdx.x / BH, bh = blockIdx.x % BH;
+  const int b = bh / a.Hq, h = bh % a.Hq, kvh = h / (a.Hq / a.Hkv);
+  const int rev = a.P * n_tiles_q - 1 - pos;
+  const int i = rev / n_tiles_q, qt = rev % n_tiles_q;
+  const int Lb = a.S / a.P, u0 = qt * kT;
+  int hull_lo, hull_hi;
+  {
+    const int u_last = min(u0 + kT, Lb) - 1;
+    const int t_first = static_cast<int>(block_token(a.order, a.S, a.P, i, u0));
+    const int t_last = static_cast<int>(block_token(a.order, a.S, a.P, i, u_last));
+    if (a.doc_start) {
+      hull_lo = a.doc_start[static_cast<long long>(b % a.pos_rows) * a.S + t_first];
+      hull_hi = t_last;
+    } else {
+      hull_lo = 0;
+      hull_hi = a.S - 1;
+    }
+  }
+  int n_tiles = 0;
+  for (int s = 0; s < a.P; ++s) {
+    int kt0, kt1;
+    block_tiles(a.order, a.S, a.P, ((i - s) % a.P + a.P) % a.P, hull_lo, hull_hi, kT, kt0, kt1);
+    n_tiles += kt1 - kt0 + 1;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&q_full), 1);
+    mbar_init(smem_u32(&s_full), 1);
+    mbar_init(smem_u32(&s_free), kT);
+    mbar_init(smem_u32(&ds_full[0]), kT);
+    mbar_init(smem_u32(&ds_full[1]), kT);
+    mbar_init(smem_u32(&dq_full), 1);
+    mbar_init(smem_u32(&done), 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(smem_u32(&kv_full[s]), 1);
+      mbar_init(smem_u32(&kv_empty[s]), 1);
+    }
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  volatile int* abort_flag = &abort_s;
+  // TMEM columns: S [0,128) dP [128,256) dQ [256,384) dS buffers [384,448) [448,512)
+  const uint32_t cS = 0, cdP = 128, cdQ = 256, cdS = 384;
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      prefetch_tmap(&tm.q);
+      prefetch_tmap(&tm.dout);
+      prefetch_tmap(&tm.k);
+      prefetch_tmap(&tm.v);
+      const uint32_t qf = smem_u32(&q_full);
+      mbar_arrive_expect_tx(qf, 2 * kTileBytes);
+      row_tma(sq, &tm.q, qf, h, a.order, i, u0, b);
+      row_tma(sdo, &tm.dout, qf, h, a.order, i, u0, b);
+      int n = 0;
+      bool ok = true;
+      for (int s = 0; s < a.P && ok; ++s) {
+        const int j = ((i - s) % a.P + a.P) % a.P;
+        int kt0, kt1;
+        block_tiles(a.order, a.S, a.P, j, hull_lo, hull_hi, kT, kt0, kt1);
+        for (int kt = kt0; kt <= kt1 && ok; ++kt) {
+          for (int kv = 0; kv < 2; ++kv, ++n) {
+            const int slot = n % kSlots;
+            if (!mbar_wait(smem_u32(&kv_empty[slot]), ((n / kSlots) & 1) ^ 1, abort_flag, a.err,
+                           kErrBwdKvEmpty)) {
+              ok = false;
+              break;
+            }
+            const uint32_t full = smem_u32(&kv_full[slot]);
+            mbar_arrive_expect_tx(full, kTileBytes);
+            row_tma(skv + slot * kTileBytes, kv == 0 ? &tm.k : &tm.v, full, kvh, a.order, j,
+                    kt * kT, b);
+          }
+        }
+      }
+      mbar_wait(qf, 0, abort_flag, a.err, kErrBwdDrain);
+      for (int m = n - 1; m >= 0 && m >= n - kSlots; --m)
+        mbar_wait(smem_u32(&kv_full[m % kSlots]), (m / kSlots) & 1, abort_flag, a.err,
+                  kErrBwdDrain);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0 && n_tiles > 0) {
+      const uint64_t dq_ = smem_desc_sw128(sq, 16, 1024), ddo = smem_desc_sw128(sdo, 16, 1024);
+      const uint64_t dkv = smem_desc_sw128(skv, 16, 1024);          // K-major view of a slot
+      const uint64_t dkmn = smem_desc_sw128(skv, kHalfBytes, 1024);  // MN-major view (K as B of dS K)
+      // S = Q K^T and dP = dO V^T for tile t (K_t at load 2t, V_t at 2t + 1)
+      auto issue_sdp = [&](int t) {
+        const uint64_t kb = dkv + ((((2 * t) % kSlots) * kTileBytes) >> 4);
+        const uint64_t vb = dkv + ((((2 * t + 1) % kSlots) * kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + cS, kmaj_desc(dq_, kk), kmaj_desc(kb, kk), kIdescKmaj, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + cdP, kmaj_desc(ddo, kk), kmaj_desc(vb, kk), kIdescKmaj, kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&s_full));
+      };
+      auto wait_kv = [&](int t) -> bool {
+        for (int m = 2 * t; m <= 2 * t + 1; ++m)
+          if (!mbar_wait(smem_u32(&kv_full[m % kSlots]), (m / kSlots) & 1, abort_flag, a.err,
+                         kErrBwdKvFull))
+            return false;
+        tc_fence_after();
+        return true;
+      };
+      bool ok = mbar_wait(smem_u32(&q_full), 0, abort_flag, a.err, kErrBwdQFull) && wait_kv(0);
+      if (ok) issue_sdp(0);
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        if (!mbar_wait(smem_u32(&s_free), t & 1, abort_flag, a.err, kErrBwdSFree)) break;
+        if (t + 1 < n_tiles) {
+          if (!wait_kv(t + 1)) break;
+          issue_sdp(t + 1);
+        }
+        if (!mbar_wait(smem_u32(&ds_full[t & 1]), (t >> 1) & 1, abort_flag, a.err, kErrBwdDsFull))
+          break;
+        tc_fence_after();
+        // dQ += dS K: dS (bf16 pairs) from TMEM, K_t as the MN-major B operand
+        const uint64_t kmn = dkmn + ((((2 * t) % kSlots) * kTileBytes) >> 4);
+        const uint32_t ds = tmem + cdS + (t & 1) * 64;
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_ts(tmem + cdQ, ds + kk * 8, kmn + ((kk * 16 * 128) >> 4), kIdescBmn,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&kv_empty[(2 * t) % kSlots]));
+        mma_commit(smem_u32(&kv_empty[(2 * t + 1) % kSlots]));
+      }
+      mma_commit(smem_u32(&dq_full));
+      mma_commit(smem_u32(&done));
+      mbar_wait(smem_u32(&done), 0, abort_flag, a.err, kErrBwdDrain);
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------- elementwise warps
+    const int row = threadIdx.x;  // TMEM lane == query row of the tile
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int u = u0 + row;
+    const bool row_live = u < Lb;
+    const int tq = row_live ? static_cast<int>(block_token(a.order, a.S, a.P, i, u)) : 0;
+    const long long li = (static_cast<long long>(b) * a.Hq + h) * a.S + tq;
+    const float lse2 = row_live ? a.lse[li] * kLog2e : 0.f;
+    const float Drow = row_live ? a.Dsum[li] : 0.f;
+    int lo = 0, hi = a.S - 1;
+    if (a.doc_start && row_live) {
+      lo = a.doc_start[static_cast<long long>(b % a.pos_rows) * a.S + tq];
+      hi = tq;
+    }
+    const float sl2 = a.scale * kLog2e;
+    int t = 0;
+    bool ok = true;
+    for (int s = 0; s < a.P && ok; ++s) {
+      const int j = ((i - s) % a.P + a.P) % a.P;
+      int kt0, kt1;
+      block_tiles(a.order, a.S, a.P, j, hull_lo, hull_hi, kT, kt0, kt1);
+      for (int kt = kt0; kt <= kt1; ++kt, ++t) {
+        const bool got = mbar_wait(smem_u32(&s_full), t & 1, abort_flag, a.err, kErrBwdSFull);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        int c_lo, c_hi;
+        col_bounds(a.order, a.S, a.P, j, kt, lo, hi, c_lo, c_hi);
+        if (!row_live) {
+          c_lo = 0;
+          c_hi = -1;
+        }
+        uint32_t dsw[kT / 2];  // dS row, bf16 pairs
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t sx[64], px[64];
+          tmem_ld32_at(tmem + lane_base + cS + half * 64, sx, 0);
+          tmem_ld32_at(tmem + lane_base + cS + half * 64 + 32, sx, 32);
+          tmem_ld32_at(tmem + lane_base + cdP + half * 64, px, 0);
+          tmem_ld32_at(tmem + lane_base + cdP + half * 64 + 32, px, 32);
+          tmem_wait_ld();
+          if (half == 1) {  // S and dP fully read: the next tile's MMAs may start
+            tc_fence_before();
+            mbar_arrive(smem_u32(&s_free));
+          }
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const int col = half * 64 + c;
+            float p0 = ex2(fmaf(__uint_as_float(sx[c]), sl2, -lse2));
+            float p1 = ex2(fmaf(__uint_as_float(sx[c + 1]), sl2, -lse2));
+            if (col < c_lo || col > c_hi) p0 = 0.f;
+            if (col + 1 < c_lo || col + 1 > c_hi) p1 = 0.f;
+            const float d0 = p0 * (__uint_as_float(px[c]) - Drow);
+            const float d1 = p1 * (__uint_as_float(px[c + 1]) - Drow);
+            dsw[col >> 1] = pack_bf16(d0, d1);
+          }
+        }
+        const uint32_t dsb = tmem + lane_base + cdS + (t & 1) * 64;
+        tmem_st32(dsb, *reinterpret_cast<uint32_t(*)[32]>(&dsw[0]));
+        tmem_st32(dsb + 32, *reinterpret_cast<uint32_t(*)[32]>(&dsw[32]));
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&ds_full[t & 1]));
+      }
+    }
+    // epilogue: dQ * scale
+    const bool have = n_tiles > 0 && ok;
+    if (have) {
+      const bool got = mbar_wait(smem_u32(&dq_full), 0, abort_flag, a.err, kErrBwdOut);
+      if (!__all_sync(0xffffffffu, got)) ok = false;
+    }
+    tc_fence_after();
+    __nv_bfloat16* dq = static_cast<__nv_bfloat16*>(a.dq);
+    uint4* orow = reinterpret_cast<uint4*>(dq + ((static_cast<long long>(b) * a.S + tq) * a.Hq + h) * kD);
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t r[32];
+      if (have && ok) {
+        tmem_ld32(tmem + lane_base + cdQ + c * 32, r);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) r[e] = 0u;
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        pk[e] = pack_bf16(__uint_as_float(r[2 * e]) * a.scale, __uint_as_float(r[2 * e + 1]) * a.scale);
+      if (row_live) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          orow[c * 4 + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// --------------------------------------------------------------- dK / dV
+constexpr int kQT = 64;                      // query rows per streamed tile
+constexpr int kQTileBytes = kQT * kD * 2;    // 16 KiB
+constexpr int kQHalf = kQTileBytes / 2;
+constexpr int kQSlots = 4;
+constexpr int kKvSmemBytes = 2 * kTileBytes + kQSlots * 2 * kQTileBytes;
+constexpr uint32_t kIdescST = idesc_bf16_f32(kT, kQT, false);  // 128 keys x 64 queries
+
+enum : int { kInfoEnd = 0, kInfoTile = 1, kInfoFull = 3 };
+
+// Per-column data of one streamed query tile, written by the producer warp.
+struct alignas(16) ColData {
+  float lse2[kQT];  // lse * log2(e); +inf for rows past the end of the block
+  float D[kQT];
+  int lo[kQT];      // a key token x is allowed for the column's query iff lo <= x <= hi
+  int hi[kQT];
+  int info;         // kInfoEnd, kInfoTile (masked per pair) or kInfoFull (every pair allowed)
+};
+
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err, int code) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err, code));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ BwdMaps tm, BwdArgs a, int n_tiles_k) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t q_full[kQSlots], q_empty[kQSlots], kv_full, s_full[2], ds_full[2],
+      dkv_full, done;
+  __shared__ ColData cols[kQSlots];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sk = smem_u32(smem), sv = sk + kTileBytes, sslot = sk + 2 * kTileBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // work item: earliest key tiles first (for causal calls they meet the most queries)
+  const int BH = a.B * a.Hkv;
+  const int pos = blockIdx.x / BH, bh = blockIdx.x % BH;
+  const int b = bh / a.Hkv, hk = bh % a.Hkv;
+  const int j = pos / n_tiles_k, kt = pos % n_tiles_k;
+  const int Lb = a.S / a.P, w0 = kt * kT;
+  const int k_first = static_cast<int>(block_token(a.order, a.S, a.P, j, w0));
+  const int k_last = static_cast<int>(block_token(a.order, a.S, a.P, j, min(w0 + kT, Lb) - 1));
+  const int32_t* ds_row =
+      a.doc_start ? a.doc_start + static_cast<long long>(b % a.pos_rows) * a.S : nullptr;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQSlots; ++s) {
+      mbar_init(smem_u32(&q_full[s]), 32);
+      mbar_init(smem_u32(&q_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&kv_full), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&s_full[s]), 1);
+      mbar_init(smem_u32(&ds_full[s]), kT);
+    }
+    mbar_init(smem_u32(&dkv_full), 1);
+    mbar_init(smem_u32(&done), 1);
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  volatile int* abort_flag = &abort_s;
+  // TMEM columns: S^T buffers [0,64) [64,128), dP^T buffers [128,192) [192,256),
+  // dV [256,384), dK [384,512).  P^T and dS^T (bf16 pairs) overwrite the
+  // first 32 columns of their S^T / dP^T buffer.
+  const uint32_t cdP = 128, cdV = 256, cdK = 384;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    const int G = a.Hq / a.Hkv;
+    if (lane == 0) {
+      prefetch_tmap(&tm.k);
+      prefetch_tmap(&tm.v);
+      prefetch_tmap(&tm.q);
+      prefetch_tmap(&tm.dout);
+      const uint32_t kf = smem_u32(&kv_full);
+      mbar_arrive_expect_tx(kf, 2 * kTileBytes);
+      row_tma(sk, &tm.k, kf, hk, a.order, j, w0, b);
+      row_tma(sv, &tm.v, kf, hk, a.order, j, w0, b);
+    }
+    int n = 0;
+    bool ok = true;
+    for (int g = 0; g < G && ok; ++g) {
+      const int h = hk * G + g;
+      for (int s = 0; s < a.P && ok; ++s) {
+        const int i = (j + s) % a.P;
+        int qt0, qt1;
+        block_tiles(a.order, a.S, a.P, i, ds_row ? k_first : 0, a.S - 1, kQT, qt0, qt1);
+        for (int qt = qt0; qt <= qt1 && ok; ++qt) {
+          const int u0 = qt * kQT;
+          const int tq_first = static_cast<int>(block_token(a.order, a.S, a.P, i, u0));
+          const int tq_last =
+              static_cast<int>(block_token(a.order, a.S, a.P, i, min(u0 + kQT, Lb) - 1));
+          int info = kInfoFull;
+          if (ds_row) {
+            // document starts do not decrease along the tokens of a block, so
+            // once a tile starts past the keys' documents the rest do too
+            if (ds_row[tq_first] > k_last) break;
+            if (!(k_last <= tq_first && ds_row[tq_last] <= k_first)) info = kInfoTile;
+          }
+          float l2[2], dd[2];
+          int lo[2], hi[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int u = u0 + lane + 32 * e;
+            if (u < Lb) {
+              const int tq = static_cast<int>(block_token(a.order, a.S, a.P, i, u));
+              const long long li = (static_cast<long long>(b) * a.Hq + h) * a.S + tq;
+              l2[e] = a.lse[li] * kLog2e;
+              dd[e] = a.Dsum[li];
+              lo[e] = ds_row ? ds_row[tq] : 0;
+              hi[e] = ds_row ? tq : a.S - 1;
+            } else {
+              l2[e] = INFINITY;
+              dd[e] = 0.f;
+              lo[e] = 1;
+              hi[e] = 0;
+            }
+          }
+          const int slot = n % kQSlots;
+          if (!wait_warp(smem_u32(&q_empty[slot]), ((n / kQSlots) & 1) ^ 1, abort_flag, a.err,
+                         kErrBwdKvEmpty)) {
+            ok = false;
+            break;
+          }
+          ColData& cd = cols[slot];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = lane + 32 * e;
+            cd.lse2[c] = l2[e];
+            cd.D[c] = dd[e];
+            cd.lo[c] = lo[e];
+            cd.hi[c] = hi[e];
+          }
+          const uint32_t full = smem_u32(&q_full[slot]);
+          if (lane == 0) {
+            cd.info = info;
+            const uint32_t dst = sslot + slot * 2 * kQTileBytes;
+            mbar_arrive_expect_tx(full, 2 * kQTileBytes);
+            row_tma(dst, &tm.q, full, h, a.order, i, u0, b, kQHalf);
+            row_tma(dst + kQTileBytes, &tm.dout, full, h, a.order, i, u0, b, kQHalf);
+          } else {
+            mbar_arrive(full);
+          }
+          ++n;
+        }
+      }
+    }
+    if (ok) {  // end of the list
+      const int slot = n % kQSlots;
+      if (wait_warp(smem_u32(&q_empty[slot]), ((n / kQSlots) & 1) ^ 1, abort_flag, a.err,
+                    kErrBwdKvEmpty)) {
+        if (lane == 0) cols[slot].info = kInfoEnd;
+        mbar_arrive(smem_u32(&q_full[slot]));
+      }
+    }
+    // copies still in flight land before the CTA can exit
+    if (lane == 0) {
+      mbar_wait(smem_u32(&kv_full), 0, abort_flag, a.err, kErrBwdDrain);
+      for (int m = n - 1; m >= 0 && m > n - kQSlots; --m)
+        mbar_wait(smem_u32(&q_full[m % kQSlots]), (m / kQSlots) & 1, abort_flag, a.err,
+                  kErrBwdDrain);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint64_t dk0 = smem_desc_sw128(sk, 16, 1024), dv0 = smem_desc_sw128(sv, 16, 1024);
+      const uint64_t dkq = smem_desc_sw128(sslot, 16, 1024);      // K-major Q / dO views
+      const uint64_t dmn = smem_desc_sw128(sslot, kQHalf, 1024);  // MN-major Q / dO views
+      // info of tile t once its slot is full; -1 when the wait gave up
+      auto tile_info = [&](int t) -> int {
+        const int slot = t % kQSlots;
+        if (!mbar_wait(smem_u32(&q_full[slot]), (t / kQSlots) & 1, abort_flag, a.err,
+                       kErrBwdQFull))
+          return -1;
+        return cols[slot].info;
+      };
+      // S^T = K Q^T and dP^T = V dO^T for tile t, into buffer t & 1
+      auto issue_sdp = [&](int t) {
+        tc_fence_after();
+        const uint64_t qb = dkq + (((t % kQSlots) * 2 * kQTileBytes) >> 4);
+        const uint64_t ob = qb + (kQTileBytes >> 4);
+        const uint32_t buf = (t & 1) * 64;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + buf, kmaj_desc(dk0, kk), kmaj_desc(qb, kk, kQHalf), kIdescST,
+                 kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + cdP + buf, kmaj_desc(dv0, kk), kmaj_desc(ob, kk, kQHalf), kIdescST,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&s_full[t & 1]));
+      };
+      // dV += P^T dO and dK += dS^T Q for tile t (64 queries: 4 k-steps)
+      auto issue_grad = [&](int t) {
+        const int slot = t % kQSlots;
+        const uint64_t qb = dmn + ((slot * 2 * kQTileBytes) >> 4);
+        const uint64_t ob = qb + (kQTileBytes >> 4);
+        const uint32_t buf = (t & 1) * 64;
+#pragma unroll
+        for (int kk = 0; kk < kQT / 16; ++kk)
+          mma_ts(tmem + cdV, tmem + buf + kk * 8, ob + ((kk * 16 * 128) >> 4), kIdescBmn,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kQT / 16; ++kk)
+          mma_ts(tmem + cdK, tmem + cdP + buf + kk * 8, qb + ((kk * 16 * 128) >> 4), kIdescBmn,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&q_empty[slot]));
+      };
+      bool ok = mbar_wait(smem_u32(&kv_full), 0, abort_flag, a.err, kErrBwdKvFull);
+      int cur = ok ? tile_info(0) : -1;
+      if (cur > 0) issue_sdp(0);
+      int nxt = cur > 0 ? tile_info(1) : 0;
+      if (nxt > 0) issue_sdp(1);
+      for (int t = 0; cur > 0; ++t) {
+        if (!mbar_wait(smem_u32(&ds_full[t & 1]), (t >> 1) & 1, abort_flag, a.err,
+                       kErrBwdDsFull))
+          break;
+        tc_fence_after();
+        issue_grad(t);
+        int nn = 0;
+        if (nxt > 0) {
+          nn = tile_info(t + 2);
+          if (nn > 0) issue_sdp(t + 2);
+        }
+        cur = nxt;
+        nxt = nn;
+      }
+      mma_commit(smem_u32(&dkv_full));
+      mma_commit(smem_u32(&done));
+      mbar_wait(smem_u32(&done), 0, abort_flag, a.err, kErrBwdDrain);
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------- elementwise warps
+    const int r = threadIdx.x;  // TMEM lane == key row of the tile
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int w = w0 + r;
+    const bool key_live = w < Lb;
+    const int ktok = key_live ? static_cast<int>(block_token(a.order, a.S, a.P, j, w)) : -1;
+    const float sl2 = a.scale * kLog2e;
+    int t = 0;
+    bool ok = true;
+    for (;; ++t) {
+      const int slot = t % kQSlots;
+      if (!wait_warp(smem_u32(&q_full[slot]), (t / kQSlots) & 1, abort_flag, a.err,
+                     kErrBwdQFull)) {
+        ok = false;
+        break;
+      }
+      const ColData& cd = cols[slot];
+      const int info = cd.info;
+      if (info == kInfoEnd) break;
+      if (!wait_warp(smem_u32(&s_full[t & 1]), (t >> 1) & 1, abort_flag, a.err, kErrBwdSFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t buf = (t & 1) * 64;
+      uint32_t sx[64], px[64];
+      tmem_ld32_at(tmem + lane_base + buf, sx, 0);
+      tmem_ld32_at(tmem + lane_base + buf + 32, sx, 32);
+      tmem_ld32_at(tmem + lane_base + cdP + buf, px, 0);
+      tmem_ld32_at(tmem + lane_base + cdP + buf + 32, px, 32);
+      tmem_wait_ld();
+      uint32_t pk[32], dk[32];
+      const bool full = info == kInfoFull;
+#pragma unroll
+      for (int c = 0; c < kQT; c += 2) {
+        const float2 l2 = *reinterpret_cast<const float2*>(&cd.lse2[c]);
+        const float2 D = *reinterpret_cast<const float2*>(&cd.D[c]);
+        float p0 = ex2(fmaf(__uint_as_float(sx[c]), sl2, -l2.x));
+        float p1 = ex2(fmaf(__uint_as_float(sx[c + 1]), sl2, -l2.y));
+        if (!full) {
+          const int2 lo = *reinterpret_cast<const int2*>(&cd.lo[c]);
+          const int2 hi = *reinterpret_cast<const int2*>(&cd.hi[c]);
+          if (ktok < lo.x || ktok > hi.x) p0 = 0.f;
+          if (ktok < lo.y || ktok > hi.y) p1 = 0.f;
+        }
+        const float d0 = p0 * (__uint_as_float(px[c]) - D.x);
+        const float d1 = p1 * (__uint_as_float(px[c + 1]) - D.y);
+        pk[c >> 1] = pack_bf16(p0, p1);
+        dk[c >> 1] = pack_bf16(d0, d1);
+      }
+      tmem_st32(tmem + lane_base + buf, pk);
+      tmem_st32(tmem + lane_base + cdP + buf, dk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&ds_full[t & 1]));
+    }
+    // epilogue: dK * scale and dV, rows of key token ktok
+    const bool have = t > 0 && ok;
+    if (have && !wait_warp(smem_u32(&dkv_full), 0, abort_flag, a.err, kErrBwdOut)) ok = false;
+    tc_fence_after();
+    const long long orow = ((static_cast<long long>(b) * a.S + (key_live ? ktok : 0)) * a.Hkv + hk) * kD;
+    uint4* dk_row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk) + orow);
+    uint4* dv_row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dv) + orow);
+#pragma unroll 1
+    for (int m = 0; m < 2; ++m) {
+      const float mul = m == 0 ? a.scale : 1.f;
+      uint4* dst = m == 0 ? dk_row : dv_row;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t x[32];
+        if (have && ok) {
+          tmem_ld32(tmem + lane_base + (m == 0 ? cdK : cdV) + c * 32, x);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16(__uint_as_float(x[2 * e]) * mul, __uint_as_float(x[2 * e + 1]) * mul);
+        if (key_live) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[c * 4 + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// D[b][h][t] = sum_c dout[b][t][h][c] * out[b][t][h][c] for d = 128 bf16 rows:
+// 16 lanes per row, one 16-byte load of each tensor per lane.
+__global__ void __launch_bounds__(256) bwd_rowsum_bf16_kernel(const uint4* __restrict__ out,
+                                                              const uint4* __restrict__ dout,
+                                                              int B, int S, int H,
+                                                              float* __restrict__ D) {
+  const long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long row = g >> 4;
+  const bool live = row < static_cast<long long>(B) * S * H;
+  float acc = 0.f;
+  if (live) {
+    const uint4 x = __ldcs(out + g), y = __ldcs(dout + g);
+    const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[e]));
+      const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[e]));
+      acc = fmaf(xf.x, yf.x, acc);
+      acc = fmaf(xf.y, yf.y, acc);
+    }
+  }
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (live && (threadIdx.x & 15) == 0) {
+    const int h = static_cast<int>(row % H);
+    const long long bt = row / H;
+    D[(bt / S * H + h) * S + bt % S] = acc;
+  }
+}
+
+}  // namespace
+
+// D, then dQ and dK/dV (independent of each other) on the tensor cores.
+int launch_attn_bwd_bf16(const BwdArgs& a, cudaStream_t st) {
+  BwdMaps tm;
+  if (!tmap::make_map(&tm.q, a.q, a.B, a.S, a.Hq, a.P, a.order) ||
+      !tmap::make_map(&tm.dout, a.dout, a.B, a.S, a.Hq, a.P, a.order) ||
+      !tmap::make_map(&tm.k, a.k, a.B, a.S, a.Hkv, a.P, a.order) ||
+      !tmap::make_map(&tm.v, a.v, a.B, a.S, a.Hkv, a.P, a.order))
+    return -1;
+  const long long rows = static_cast<long long>(a.B) * a.S * a.Hq;
+  bwd_rowsum_bf16_kernel<<<static_cast<unsigned>((rows * 16 + 255) / 256), 256, 0, st>>>(
+      static_cast<const uint4*>(a.out), static_cast<const uint4*>(a.dout), a.B, a.S, a.Hq,
+      a.Dsum);
+  const int Lb = a.S / a.P, n_tiles = (Lb + kT - 1) / kT;
+  const int dq_smem = kSmemBytes + 1024, kv_smem = kKvSmemBytes + 1024;
+  if (cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kv_smem) != cudaSuccess)
+    return -1;
+  const unsigned n_q = static_cast<unsigned>(a.P) * n_tiles * a.B * a.Hq;
+  bwd_dq_kernel<<<n_q, kThreads, dq_smem, st>>>(tm, a, n_tiles);
+  BwdMaps tk;  // the dK/dV kernel streams 64-row query tiles
+  tk.k = tm.k;
+  tk.v = tm.v;
+  if (!tmap::make_map(&tk.q, a.q, a.B, a.S, a.Hq, a.P, a.order, kQT) ||
+      !tmap::make_map(&tk.dout, a.dout, a.B, a.S, a.Hq, a.P, a.order, kQT))
+    return -1;
+  const unsigned n_kv = static_cast<unsigned>(a.P) * n_tiles * a.B * a.Hkv;
+  bwd_dkdv_kernel<<<n_kv, kThreads, kv_smem, st>>>(tk, a, n_tiles);
+  return cudaGetLastError() == cudaSuccess ? 3 : -1;
+}
+
+}  // namespace sp

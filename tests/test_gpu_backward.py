@@ -52,6 +52,8 @@ def test_backward_f32(sp, B, S, Hq, Hkv, d, P, order, pos):
     (1, 768, 2, 2, 4, "striped", "packed"),
     (2, 256, 2, 1, 1, "contiguous", "none"),
     (1, 1000, 2, 1, 2, "striped", "none"),          # ragged blocks of 500
+    (1, 2048, 8, 2, 4, "contiguous", "packed"),     # GQA group of 4, documents across blocks
+    (1, 1416, 4, 4, 3, "striped", "causal"),        # ragged tiles: blocks of 472 rows
 ])
 def test_backward_bf16(sp, B, S, Hq, Hkv, P, order, pos):
     _run_bwd(sp, "bf16", B, S, Hq, Hkv, 128, P, order, pos, 850 + S)

@@ -130,3 +130,31 @@ def test_backward_planted_mistakes_are_caught():
     D = (doh * (p_ @ vh)).sum(axis=1)
     ds = p_ * (dp - D[:, None])
     assert np.abs(scale * ds @ qh - tk[0, :, 0]).max() > 1e-3   # dS instead of dS^T
+
+
+@pytest.mark.parametrize("case", ["noncausal", "causal", "packed"])
+def test_sampled_rows_and_keys_match_autograd(case):
+    """The sampled-row (dq) and sampled-key (dk, dv) forms against float64
+    autograd on the whole problem, GQA group of 3."""
+    B, S, Hq, Hkv, d = 2, 37, 6, 2, 8
+    q, k, v, do = (_rand((B, S, h, d), s) for s, h in ((11, Hq), (12, Hkv), (13, Hkv), (14, Hq)))
+    if case == "noncausal":
+        pos, mask = None, None
+    elif case == "causal":
+        pos = np.tile(np.arange(S)[None, :], (B, 1))
+        mask = np.tril(np.ones((S, S), dtype=bool))
+    else:
+        pos = np.tile(_packed([10, 1, 15, 11]), (B, 1))
+        mask = oracle.allowed_mask(pos, 1, S)[0]
+    scale = 0.3
+    tq, tk, tv = _torch_grads(q, k, v, do, mask, scale)
+    rows = np.array([0, 5, 10, 11, 20, 36])
+    keys = np.array([0, 9, 10, 11, 25, 36])
+    dq = oracle.attention_backward_rows(q, k, v, do, rows, pos, scale, max_chunk_elems=64)
+    assert np.abs(dq - tq[:, rows]).max() < 1e-12
+    dk, dv = oracle.attention_backward_keys(q, k, v, do, keys, pos, scale, max_chunk_elems=64)
+    assert np.abs(dk - tk[:, keys]).max() < 1e-12
+    assert np.abs(dv - tv[:, keys]).max() < 1e-12
+    dk1, dv1 = oracle.attention_backward_keys(q, k, v, do, keys, pos, scale, kv_heads=[1])
+    assert np.abs(dk1[:, :, 1] - tk[:, keys, 1]).max() < 1e-12
+    assert not dk1[:, :, 0].any() and not dv1[:, :, 0].any()
