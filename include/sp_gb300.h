@@ -264,10 +264,10 @@ sp_status sp_blockwise_attn_fwd_noalloc(const void* q, const void* k, const void
  * P and dS are rounded to bf16 before they enter the dV, dQ and dK products;
  * every tensor pointer 16-byte aligned, else SP_ERR_INVALID_ARG), SP_F32
  * with d <= 256 (CUDA cores, float32 throughout).  workspace:
- * sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, position_ids != NULL)
+ * sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, P, position_ids != NULL)
  * bytes, 256-byte aligned.  Errors as for sp_blockwise_attn_fwd.
  * ------------------------------------------------------------------------ */
-size_t sp_blockwise_attn_bwd_workspace_bytes(int B, int S, int Hq, int causal);
+size_t sp_blockwise_attn_bwd_workspace_bytes(int B, int S, int Hq, int P, int causal);
 sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const void* v, const void* out,
                                 const void* dout, const float* lse, const int32_t* position_ids,
                                 int B, int S, int Hq, int Hkv, int d, int P, sp_block_order order,

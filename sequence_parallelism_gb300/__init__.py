@@ -83,7 +83,7 @@ def blockwise_attention_backward(q, k, v, out, dout, lse, P, order="contiguous",
     """Gradients (dq, dk, dv) of blockwise attention; lse from the forward."""
     B, S, Hq, d = q.shape
     if workspace is None:
-        n = _lib.sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, position_ids is not None)
+        n = _lib.sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, P, position_ids is not None)
         workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     return _lib.sp_blockwise_attn_bwd(q, k, v, out, dout, lse, position_ids, P, order, scale, dq,

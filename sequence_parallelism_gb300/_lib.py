@@ -64,7 +64,7 @@ def _load():
         "sp_ulysses_ring_attn_workspace_bytes": (sz, [i, i, i, i, i, i, i]),
         "sp_ulysses_ring_attn_fwd": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp,
                                          sz, vp]),
-        "sp_blockwise_attn_bwd_workspace_bytes": (sz, [i, i, i, i]),
+        "sp_blockwise_attn_bwd_workspace_bytes": (sz, [i, i, i, i, i]),
         "sp_blockwise_attn_bwd": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp,
                                       vp, vp, vp, sz, vp]),
         "sp_attn_merge_partials": (i, [vp, vp, i, i, i, i, i, i, vp, vp, vp]),
@@ -222,8 +222,8 @@ def sp_ulysses_ring_attn_fwd(q, k, v, position_ids, P_u, P_r, order, scale, out,
     return out, lse
 
 
-def sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, causal):
-    return _lib.sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, int(bool(causal)))
+def sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, P, causal):
+    return _lib.sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, P, int(bool(causal)))
 
 
 def sp_blockwise_attn_bwd(q, k, v, out, dout, lse, position_ids, P, order, scale, dq, dk, dv,

@@ -1,11 +1,15 @@
 // api_bwd.cu -- entry point of the attention backward: checks, workspace
 // layout, dispatch.
 //
-// Workspace layout (256-byte aligned, caller-owned):
+// Workspace layout (256-byte aligned, caller-owned; Lbp = S/P rounded up to
+// a multiple of 64):
 //   [0, 256)                      error word + reserved
-//   [256, +B*Hq*S*4)              D = rowsum(dout * out) per query row, fp32
-//   [.., +B*S*4)                  doc_start (causal only)
-//   [.., + scan scratch)          doc_start scan scratch (causal only)
+//   D                             rowsum(dout * out), fp32: [B][Hq][S] (f32
+//                                 path) or [B][Hq][P][Lbp] (bf16 path)
+//   lse2                          [B][Hq][P][Lbp] lse * log2(e) (bf16 path)
+//   lo                            [B][P][Lbp] doc_start in block order (causal)
+//   doc_start                     [B][S] (causal only)
+//   scan scratch                  doc_start scan (causal only)
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -16,24 +20,31 @@ namespace sp {
 namespace {
 
 struct BwdLayout {
-  size_t dsum, doc, scan, total;
+  size_t dsum, lse2, lo, doc, scan, total;
+  int Lbp;
 };
 
-BwdLayout bwd_layout(int B, int S, int Hq, int causal) {
+BwdLayout bwd_layout(int B, int S, int Hq, int P, int causal) {
   BwdLayout L;
-  L.dsum = round_up(static_cast<size_t>(B) * Hq * S * sizeof(float), 256);
+  L.Lbp = static_cast<int>(round_up(static_cast<size_t>(S / P), kBwdRowPad));
+  const size_t blk = static_cast<size_t>(B) * Hq * P * L.Lbp * sizeof(float);
+  const size_t tok = static_cast<size_t>(B) * Hq * S * sizeof(float);
+  L.dsum = round_up(blk > tok ? blk : tok, 256);
+  L.lse2 = round_up(blk, 256);
+  L.lo = causal ? round_up(static_cast<size_t>(B) * P * L.Lbp * sizeof(int32_t), 256) : 0;
   L.doc = causal ? round_up(static_cast<size_t>(B) * S * sizeof(int32_t), 256) : 0;
   L.scan = causal ? segment_scratch_bytes(B, S) : 0;
-  L.total = kWsHeaderBytes + L.dsum + L.doc + L.scan;
+  L.total = kWsHeaderBytes + L.dsum + L.lse2 + L.lo + L.doc + L.scan;
   return L;
 }
 
 }  // namespace
 }  // namespace sp
 
-extern "C" size_t sp_blockwise_attn_bwd_workspace_bytes(int B, int S, int Hq, int causal) {
-  if (B < 1 || S < 1 || Hq < 1) return 0;
-  return sp::bwd_layout(B, S, Hq, causal).total;
+extern "C" size_t sp_blockwise_attn_bwd_workspace_bytes(int B, int S, int Hq, int P,
+                                                        int causal) {
+  if (B < 1 || S < 1 || Hq < 1 || P < 1 || S % P != 0) return 0;
+  return sp::bwd_layout(B, S, Hq, P, causal).total;
 }
 
 extern "C" sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const void* v,
@@ -59,7 +70,7 @@ extern "C" sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const v
       if (!sp::aligned(p, 16)) return SP_ERR_INVALID_ARG;
   }
   const int causal = position_ids != nullptr;
-  const sp::BwdLayout L = sp::bwd_layout(B, S, Hq, causal);
+  const sp::BwdLayout L = sp::bwd_layout(B, S, Hq, P, causal);
   if (!workspace || !sp::aligned(workspace, 256) || workspace_bytes < L.total)
     return SP_ERR_WORKSPACE;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -73,6 +84,11 @@ extern "C" sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const v
   a.lse = lse;
   a.err = reinterpret_cast<int*>(ws);
   a.Dsum = reinterpret_cast<float*>(ws + sp::kWsHeaderBytes);
+  a.D_blk = a.Dsum;
+  a.lse2_blk = reinterpret_cast<float*>(ws + sp::kWsHeaderBytes + L.dsum);
+  a.lo_blk = causal ? reinterpret_cast<int32_t*>(ws + sp::kWsHeaderBytes + L.dsum + L.lse2)
+                    : nullptr;
+  a.Lbp = L.Lbp;
   a.doc_start = nullptr;
   a.dq = dq;
   a.dk = dk;
@@ -90,9 +106,9 @@ extern "C" sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const v
   int launches = 0;
   if (cudaMemsetAsync(a.err, 0, sizeof(int), st) != cudaSuccess) return SP_ERR_CUDA;
   if (causal) {
-    int32_t* doc = reinterpret_cast<int32_t*>(ws + sp::kWsHeaderBytes + L.dsum);
-    const int n = sp::launch_segment_starts(position_ids, doc, B, S,
-                                            ws + sp::kWsHeaderBytes + L.dsum + L.doc, st);
+    uint8_t* base = ws + sp::kWsHeaderBytes + L.dsum + L.lse2 + L.lo;
+    int32_t* doc = reinterpret_cast<int32_t*>(base);
+    const int n = sp::launch_segment_starts(position_ids, doc, B, S, base + L.doc, st);
     if (n < 0) return SP_ERR_CUDA;
     launches += n;
     a.doc_start = doc;

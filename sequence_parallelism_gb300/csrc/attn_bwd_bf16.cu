@@ -6,22 +6,29 @@
 // tokens" -- but print no backward):
 //   P = exp(scale * Q K^T - lse), dP = dO V^T, dS = P * (dP - D),
 //   dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO,
-// D_t = sum_c dO[t, c] O[t, c] (computed by the rowsum kernel first).
+// D_t = sum_c dO[t, c] O[t, c].
 //
-// Two kernels, no atomics:
+// Three kernels, no atomics:
+//  * prep: D per query row, and lse * log2(e), D and the document starts
+//    rewritten in block order (each block padded to a multiple of 64 rows), so
+//    that the dK/dV kernel fetches a query tile's per-column data with three
+//    contiguous bulk copies.
 //  * dQ: query-stationary.  One CTA keeps a 128-row Q tile and its dO tile in
 //    shared memory and walks the key/value blocks in ring order
 //    j = (i - s) mod P ("Ring Attention", "Cómo funciona la atención en
-//    anillo").  Per key tile: S = Q K^T and dP = dO V^T (SS MMAs), dS from
-//    P and dP in the elementwise warps, dQ += dS K with dS read from TMEM.
+//    anillo").  Per key tile: S = Q K^T and dP = dO V^T (SS MMAs); two
+//    elementwise warpgroups, one per 64 columns, read S and dP at once (so the
+//    next tile's MMAs start), form dS = P * (dP - D) and store it to TMEM as
+//    bf16; dQ += dS K reads dS from TMEM.
 //  * dK/dV: key-stationary.  One CTA keeps a 128-key K tile and V tile and
 //    walks, for every query head of the GQA group, the query blocks in the
-//    order its key block meets them on the ring, i = (j + s) mod P.  Per query
-//    tile: S^T = K Q^T and dP^T = V dO^T, then P^T and dS^T, then
-//    dV += P^T dO and dK += dS^T Q with P^T / dS^T read from TMEM.
-// Warp roles as in the forward: 4 elementwise warps (one thread per TMEM
-// lane = tile row), a TMA producer warp and an MMA warp (TMEM owner).  Every
-// barrier wait is bounded.
+//    order its key block meets them on the ring, i = (j + s) mod P, in tiles
+//    of 64 queries.  Per tile: S^T = K Q^T and dP^T = V dO^T into one of two
+//    TMEM buffers, P^T and dS^T written back over them as bf16, then
+//    dV += P^T dO and dK += dS^T Q read them from TMEM.
+// Warp roles: elementwise warps (one thread per TMEM lane = tile row), a TMA
+// producer warp and an MMA warp (TMEM owner).  Every barrier wait is bounded.
+#include <climits>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,14 +44,10 @@ namespace {
 using namespace ptx;
 
 constexpr int kD = 128;
-constexpr int kT = 128;                      // rows per tile (queries or keys)
-constexpr int kSlots = 4;                    // streamed tile ring depth
+constexpr int kT = 128;                      // rows per resident tile
+constexpr int kSlots = 4;                    // streamed K/V tile ring depth (dQ)
 constexpr int kTileBytes = kT * kD * 2;      // 32 KiB
 constexpr int kHalfBytes = kTileBytes / 2;   // one 64-column half
-constexpr int kSmemBytes = (2 + kSlots) * kTileBytes;
-constexpr int kThreads = 192;                // 4 elementwise warps + TMA + MMA
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -60,7 +63,7 @@ struct BwdMaps {
   CUtensorMap q, k, v, dout;
 };
 
-__device__ __forceinline__ int floor_div_i(int a, int b) {
+__host__ __device__ __forceinline__ int floor_div_i(int a, int b) {
   return a >= 0 ? a / b : -((-a + b - 1) / b);
 }
 
@@ -125,8 +128,97 @@ __device__ __forceinline__ uint64_t kmaj_desc(uint64_t base, int kk, int half = 
   return base + ((((kk >> 2) * half) + (kk & 3) * 32) >> 4);
 }
 
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err, int code) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err, code));
+}
+
+// Offset of local row u of block p in a block-ordered [outer][P][Lbp] array.
+__device__ __forceinline__ long long blk_index(long long outer, int P, int Lbp, int p, int u) {
+  return (outer * P + p) * Lbp + u;
+}
+
+// ------------------------------------------------------------------ prep
+// Three index ranges in one launch:
+//  [0, nA)        16 lanes per query row (b, t, h): D = dout . out (16-byte
+//                 loads), written with lse * log2(e) at the row's block slot;
+//  [nA, +nB)      the padding slots u in [Lb, Lbp): D = 0, lse2 = +inf;
+//  [.., +nC)      doc_start in block order (INT_MAX in the padding), causal.
+// nA is a multiple of 32 so that no warp straddles the first two ranges.
+struct PrepArgs {
+  const uint4* out;
+  const uint4* dout;
+  const float* lse;
+  const int32_t* doc_start;
+  float* D_blk;
+  float* lse2_blk;
+  int32_t* lo_blk;
+  long long rows, nA, nB, nC;
+  int S, H, P, Lbp, order;
+};
+
+__global__ void __launch_bounds__(256) bwd_prep_kernel(PrepArgs pa) {
+  long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int Lb = pa.S / pa.P;
+  if (g < pa.nA) {
+    const long long row = g >> 4;
+    const bool live = row < pa.rows;
+    float acc = 0.f;
+    if (live) {
+      const uint4 x = __ldcs(pa.out + g), y = __ldcs(pa.dout + g);
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[e]));
+        const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[e]));
+        acc = fmaf(xf.x, yf.x, acc);
+        acc = fmaf(xf.y, yf.y, acc);
+      }
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (live && (threadIdx.x & 15) == 0) {
+      const int h = static_cast<int>(row % pa.H);
+      const long long bt = row / pa.H;
+      const int t = static_cast<int>(bt % pa.S);
+      const long long b = bt / pa.S;
+      const int p = pa.order == SP_ORDER_STRIPED ? t % pa.P : t / Lb;
+      const int u = pa.order == SP_ORDER_STRIPED ? t / pa.P : t % Lb;
+      const long long bh = b * pa.H + h;
+      const long long idx = blk_index(bh, pa.P, pa.Lbp, p, u);
+      pa.D_blk[idx] = acc;
+      pa.lse2_blk[idx] = pa.lse[bh * pa.S + t] * kLog2e;
+    }
+    return;
+  }
+  g -= pa.nA;
+  if (g < pa.nB) {
+    const int w = pa.Lbp - Lb;
+    const long long bhp = g / w;
+    const long long idx = bhp * pa.Lbp + Lb + g % w;
+    pa.D_blk[idx] = 0.f;
+    pa.lse2_blk[idx] = INFINITY;
+    return;
+  }
+  g -= pa.nB;
+  if (g < pa.nC) {
+    const int u = static_cast<int>(g % pa.Lbp);
+    const long long rp = g / pa.Lbp;
+    const int p = static_cast<int>(rp % pa.P);
+    const long long r = rp / pa.P;
+    pa.lo_blk[g] = u < Lb ? pa.doc_start[r * pa.S + block_token(pa.order, pa.S, pa.P, p, u)]
+                          : INT_MAX;
+  }
+}
+
 // ------------------------------------------------------------------ dQ
-__global__ void __launch_bounds__(kThreads, 1)
+constexpr int kQThreads = 320;  // warps 0-7 elementwise (two warpgroups), 8 TMA, 9 MMA
+constexpr int kQProducer = 8;
+constexpr int kQMma = 9;
+constexpr int kQEw = 256;       // elementwise threads
+constexpr int kQSmemBytes = (2 + kSlots) * kTileBytes;
+
+__global__ void __launch_bounds__(kQThreads, 1)
     bwd_dq_kernel(const __grid_constant__ BwdMaps tm, BwdArgs a, int n_tiles_q) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t q_full, s_full, s_free, dq_full, done;
@@ -169,9 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&q_full), 1);
     mbar_init(smem_u32(&s_full), 1);
-    mbar_init(smem_u32(&s_free), kT);
-    mbar_init(smem_u32(&ds_full[0]), kT);
-    mbar_init(smem_u32(&ds_full[1]), kT);
+    mbar_init(smem_u32(&s_free), kQEw);
+    mbar_init(smem_u32(&ds_full[0]), kQEw);
+    mbar_init(smem_u32(&ds_full[1]), kQEw);
     mbar_init(smem_u32(&dq_full), 1);
     mbar_init(smem_u32(&done), 1);
     for (int s = 0; s < kSlots; ++s) {
@@ -181,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     abort_s = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kQMma) {
     tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
     tmem_relinquish();
   }
@@ -193,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // TMEM columns: S [0,128) dP [128,256) dQ [256,384) dS buffers [384,448) [448,512)
   const uint32_t cS = 0, cdP = 128, cdQ = 256, cdS = 384;
 
-  if (warp == kProducerWarp) {
+  if (warp == kQProducer) {
     if (lane == 0) {
       prefetch_tmap(&tm.q);
       prefetch_tmap(&tm.dout);
@@ -229,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(smem_u32(&kv_full[m % kSlots]), (m / kSlots) & 1, abort_flag, a.err,
                   kErrBwdDrain);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kQMma) {
     if (lane == 0 && n_tiles > 0) {
       const uint64_t dq_ = smem_desc_sw128(sq, 16, 1024), ddo = smem_desc_sw128(sdo, 16, 1024);
       const uint64_t dkv = smem_desc_sw128(skv, 16, 1024);          // K-major view of a slot
@@ -282,20 +374,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // --------------------------------------------------- elementwise warps
-    const int row = threadIdx.x;  // TMEM lane == query row of the tile
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // warpgroup `half` owns columns [64 half, 64 half + 64) of every tile
+    const int half = warp >> 2;
+    const int row = threadIdx.x & 127;  // TMEM lane == query row of the tile
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int u = u0 + row;
     const bool row_live = u < Lb;
     const int tq = row_live ? static_cast<int>(block_token(a.order, a.S, a.P, i, u)) : 0;
-    const long long li = (static_cast<long long>(b) * a.Hq + h) * a.S + tq;
-    const float lse2 = row_live ? a.lse[li] * kLog2e : 0.f;
-    const float Drow = row_live ? a.Dsum[li] : 0.f;
+    const long long bi = blk_index(static_cast<long long>(b) * a.Hq + h, a.P, a.Lbp, i, u);
+    const float lse2 = row_live ? a.lse2_blk[bi] : 0.f;
+    const float Drow = row_live ? a.D_blk[bi] : 0.f;
     int lo = 0, hi = a.S - 1;
     if (a.doc_start && row_live) {
       lo = a.doc_start[static_cast<long long>(b % a.pos_rows) * a.S + tq];
       hi = tq;
     }
     const float sl2 = a.scale * kLog2e;
+    const int col0 = half * 64;
     int t = 0;
     bool ok = true;
     for (int s = 0; s < a.P && ok; ++s) {
@@ -303,65 +398,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       int kt0, kt1;
       block_tiles(a.order, a.S, a.P, j, hull_lo, hull_hi, kT, kt0, kt1);
       for (int kt = kt0; kt <= kt1; ++kt, ++t) {
-        const bool got = mbar_wait(smem_u32(&s_full), t & 1, abort_flag, a.err, kErrBwdSFull);
-        if (!__all_sync(0xffffffffu, got)) {
+        if (!wait_warp(smem_u32(&s_full), t & 1, abort_flag, a.err, kErrBwdSFull)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        uint32_t sx[64], px[64];
+        tmem_ld32_at(tmem + lane_base + cS + col0, sx, 0);
+        tmem_ld32_at(tmem + lane_base + cS + col0 + 32, sx, 32);
+        tmem_ld32_at(tmem + lane_base + cdP + col0, px, 0);
+        tmem_ld32_at(tmem + lane_base + cdP + col0 + 32, px, 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&s_free));  // S and dP read: the next tile's MMAs may start
         int c_lo, c_hi;
         col_bounds(a.order, a.S, a.P, j, kt, lo, hi, c_lo, c_hi);
         if (!row_live) {
           c_lo = 0;
           c_hi = -1;
         }
-        uint32_t dsw[kT / 2];  // dS row, bf16 pairs
+        c_lo -= col0;
+        c_hi -= col0;
+        const bool whole = c_lo <= 0 && c_hi >= 63;
+        uint32_t dsw[32];  // dS, bf16 pairs
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t sx[64], px[64];
-          tmem_ld32_at(tmem + lane_base + cS + half * 64, sx, 0);
-          tmem_ld32_at(tmem + lane_base + cS + half * 64 + 32, sx, 32);
-          tmem_ld32_at(tmem + lane_base + cdP + half * 64, px, 0);
-          tmem_ld32_at(tmem + lane_base + cdP + half * 64 + 32, px, 32);
-          tmem_wait_ld();
-          if (half == 1) {  // S and dP fully read: the next tile's MMAs may start
-            tc_fence_before();
-            mbar_arrive(smem_u32(&s_free));
+        for (int c = 0; c < 64; c += 2) {
+          float x0, x1, p0, p1, d0, d1;
+          ffma2(x0, x1, __uint_as_float(sx[c]), __uint_as_float(sx[c + 1]), sl2, sl2, -lse2,
+                -lse2);
+          p0 = ex2(x0);
+          p1 = ex2(x1);
+          if (!whole) {
+            if (c < c_lo || c > c_hi) p0 = 0.f;
+            if (c + 1 < c_lo || c + 1 > c_hi) p1 = 0.f;
           }
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const int col = half * 64 + c;
-            float p0 = ex2(fmaf(__uint_as_float(sx[c]), sl2, -lse2));
-            float p1 = ex2(fmaf(__uint_as_float(sx[c + 1]), sl2, -lse2));
-            if (col < c_lo || col > c_hi) p0 = 0.f;
-            if (col + 1 < c_lo || col + 1 > c_hi) p1 = 0.f;
-            const float d0 = p0 * (__uint_as_float(px[c]) - Drow);
-            const float d1 = p1 * (__uint_as_float(px[c + 1]) - Drow);
-            dsw[col >> 1] = pack_bf16(d0, d1);
-          }
+          fadd2(d0, d1, __uint_as_float(px[c]), __uint_as_float(px[c + 1]), -Drow, -Drow);
+          fmul2(d0, d1, d0, d1, p0, p1);
+          dsw[c >> 1] = pack_bf16(d0, d1);
         }
-        const uint32_t dsb = tmem + lane_base + cdS + (t & 1) * 64;
-        tmem_st32(dsb, *reinterpret_cast<uint32_t(*)[32]>(&dsw[0]));
-        tmem_st32(dsb + 32, *reinterpret_cast<uint32_t(*)[32]>(&dsw[32]));
+        tmem_st32(tmem + lane_base + cdS + (t & 1) * 64 + half * 32, dsw);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&ds_full[t & 1]));
       }
     }
-    // epilogue: dQ * scale
+    // epilogue: dQ * scale, this warpgroup's 64 columns
     const bool have = n_tiles > 0 && ok;
-    if (have) {
-      const bool got = mbar_wait(smem_u32(&dq_full), 0, abort_flag, a.err, kErrBwdOut);
-      if (!__all_sync(0xffffffffu, got)) ok = false;
-    }
+    if (have && !wait_warp(smem_u32(&dq_full), 0, abort_flag, a.err, kErrBwdOut)) ok = false;
     tc_fence_after();
     __nv_bfloat16* dq = static_cast<__nv_bfloat16*>(a.dq);
-    uint4* orow = reinterpret_cast<uint4*>(dq + ((static_cast<long long>(b) * a.S + tq) * a.Hq + h) * kD);
+    uint4* orow = reinterpret_cast<uint4*>(
+        dq + ((static_cast<long long>(b) * a.S + tq) * a.Hq + h) * kD + col0);
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       uint32_t r[32];
       if (have && ok) {
-        tmem_ld32(tmem + lane_base + cdQ + c * 32, r);
+        tmem_ld32(tmem + lane_base + cdQ + col0 + c * 32, r);
         tmem_wait_ld();
       } else {
 #pragma unroll
@@ -370,7 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pk[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e)
-        pk[e] = pack_bf16(__uint_as_float(r[2 * e]) * a.scale, __uint_as_float(r[2 * e + 1]) * a.scale);
+        pk[e] = pack_bf16(__uint_as_float(r[2 * e]) * a.scale,
+                          __uint_as_float(r[2 * e + 1]) * a.scale);
       if (row_live) {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
@@ -380,37 +473,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kQMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 // --------------------------------------------------------------- dK / dV
+constexpr int kKvThreads = 192;             // warps 0-3 elementwise, 4 TMA, 5 MMA
+constexpr int kKvProducer = 4;
+constexpr int kKvMma = 5;
 constexpr int kQT = 64;                      // query rows per streamed tile
 constexpr int kQTileBytes = kQT * kD * 2;    // 16 KiB
 constexpr int kQHalf = kQTileBytes / 2;
 constexpr int kQSlots = 4;
 constexpr int kKvSmemBytes = 2 * kTileBytes + kQSlots * 2 * kQTileBytes;
 constexpr uint32_t kIdescST = idesc_bf16_f32(kT, kQT, false);  // 128 keys x 64 queries
+static_assert(kQT == kBwdRowPad, "query tiles are the block-order padding unit");
 
 enum : int { kInfoEnd = 0, kInfoTile = 1, kInfoFull = 3 };
 
-// Per-column data of one streamed query tile, written by the producer warp.
+// Per-column data of one streamed query tile: three bulk copies from the
+// block-ordered arrays, plus a header the producer writes.
 struct alignas(16) ColData {
   float lse2[kQT];  // lse * log2(e); +inf for rows past the end of the block
   float D[kQT];
-  int lo[kQT];      // a key token x is allowed for the column's query iff lo <= x <= hi
-  int hi[kQT];
+  int lo[kQT];      // doc_start of the column's query (causal); INT_MAX past the end
   int info;         // kInfoEnd, kInfoTile (masked per pair) or kInfoFull (every pair allowed)
+  int i, u0;        // query block and first local row of the tile
+  int pad;
 };
 
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* err, int code) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err, code));
-}
-
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kKvThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ BwdMaps tm, BwdArgs a, int n_tiles_k) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t q_full[kQSlots], q_empty[kQSlots], kv_full, s_full[2], ds_full[2],
@@ -436,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kQSlots; ++s) {
-      mbar_init(smem_u32(&q_full[s]), 32);
+      mbar_init(smem_u32(&q_full[s]), 1);
       mbar_init(smem_u32(&q_empty[s]), 1);
     }
     mbar_init(smem_u32(&kv_full), 1);
@@ -449,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     abort_s = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kKvMma) {
     tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
     tmem_relinquish();
   }
@@ -463,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // first 32 columns of their S^T / dP^T buffer.
   const uint32_t cdP = 128, cdV = 256, cdK = 384;
 
-  if (warp == kProducerWarp) {
+  if (warp == kKvProducer) {
     // ------------------------------------------------------------ producer
     const int G = a.Hq / a.Hkv;
     if (lane == 0) {
@@ -476,79 +570,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       row_tma(sk, &tm.k, kf, hk, a.order, j, w0, b);
       row_tma(sv, &tm.v, kf, hk, a.order, j, w0, b);
     }
+    const long long lo_row = static_cast<long long>(b % a.pos_rows);
+    const uint32_t col_bytes = (ds_row ? 3 : 2) * kQT * 4;
     int n = 0;
     bool ok = true;
     for (int g = 0; g < G && ok; ++g) {
       const int h = hk * G + g;
+      const long long bhq = static_cast<long long>(b) * a.Hq + h;
       for (int s = 0; s < a.P && ok; ++s) {
         const int i = (j + s) % a.P;
         int qt0, qt1;
         block_tiles(a.order, a.S, a.P, i, ds_row ? k_first : 0, a.S - 1, kQT, qt0, qt1);
-        for (int qt = qt0; qt <= qt1 && ok; ++qt) {
-          const int u0 = qt * kQT;
-          const int tq_first = static_cast<int>(block_token(a.order, a.S, a.P, i, u0));
-          const int tq_last =
-              static_cast<int>(block_token(a.order, a.S, a.P, i, min(u0 + kQT, Lb) - 1));
-          int info = kInfoFull;
-          if (ds_row) {
+        // flags of 32 tiles at a time, one per lane
+        for (int base = qt0; base <= qt1 && ok; base += 32) {
+          const int qt = base + lane;
+          bool stop = false, full = true;
+          if (ds_row && qt <= qt1) {
+            const int u0 = qt * kQT;
+            const int tq_first = static_cast<int>(block_token(a.order, a.S, a.P, i, u0));
+            const int tq_last =
+                static_cast<int>(block_token(a.order, a.S, a.P, i, min(u0 + kQT, Lb) - 1));
             // document starts do not decrease along the tokens of a block, so
             // once a tile starts past the keys' documents the rest do too
-            if (ds_row[tq_first] > k_last) break;
-            if (!(k_last <= tq_first && ds_row[tq_last] <= k_first)) info = kInfoTile;
+            stop = ds_row[tq_first] > k_last;
+            full = k_last <= tq_first && ds_row[tq_last] <= k_first;
           }
-          float l2[2], dd[2];
-          int lo[2], hi[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int u = u0 + lane + 32 * e;
-            if (u < Lb) {
-              const int tq = static_cast<int>(block_token(a.order, a.S, a.P, i, u));
-              const long long li = (static_cast<long long>(b) * a.Hq + h) * a.S + tq;
-              l2[e] = a.lse[li] * kLog2e;
-              dd[e] = a.Dsum[li];
-              lo[e] = ds_row ? ds_row[tq] : 0;
-              hi[e] = ds_row ? tq : a.S - 1;
-            } else {
-              l2[e] = INFINITY;
-              dd[e] = 0.f;
-              lo[e] = 1;
-              hi[e] = 0;
+          const unsigned stops = __ballot_sync(0xffffffffu, stop);
+          const unsigned fulls = __ballot_sync(0xffffffffu, full);
+          int cnt = min(32, qt1 - base + 1);
+          if (stops) cnt = min(cnt, __ffs(static_cast<int>(stops)) - 1);
+          for (int e = 0; e < cnt; ++e) {
+            const int slot = n % kQSlots;
+            if (!wait_warp(smem_u32(&q_empty[slot]), ((n / kQSlots) & 1) ^ 1, abort_flag, a.err,
+                           kErrBwdKvEmpty)) {
+              ok = false;
+              break;
             }
+            if (lane == 0) {
+              const int u0 = (base + e) * kQT;
+              ColData& cd = cols[slot];
+              cd.info = (fulls >> e) & 1u ? kInfoFull : kInfoTile;
+              cd.i = i;
+              cd.u0 = u0;
+              const uint32_t bar = smem_u32(&q_full[slot]);
+              const uint32_t dst = sslot + slot * 2 * kQTileBytes;
+              mbar_arrive_expect_tx(bar, 2 * kQTileBytes + col_bytes);
+              row_tma(dst, &tm.q, bar, h, a.order, i, u0, b, kQHalf);
+              row_tma(dst + kQTileBytes, &tm.dout, bar, h, a.order, i, u0, b, kQHalf);
+              const long long off = blk_index(bhq, a.P, a.Lbp, i, u0);
+              bulk_load(smem_u32(cd.lse2), a.lse2_blk + off, kQT * 4, bar);
+              bulk_load(smem_u32(cd.D), a.D_blk + off, kQT * 4, bar);
+              if (ds_row)
+                bulk_load(smem_u32(cd.lo), a.lo_blk + blk_index(lo_row, a.P, a.Lbp, i, u0),
+                          kQT * 4, bar);
+            }
+            ++n;
           }
-          const int slot = n % kQSlots;
-          if (!wait_warp(smem_u32(&q_empty[slot]), ((n / kQSlots) & 1) ^ 1, abort_flag, a.err,
-                         kErrBwdKvEmpty)) {
-            ok = false;
-            break;
-          }
-          ColData& cd = cols[slot];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = lane + 32 * e;
-            cd.lse2[c] = l2[e];
-            cd.D[c] = dd[e];
-            cd.lo[c] = lo[e];
-            cd.hi[c] = hi[e];
-          }
-          const uint32_t full = smem_u32(&q_full[slot]);
-          if (lane == 0) {
-            cd.info = info;
-            const uint32_t dst = sslot + slot * 2 * kQTileBytes;
-            mbar_arrive_expect_tx(full, 2 * kQTileBytes);
-            row_tma(dst, &tm.q, full, h, a.order, i, u0, b, kQHalf);
-            row_tma(dst + kQTileBytes, &tm.dout, full, h, a.order, i, u0, b, kQHalf);
-          } else {
-            mbar_arrive(full);
-          }
-          ++n;
+          if (stops) break;
         }
       }
     }
     if (ok) {  // end of the list
       const int slot = n % kQSlots;
       if (wait_warp(smem_u32(&q_empty[slot]), ((n / kQSlots) & 1) ^ 1, abort_flag, a.err,
-                    kErrBwdKvEmpty)) {
-        if (lane == 0) cols[slot].info = kInfoEnd;
+                    kErrBwdKvEmpty) &&
+          lane == 0) {
+        cols[slot].info = kInfoEnd;
         mbar_arrive(smem_u32(&q_full[slot]));
       }
     }
@@ -560,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   kErrBwdDrain);
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kKvMma) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       const uint64_t dk0 = smem_desc_sw128(sk, 16, 1024), dv0 = smem_desc_sw128(sv, 16, 1024);
@@ -661,25 +748,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32_at(tmem + lane_base + buf + 32, sx, 32);
       tmem_ld32_at(tmem + lane_base + cdP + buf, px, 0);
       tmem_ld32_at(tmem + lane_base + cdP + buf + 32, px, 32);
+      const bool full = info == kInfoFull;
+      // causal part of the mask: column c holds a query token >= ktok iff c >= c_min
+      int c_min = 0;
+      if (!full) {
+        c_min = a.order == SP_ORDER_STRIPED ? -floor_div_i(-(ktok - cd.i), a.P) - cd.u0
+                                            : ktok - (cd.i * Lb + cd.u0);
+      }
       tmem_wait_ld();
       uint32_t pk[32], dk[32];
-      const bool full = info == kInfoFull;
 #pragma unroll
-      for (int c = 0; c < kQT; c += 2) {
-        const float2 l2 = *reinterpret_cast<const float2*>(&cd.lse2[c]);
-        const float2 D = *reinterpret_cast<const float2*>(&cd.D[c]);
-        float p0 = ex2(fmaf(__uint_as_float(sx[c]), sl2, -l2.x));
-        float p1 = ex2(fmaf(__uint_as_float(sx[c + 1]), sl2, -l2.y));
+      for (int c = 0; c < kQT; c += 4) {
+        const float4 l2 = *reinterpret_cast<const float4*>(&cd.lse2[c]);
+        const float4 D = *reinterpret_cast<const float4*>(&cd.D[c]);
+        float x0, x1, x2, x3;
+        ffma2(x0, x1, __uint_as_float(sx[c]), __uint_as_float(sx[c + 1]), sl2, sl2, -l2.x, -l2.y);
+        ffma2(x2, x3, __uint_as_float(sx[c + 2]), __uint_as_float(sx[c + 3]), sl2, sl2, -l2.z,
+              -l2.w);
+        float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
         if (!full) {
-          const int2 lo = *reinterpret_cast<const int2*>(&cd.lo[c]);
-          const int2 hi = *reinterpret_cast<const int2*>(&cd.hi[c]);
-          if (ktok < lo.x || ktok > hi.x) p0 = 0.f;
-          if (ktok < lo.y || ktok > hi.y) p1 = 0.f;
+          const int4 lo = *reinterpret_cast<const int4*>(&cd.lo[c]);
+          if (c < c_min || lo.x > ktok) p0 = 0.f;
+          if (c + 1 < c_min || lo.y > ktok) p1 = 0.f;
+          if (c + 2 < c_min || lo.z > ktok) p2 = 0.f;
+          if (c + 3 < c_min || lo.w > ktok) p3 = 0.f;
         }
-        const float d0 = p0 * (__uint_as_float(px[c]) - D.x);
-        const float d1 = p1 * (__uint_as_float(px[c + 1]) - D.y);
+        float d0, d1, d2, d3;
+        fadd2(d0, d1, __uint_as_float(px[c]), __uint_as_float(px[c + 1]), -D.x, -D.y);
+        fadd2(d2, d3, __uint_as_float(px[c + 2]), __uint_as_float(px[c + 3]), -D.z, -D.w);
+        fmul2(d0, d1, d0, d1, p0, p1);
+        fmul2(d2, d3, d2, d3, p2, p3);
         pk[c >> 1] = pack_bf16(p0, p1);
+        pk[(c >> 1) + 1] = pack_bf16(p2, p3);
         dk[c >> 1] = pack_bf16(d0, d1);
+        dk[(c >> 1) + 1] = pack_bf16(d2, d3);
       }
       tmem_st32(tmem + lane_base + buf, pk);
       tmem_st32(tmem + lane_base + cdP + buf, dk);
@@ -691,7 +793,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool have = t > 0 && ok;
     if (have && !wait_warp(smem_u32(&dkv_full), 0, abort_flag, a.err, kErrBwdOut)) ok = false;
     tc_fence_after();
-    const long long orow = ((static_cast<long long>(b) * a.S + (key_live ? ktok : 0)) * a.Hkv + hk) * kD;
+    const long long orow =
+        ((static_cast<long long>(b) * a.S + (key_live ? ktok : 0)) * a.Hkv + hk) * kD;
     uint4* dk_row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk) + orow);
     uint4* dv_row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dv) + orow);
 #pragma unroll 1
@@ -722,73 +825,57 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kKvMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-// D[b][h][t] = sum_c dout[b][t][h][c] * out[b][t][h][c] for d = 128 bf16 rows:
-// 16 lanes per row, one 16-byte load of each tensor per lane.
-__global__ void __launch_bounds__(256) bwd_rowsum_bf16_kernel(const uint4* __restrict__ out,
-                                                              const uint4* __restrict__ dout,
-                                                              int B, int S, int H,
-                                                              float* __restrict__ D) {
-  const long long g = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long row = g >> 4;
-  const bool live = row < static_cast<long long>(B) * S * H;
-  float acc = 0.f;
-  if (live) {
-    const uint4 x = __ldcs(out + g), y = __ldcs(dout + g);
-    const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 xf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[e]));
-      const float2 yf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[e]));
-      acc = fmaf(xf.x, yf.x, acc);
-      acc = fmaf(xf.y, yf.y, acc);
-    }
-  }
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (live && (threadIdx.x & 15) == 0) {
-    const int h = static_cast<int>(row % H);
-    const long long bt = row / H;
-    D[(bt / S * H + h) * S + bt % S] = acc;
-  }
-}
-
 }  // namespace
 
-// D, then dQ and dK/dV (independent of each other) on the tensor cores.
+// prep, then dQ and dK/dV (independent of each other) on the tensor cores.
 int launch_attn_bwd_bf16(const BwdArgs& a, cudaStream_t st) {
-  BwdMaps tm;
+  BwdMaps tm, tk;
   if (!tmap::make_map(&tm.q, a.q, a.B, a.S, a.Hq, a.P, a.order) ||
       !tmap::make_map(&tm.dout, a.dout, a.B, a.S, a.Hq, a.P, a.order) ||
       !tmap::make_map(&tm.k, a.k, a.B, a.S, a.Hkv, a.P, a.order) ||
-      !tmap::make_map(&tm.v, a.v, a.B, a.S, a.Hkv, a.P, a.order))
+      !tmap::make_map(&tm.v, a.v, a.B, a.S, a.Hkv, a.P, a.order) ||
+      !tmap::make_map(&tk.q, a.q, a.B, a.S, a.Hq, a.P, a.order, kQT) ||
+      !tmap::make_map(&tk.dout, a.dout, a.B, a.S, a.Hq, a.P, a.order, kQT))
     return -1;
-  const long long rows = static_cast<long long>(a.B) * a.S * a.Hq;
-  bwd_rowsum_bf16_kernel<<<static_cast<unsigned>((rows * 16 + 255) / 256), 256, 0, st>>>(
-      static_cast<const uint4*>(a.out), static_cast<const uint4*>(a.dout), a.B, a.S, a.Hq,
-      a.Dsum);
-  const int Lb = a.S / a.P, n_tiles = (Lb + kT - 1) / kT;
-  const int dq_smem = kSmemBytes + 1024, kv_smem = kKvSmemBytes + 1024;
+  tk.k = tm.k;
+  tk.v = tm.v;
+  const int Lb = a.S / a.P;
+  PrepArgs pa;
+  pa.out = static_cast<const uint4*>(a.out);
+  pa.dout = static_cast<const uint4*>(a.dout);
+  pa.lse = a.lse;
+  pa.doc_start = a.doc_start;
+  pa.D_blk = a.D_blk;
+  pa.lse2_blk = a.lse2_blk;
+  pa.lo_blk = a.lo_blk;
+  pa.rows = static_cast<long long>(a.B) * a.S * a.Hq;
+  pa.nA = (pa.rows * 16 + 31) / 32 * 32;
+  pa.nB = static_cast<long long>(a.B) * a.Hq * a.P * (a.Lbp - Lb);
+  pa.nC = a.doc_start ? static_cast<long long>(a.pos_rows) * a.P * a.Lbp : 0;
+  pa.S = a.S;
+  pa.H = a.Hq;
+  pa.P = a.P;
+  pa.Lbp = a.Lbp;
+  pa.order = a.order;
+  const long long n_prep = pa.nA + pa.nB + pa.nC;
+  bwd_prep_kernel<<<static_cast<unsigned>((n_prep + 255) / 256), 256, 0, st>>>(pa);
+  const int n_tiles = (Lb + kT - 1) / kT;
+  const int dq_smem = kQSmemBytes + 1024, kv_smem = kKvSmemBytes + 1024;
   if (cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem) !=
           cudaSuccess ||
       cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kv_smem) != cudaSuccess)
     return -1;
   const unsigned n_q = static_cast<unsigned>(a.P) * n_tiles * a.B * a.Hq;
-  bwd_dq_kernel<<<n_q, kThreads, dq_smem, st>>>(tm, a, n_tiles);
-  BwdMaps tk;  // the dK/dV kernel streams 64-row query tiles
-  tk.k = tm.k;
-  tk.v = tm.v;
-  if (!tmap::make_map(&tk.q, a.q, a.B, a.S, a.Hq, a.P, a.order, kQT) ||
-      !tmap::make_map(&tk.dout, a.dout, a.B, a.S, a.Hq, a.P, a.order, kQT))
-    return -1;
+  bwd_dq_kernel<<<n_q, kQThreads, dq_smem, st>>>(tm, a, n_tiles);
   const unsigned n_kv = static_cast<unsigned>(a.P) * n_tiles * a.B * a.Hkv;
-  bwd_dkdv_kernel<<<n_kv, kThreads, kv_smem, st>>>(tk, a, n_tiles);
+  bwd_dkdv_kernel<<<n_kv, kKvThreads, kv_smem, st>>>(tk, a, n_tiles);
   return cudaGetLastError() == cudaSuccess ? 3 : -1;
 }
 

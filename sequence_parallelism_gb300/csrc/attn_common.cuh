@@ -42,7 +42,12 @@ struct BwdArgs {
   const void* dout;            // [B][S][Hq][d]  upstream gradient
   const float* lse;            // [B][Hq][S]     forward log-sum-exp (natural)
   const int32_t* doc_start;    // [pos_rows][S] or nullptr (non-causal)
-  float* Dsum;                 // [B][Hq][S] scratch: rowsum(dout * out)
+  float* Dsum;                 // [B][Hq][S] scratch: rowsum(dout * out) (f32 path)
+  // bf16 path: per-query data in block order, each block padded to Lbp rows
+  float* lse2_blk;             // [B][Hq][P][Lbp] lse * log2(e), +inf in the padding
+  float* D_blk;                // [B][Hq][P][Lbp] rowsum(dout * out), 0 in the padding
+  int32_t* lo_blk;             // [B][P][Lbp] doc_start of the row's token (causal), INT_MAX pad
+  int Lbp;
   void* dq;                    // [B][S][Hq][d]
   void* dk;                    // [B][S][Hkv][d]
   void* dv;                    // [B][S][Hkv][d]
@@ -54,6 +59,7 @@ struct BwdArgs {
 
 int launch_attn_bwd_simt(const BwdArgs& a, cudaStream_t stream);
 int launch_attn_bwd_bf16(const BwdArgs& a, cudaStream_t stream);  // d == 128
+constexpr int kBwdRowPad = 64;  // Lbp = S / P rounded up to a multiple of this
 
 // Validates and runs one blockwise-attention call (doc_start scan when
 // position_ids != NULL, then the f32 or bf16 kernel).  position_ids has
