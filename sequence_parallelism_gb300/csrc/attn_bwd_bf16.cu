@@ -45,7 +45,8 @@ using namespace ptx;
 
 constexpr int kD = 128;
 constexpr int kT = 128;                      // rows per resident tile
-constexpr int kSlots = 4;                    // streamed K/V tile ring depth (dQ)
+constexpr int kKSlots = 3;                   // dQ: streamed K tiles (held until dQ += dS K)
+constexpr int kVSlots = 2;                   // dQ: streamed V tiles (held until dP = dO V^T)
 constexpr int kTileBytes = kT * kD * 2;      // 32 KiB
 constexpr int kHalfBytes = kTileBytes / 2;   // one 64-column half
 constexpr uint32_t kTmemCols = 512;
@@ -216,19 +217,20 @@ constexpr int kQThreads = 320;  // warps 0-7 elementwise (two warpgroups), 8 TMA
 constexpr int kQProducer = 8;
 constexpr int kQMma = 9;
 constexpr int kQEw = 256;       // elementwise threads
-constexpr int kQSmemBytes = (2 + kSlots) * kTileBytes;
+constexpr int kQSmemBytes = (2 + kKSlots + kVSlots) * kTileBytes;
 
 __global__ void __launch_bounds__(kQThreads, 1)
     bwd_dq_kernel(const __grid_constant__ BwdMaps tm, BwdArgs a, int n_tiles_q) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t q_full, s_full, s_free, dq_full, done;
   __shared__ uint64_t ds_full[2];  // per dS buffer
-  __shared__ uint64_t kv_full[kSlots], kv_empty[kSlots];
+  __shared__ uint64_t k_full[kKSlots], k_empty[kKSlots], v_full[kVSlots], v_empty[kVSlots];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sq = smem_u32(smem), sdo = sq + kTileBytes, skv = sq + 2 * kTileBytes;
+  const uint32_t sq = smem_u32(smem), sdo = sq + kTileBytes, sks = sq + 2 * kTileBytes;
+  const uint32_t svs = sks + kKSlots * kTileBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // work item: heavy query positions first, heads innermost
@@ -266,9 +268,13 @@ __global__ void __launch_bounds__(kQThreads, 1)
     mbar_init(smem_u32(&ds_full[1]), kQEw);
     mbar_init(smem_u32(&dq_full), 1);
     mbar_init(smem_u32(&done), 1);
-    for (int s = 0; s < kSlots; ++s) {
-      mbar_init(smem_u32(&kv_full[s]), 1);
-      mbar_init(smem_u32(&kv_empty[s]), 1);
+    for (int s = 0; s < kKSlots; ++s) {
+      mbar_init(smem_u32(&k_full[s]), 1);
+      mbar_init(smem_u32(&k_empty[s]), 1);
+    }
+    for (int s = 0; s < kVSlots; ++s) {
+      mbar_init(smem_u32(&v_full[s]), 1);
+      mbar_init(smem_u32(&v_empty[s]), 1);
     }
     abort_s = 0;
     fence_mbar_init();
@@ -295,77 +301,84 @@ __global__ void __launch_bounds__(kQThreads, 1)
       mbar_arrive_expect_tx(qf, 2 * kTileBytes);
       row_tma(sq, &tm.q, qf, h, a.order, i, u0, b);
       row_tma(sdo, &tm.dout, qf, h, a.order, i, u0, b);
-      int n = 0;
+      int n = 0;  // tiles loaded
       bool ok = true;
       for (int s = 0; s < a.P && ok; ++s) {
         const int j = ((i - s) % a.P + a.P) % a.P;
         int kt0, kt1;
         block_tiles(a.order, a.S, a.P, j, hull_lo, hull_hi, kT, kt0, kt1);
-        for (int kt = kt0; kt <= kt1 && ok; ++kt) {
-          for (int kv = 0; kv < 2; ++kv, ++n) {
-            const int slot = n % kSlots;
-            if (!mbar_wait(smem_u32(&kv_empty[slot]), ((n / kSlots) & 1) ^ 1, abort_flag, a.err,
-                           kErrBwdKvEmpty)) {
-              ok = false;
-              break;
-            }
-            const uint32_t full = smem_u32(&kv_full[slot]);
-            mbar_arrive_expect_tx(full, kTileBytes);
-            row_tma(skv + slot * kTileBytes, kv == 0 ? &tm.k : &tm.v, full, kvh, a.order, j,
-                    kt * kT, b);
+        for (int kt = kt0; kt <= kt1; ++kt, ++n) {
+          const int ks = n % kKSlots, vs = n % kVSlots;
+          if (!mbar_wait(smem_u32(&k_empty[ks]), ((n / kKSlots) & 1) ^ 1, abort_flag, a.err,
+                         kErrBwdKvEmpty)) {
+            ok = false;
+            break;
           }
+          mbar_arrive_expect_tx(smem_u32(&k_full[ks]), kTileBytes);
+          row_tma(sks + ks * kTileBytes, &tm.k, smem_u32(&k_full[ks]), kvh, a.order, j, kt * kT, b);
+          if (!mbar_wait(smem_u32(&v_empty[vs]), ((n / kVSlots) & 1) ^ 1, abort_flag, a.err,
+                         kErrBwdKvEmpty)) {
+            ok = false;
+            ++n;  // K of this tile is in flight
+            break;
+          }
+          mbar_arrive_expect_tx(smem_u32(&v_full[vs]), kTileBytes);
+          row_tma(svs + vs * kTileBytes, &tm.v, smem_u32(&v_full[vs]), kvh, a.order, j, kt * kT, b);
         }
       }
+      // copies still in flight land before the CTA can exit
       mbar_wait(qf, 0, abort_flag, a.err, kErrBwdDrain);
-      for (int m = n - 1; m >= 0 && m >= n - kSlots; --m)
-        mbar_wait(smem_u32(&kv_full[m % kSlots]), (m / kSlots) & 1, abort_flag, a.err,
+      for (int m = n - 1; m >= 0 && m >= n - kKSlots; --m)
+        mbar_wait(smem_u32(&k_full[m % kKSlots]), (m / kKSlots) & 1, abort_flag, a.err,
+                  kErrBwdDrain);
+      for (int m = n - 1; m >= 0 && m >= n - kVSlots; --m)
+        mbar_wait(smem_u32(&v_full[m % kVSlots]), (m / kVSlots) & 1, abort_flag, a.err,
                   kErrBwdDrain);
     }
   } else if (warp == kQMma) {
     if (lane == 0 && n_tiles > 0) {
       const uint64_t dq_ = smem_desc_sw128(sq, 16, 1024), ddo = smem_desc_sw128(sdo, 16, 1024);
-      const uint64_t dkv = smem_desc_sw128(skv, 16, 1024);          // K-major view of a slot
-      const uint64_t dkmn = smem_desc_sw128(skv, kHalfBytes, 1024);  // MN-major view (K as B of dS K)
-      // S = Q K^T and dP = dO V^T for tile t (K_t at load 2t, V_t at 2t + 1)
-      auto issue_sdp = [&](int t) {
-        const uint64_t kb = dkv + ((((2 * t) % kSlots) * kTileBytes) >> 4);
-        const uint64_t vb = dkv + ((((2 * t + 1) % kSlots) * kTileBytes) >> 4);
+      const uint64_t dk0 = smem_desc_sw128(sks, 16, 1024);          // K-major K slots
+      const uint64_t dkmn = smem_desc_sw128(sks, kHalfBytes, 1024);  // MN-major view (B of dS K)
+      const uint64_t dv0 = smem_desc_sw128(svs, 16, 1024);          // K-major V slots
+      // S = Q K^T, then dP = dO V^T for tile t, each as soon as its operand landed
+      auto issue_sdp = [&](int t) -> bool {
+        const int ks = t % kKSlots, vs = t % kVSlots;
+        if (!mbar_wait(smem_u32(&k_full[ks]), (t / kKSlots) & 1, abort_flag, a.err, kErrBwdKvFull))
+          return false;
+        tc_fence_after();
+        const uint64_t kb = dk0 + ((ks * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
           mma_ss(tmem + cS, kmaj_desc(dq_, kk), kmaj_desc(kb, kk), kIdescKmaj, kk > 0 ? 1u : 0u);
+        if (!mbar_wait(smem_u32(&v_full[vs]), (t / kVSlots) & 1, abort_flag, a.err, kErrBwdKvFull))
+          return false;
+        tc_fence_after();
+        const uint64_t vb = dv0 + ((vs * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
           mma_ss(tmem + cdP, kmaj_desc(ddo, kk), kmaj_desc(vb, kk), kIdescKmaj, kk > 0 ? 1u : 0u);
         mma_commit(smem_u32(&s_full));
-      };
-      auto wait_kv = [&](int t) -> bool {
-        for (int m = 2 * t; m <= 2 * t + 1; ++m)
-          if (!mbar_wait(smem_u32(&kv_full[m % kSlots]), (m / kSlots) & 1, abort_flag, a.err,
-                         kErrBwdKvFull))
-            return false;
-        tc_fence_after();
+        mma_commit(smem_u32(&v_empty[vs]));  // V_t consumed once dP is done
         return true;
       };
-      bool ok = mbar_wait(smem_u32(&q_full), 0, abort_flag, a.err, kErrBwdQFull) && wait_kv(0);
-      if (ok) issue_sdp(0);
+      bool ok = mbar_wait(smem_u32(&q_full), 0, abort_flag, a.err, kErrBwdQFull);
+      tc_fence_after();
+      if (ok) ok = issue_sdp(0);
       for (int t = 0; t < n_tiles && ok; ++t) {
         if (!mbar_wait(smem_u32(&s_free), t & 1, abort_flag, a.err, kErrBwdSFree)) break;
-        if (t + 1 < n_tiles) {
-          if (!wait_kv(t + 1)) break;
-          issue_sdp(t + 1);
-        }
+        if (t + 1 < n_tiles && !issue_sdp(t + 1)) break;
         if (!mbar_wait(smem_u32(&ds_full[t & 1]), (t >> 1) & 1, abort_flag, a.err, kErrBwdDsFull))
           break;
         tc_fence_after();
         // dQ += dS K: dS (bf16 pairs) from TMEM, K_t as the MN-major B operand
-        const uint64_t kmn = dkmn + ((((2 * t) % kSlots) * kTileBytes) >> 4);
+        const uint64_t kmn = dkmn + (((t % kKSlots) * kTileBytes) >> 4);
         const uint32_t ds = tmem + cdS + (t & 1) * 64;
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
           mma_ts(tmem + cdQ, ds + kk * 8, kmn + ((kk * 16 * 128) >> 4), kIdescBmn,
                  (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&kv_empty[(2 * t) % kSlots]));
-        mma_commit(smem_u32(&kv_empty[(2 * t + 1) % kSlots]));
+        mma_commit(smem_u32(&k_empty[t % kKSlots]));  // K_t consumed
       }
       mma_commit(smem_u32(&dq_full));
       mma_commit(smem_u32(&done));
