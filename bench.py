@@ -40,8 +40,9 @@ sys.path.insert(0, ROOT)
 METRIC = ("causal blockwise-attention TFLOP/s (% BF16 peak); seq↔head permute GB/s")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
-# kernel from the committed ncu capture (None until taken for this kernel).
-NCU_TRAFFIC_BYTES = {}
+# kernel from the committed ncu capture (profiles/attn_bf16_kernel.md; None
+# for workloads not captured at their own size).
+NCU_TRAFFIC_BYTES = {"ulysses_4k": 239632640}
 
 
 def load_peaks():
@@ -369,6 +370,7 @@ def extra_measurements(args, peaks):
                 tf / peaks["bf16_tflops"], 4), "flops": fl, "reps": reps,
             "note": "doc_start scan + attention kernel, median of reps"}
         del q, k, v, out
+    res["llama8b_32k_causal_backward"] = backward_measurement(peaks, flush, stream)
     x = torch.randn((1, 32768, 32, 128), device="cuda").to(torch.bfloat16)
     y = torch.empty((8, 1, 32768, 4, 128), dtype=torch.bfloat16, device="cuda")
     for _ in range(3):
@@ -387,6 +389,51 @@ def extra_measurements(args, peaks):
     res["permute_256MiB"] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
                              "shape": "[1][32768][32][128] bf16, P=8"}
     return res
+
+
+def backward_measurement(peaks, flush, stream, reps=20):
+    """Attention backward (dq, dk, dv) on llama8b_32k: prep + dQ + dK/dV
+    kernels, L2 flushed between reps.  Algorithmic FLOPs = 2.5 x the
+    forward's (five d-long products per allowed pair: S, dP, dV, dQ, dK)."""
+    import torch
+
+    import sequence_parallelism_gb300 as sp
+    from sequence_parallelism_gb300 import _lib, workloads
+
+    cfg = workloads.CONFIGS["llama8b_32k"]
+    B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
+    q, k, v = workloads.qkv_torch(B, S, Hq, Hkv, d, cfg["seed"], torch.bfloat16, "cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(cfg["seed"] + 7)
+    dout = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
+    pos_np = workloads.position_ids(cfg)
+    pos = torch.from_numpy(pos_np).cuda()
+    out, lse = sp.blockwise_attention(q, k, v, P, "contiguous", pos)
+    ws = torch.empty(_lib.sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, P, True),
+                     dtype=torch.uint8, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    call = lambda: _lib.sp_blockwise_attn_bwd(q, k, v, out, dout, lse, pos, P, "contiguous", 0.0,
+                                              dq, dk, dv, ws)
+    for _ in range(3):
+        call()
+    launches = _lib.sp_last_launch_count()
+    ms = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        ms.append((a, b))
+    torch.cuda.synchronize()
+    t = statistics.median([a.elapsed_time(b) for a, b in ms])
+    fl = 2.5 * attention_flops(cfg, pos_np)
+    tf = fl / (t * 1e-3) / 1e12
+    return {"ms": round(t, 4), "TFLOP/s": round(tf, 1),
+            "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4), "flops": fl,
+            "reps": reps, "launches_per_call": launches,
+            "note": "doc_start scan + prep + dQ + dK/dV kernels, median of reps; "
+                    "flops = 2.5 x forward (S, dP, dV, dQ, dK)"}
 
 
 # ------------------------------------------------------- CPU oracle leg
