@@ -95,7 +95,8 @@ def test_backward_full_size(sp, name, order):
                                               vn[:, :, kv:kv + 1], don[:, :, h:h + 1], rows, pos)
 
     ref_dq = np.concatenate(_pool(dq_head, list(range(Hq))), axis=2)
-    check_grad(got_dq, ref_dq, "bf16", f"dq {name} {order}")
+    e = check_grad(got_dq, ref_dq, "bf16", f"dq {name} {order}")
+    print(f"PARITY-GRAD {name} {order} dq max=%.3e mean=%.3e" % e)
 
     keys = _sampled_keys(pos, S, P, order)
     kvh = 0
@@ -108,5 +109,7 @@ def test_backward_full_size(sp, name, order):
     parts = _pool(dkv_head, list(range(kvh * G, (kvh + 1) * G)))
     ref_dk = sum(p[0] for p in parts)[:, :, 0]
     ref_dv = sum(p[1] for p in parts)[:, :, 0]
-    check_grad(np32(dk[:, keys, kvh]), ref_dk, "bf16", f"dk {name} {order}")
-    check_grad(np32(dv[:, keys, kvh]), ref_dv, "bf16", f"dv {name} {order}")
+    e = check_grad(np32(dk[:, keys, kvh]), ref_dk, "bf16", f"dk {name} {order}")
+    print(f"PARITY-GRAD {name} {order} dk max=%.3e mean=%.3e" % e)
+    e = check_grad(np32(dv[:, keys, kvh]), ref_dv, "bf16", f"dv {name} {order}")
+    print(f"PARITY-GRAD {name} {order} dv max=%.3e mean=%.3e" % e)

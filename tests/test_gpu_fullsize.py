@@ -60,8 +60,9 @@ def test_ulysses_4k_pipeline(sp):
     rows = workloads.sample_rows(S, P, 512, cfg["seed"])
     ref_out, ref_lse = oracle_rows(np32(q), np32(k), np32(v), rows, None)
     lse = ylse.view(P, B, G, S).permute(1, 0, 2, 3).reshape(B, H, S)
-    check_attention(np32(out)[:, rows], lse.cpu().numpy()[:, :, rows], ref_out, ref_lse, "bf16",
-                    "ulysses_4k")
+    stats = check_attention(np32(out)[:, rows], lse.cpu().numpy()[:, :, rows], ref_out, ref_lse,
+                            "bf16", "ulysses_4k")
+    print("PARITY ulysses_4k contiguous max=%.3e mean=%.3e lse=%.3e" % stats)
 
 
 @pytest.mark.parametrize("name,order", [("llama8b_32k", "contiguous"),
@@ -80,7 +81,8 @@ def test_causal_full_size(sp, name, order):
     got_lse = lse[:, :, rows].cpu().numpy()
     del out, lse
     ref_out, ref_lse = oracle_rows(np32(q), np32(k), np32(v), rows, pos)
-    check_attention(got_out, got_lse, ref_out, ref_lse, "bf16", f"{name} {order}")
+    stats = check_attention(got_out, got_lse, ref_out, ref_lse, "bf16", f"{name} {order}")
+    print(f"PARITY {name} {order} " + "max=%.3e mean=%.3e lse=%.3e" % stats)
 
 
 def test_halfmil_ulysses_ring_hybrid(sp):
@@ -96,4 +98,5 @@ def test_halfmil_ulysses_ring_hybrid(sp):
     got_lse = lse.permute(1, 0, 2, 3).reshape(1, cfg["Hq"], cfg["S"])[:, :, rows].cpu().numpy()
     del out, lse
     ref_out, ref_lse = oracle_rows(np32(q), np32(k), np32(v), rows, pos)
-    check_attention(got_out, got_lse, ref_out, ref_lse, "bf16", "halfmil hybrid 8x2")
+    stats = check_attention(got_out, got_lse, ref_out, ref_lse, "bf16", "halfmil hybrid 8x2")
+    print("PARITY halfmil_512k hybrid-8x2 max=%.3e mean=%.3e lse=%.3e" % stats)
