@@ -68,7 +68,8 @@ sp_status attn(const void* q, const void* k, const void* v, const int32_t* posit
   int* err = reinterpret_cast<int*>(ws);
   int32_t* doc_start = nullptr;
   int launches = 0;
-  if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return SP_ERR_CUDA;
+  // error word and work-unit counter
+  if (cudaMemsetAsync(err, 0, 2 * sizeof(int), st) != cudaSuccess) return SP_ERR_CUDA;
   if (causal) {
     doc_start = reinterpret_cast<int32_t*>(ws + kWsHeaderBytes);
     void* scan = ws + kWsHeaderBytes + doc_start_bytes(pos_rows, S);
@@ -84,6 +85,7 @@ sp_status attn(const void* q, const void* k, const void* v, const int32_t* posit
   a.out = out;
   a.lse = lse;
   a.err = err;
+  a.counter = err + 1;
   a.B = B;
   a.pos_rows = pos_rows;
   a.S = S;

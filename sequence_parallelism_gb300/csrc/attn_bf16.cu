@@ -64,7 +64,8 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, true);
 // error codes recorded in the workspace error word (which wait gave up)
 enum : int {
   kErrQFull = 0x101, kErrKvEmpty = 0x102, kErrKvFull = 0x103, kErrSFull = 0x104,
-  kErrPFull = 0x105, kErrOFull = 0x106, kErrDrain = 0x107
+  kErrPFull = 0x105, kErrOFull = 0x106, kErrDrain = 0x107, kErrUnit = 0x108,
+  kErrQEmpty = 0x109, kErrOFree = 0x10a
 };
 
 struct Tmaps {
@@ -136,21 +137,79 @@ __device__ __forceinline__ void item_coords(int L, const AttnArgs& a, int n_pair
 }
 
 struct __align__(8) Barriers {
-  uint64_t q_full;
+  uint64_t unit_full[2];   // producer -> all: work-unit index published
+  uint64_t unit_empty[2];  // all -> producer: work-unit index read
+  uint64_t q_full;         // Q tiles of a unit landed
+  uint64_t q_empty;        // last S MMAs of a unit done: Q may be replaced
   uint64_t kv_full[kSlots];
   uint64_t kv_empty[kSlots];
   uint64_t s_full[kQTiles];
   uint64_t p_full[kQTiles];
   uint64_t o_full[kQTiles];
+  uint64_t o_free[kQTiles];  // epilogue read O: the next unit may overwrite it
   uint64_t done;
 };
 
+// Everything a role derives from a work-unit index w: units [0, n_whole) are
+// whole items, the units after them are split_k pieces (tile windows) of each
+// remaining item, whose fp32 partials merge_split_kernel combines.
+struct Unit {
+  int w;  // unit index; -1: no more work
+  int b, hq, i, kvh, u0, split, sidx;
+  int n_tiles;
+  Schedule sch;
+};
+
+__device__ __forceinline__ void make_unit(int w, const AttnArgs& a, int n_pairs, int n_whole,
+                                          int split_k, Unit& U) {
+  const bool whole = w < n_whole;
+  U.w = w;
+  U.split = whole ? 1 : split_k;
+  U.sidx = whole ? 0 : w - n_whole;
+  int pair;
+  item_coords(whole ? w : n_whole + U.sidx / split_k, a, n_pairs, U.b, U.hq, U.i, pair);
+  const int piece = whole ? 0 : U.sidx % split_k;
+  U.kvh = U.hq / (a.Hq / a.Hkv);
+  const int Lb = a.S / a.P;
+  U.u0 = pair * kRowsPerCta;
+  Schedule& sch = U.sch;
+  sch.i = U.i;
+  sch.P = a.P;
+  sch.Lb = Lb;
+  sch.S = a.S;
+  sch.order = a.order;
+  sch.step_begin = a.step_begin;
+  sch.step_end = a.step_end;
+  const int u_last = min(U.u0 + kRowsPerCta, Lb) - 1;
+  const int t_first = static_cast<int>(block_token(a.order, a.S, a.P, U.i, U.u0));
+  const int t_last = static_cast<int>(block_token(a.order, a.S, a.P, U.i, u_last));
+  if (a.doc_start) {
+    sch.hull_lo = a.doc_start[static_cast<long long>(U.b % a.pos_rows) * a.S + t_first];
+    sch.hull_hi = t_last;
+  } else {
+    sch.hull_lo = 0;
+    sch.hull_hi = a.S - 1;
+  }
+  const int tot = sch.total();
+  sch.t_lo = static_cast<int>(static_cast<long long>(tot) * piece / U.split);
+  sch.t_hi = static_cast<int>(static_cast<long long>(tot) * (piece + 1) / U.split);
+  U.n_tiles = sch.t_hi - sch.t_lo;
+}
+
+// Persistent: each CTA runs work units until the counter passes n_work; the
+// producer fetches the next unit (the first one is blockIdx.x, the others
+// come from an atomic counter, so units start in heavy-first order) and
+// publishes its decoded description in a two-slot shared-memory mailbox that
+// the other roles read in place (a slot is released at the end of the unit).  The next unit's Q is loaded as
+// soon as the current unit's last S MMAs are done, and its first S MMAs run
+// while the softmax warps are still in the current unit's epilogue.
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bf16_kernel(const __grid_constant__ Tmaps tm, AttnArgs a, float scale_log2, int n_pairs,
-                     int n_whole, int split_k, float* __restrict__ part_o,
+                     int n_whole, int split_k, int n_work, float* __restrict__ part_o,
                      float* __restrict__ part_lse) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ Barriers bars;
+  __shared__ Unit units_s[2];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
 
@@ -162,51 +221,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- work item: CTAs [0, n_whole) run whole items; the CTAs after them
-  // run split_k pieces (tile windows) of each remaining item and write fp32
-  // partials that merge_split_kernel combines.  Scheduled last, the pieces
-  // fill the final wave of the launch.
-  const int cta = static_cast<int>(blockIdx.x);
-  const bool whole = cta < n_whole;
-  const int split = whole ? 1 : split_k;
-  const int sidx = whole ? 0 : cta - n_whole;  // index among the pieces
-  int b, hq, i, pair;
-  item_coords(whole ? cta : n_whole + sidx / split_k, a, n_pairs, b, hq, i, pair);
-  const int piece = whole ? 0 : sidx % split_k;
-  const int kvh = hq / (a.Hq / a.Hkv);
   const int Lb = a.S / a.P;
-  const int u0 = pair * kRowsPerCta;  // first local query row of the CTA
-
-  Schedule sch;
-  sch.i = i;
-  sch.P = a.P;
-  sch.Lb = Lb;
-  sch.S = a.S;
-  sch.order = a.order;
-  sch.step_begin = a.step_begin;
-  sch.step_end = a.step_end;
-  {
-    const int u_last = min(u0 + kRowsPerCta, Lb) - 1;
-    const int t_first = static_cast<int>(block_token(a.order, a.S, a.P, i, u0));
-    const int t_last = static_cast<int>(block_token(a.order, a.S, a.P, i, u_last));
-    if (a.doc_start) {
-      sch.hull_lo = a.doc_start[static_cast<long long>(b % a.pos_rows) * a.S + t_first];
-      sch.hull_hi = t_last;
-    } else {
-      sch.hull_lo = 0;
-      sch.hull_hi = a.S - 1;
-    }
-  }
-  {
-    const int tot = sch.total();
-    sch.t_lo = static_cast<int>(static_cast<long long>(tot) * piece / split);
-    sch.t_hi = static_cast<int>(static_cast<long long>(tot) * (piece + 1) / split);
-  }
-  const int n_tiles = sch.t_hi - sch.t_lo;
 
   if (threadIdx.x == 0) {
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(&bars.unit_full[x]), 1);
+      mbar_init(smem_u32(&bars.unit_empty[x]), 1 + 2 * kBM);
+    }
     mbar_init(smem_u32(&bars.q_full), 1);
+    mbar_init(smem_u32(&bars.q_empty), 1);
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(smem_u32(&bars.kv_full[s]), 1);
       mbar_init(smem_u32(&bars.kv_empty[s]), 1);
@@ -215,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars.s_full[t]), 1);
       mbar_init(smem_u32(&bars.p_full[t]), kBM);
       mbar_init(smem_u32(&bars.o_full[t]), 1);
+      mbar_init(smem_u32(&bars.o_free[t]), kBM);
     }
     mbar_init(smem_u32(&bars.done), 1);
     abort_s = 0;
@@ -247,54 +271,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tm.q);
       prefetch_tmap(&tm.k);
       prefetch_tmap(&tm.v);
-      const uint32_t qf = smem_u32(&bars.q_full);
-      mbar_arrive_expect_tx(qf, kQTiles * kTileBytes);
-      for (int t = 0; t < kQTiles; ++t) {
-        int c2, c3;
-        coord_rows(i, u0 + t * kBM, c2, c3);
-        for (int half = 0; half < 2; ++half)
-          tma_load_5d(smem_q + t * kTileBytes + half * kHalfBytes, &tm.q, qf, half * 64, hq, c2,
-                      c3, b);
-      }
-      int n = 0;   // load index: K_t = 2t, V_t = 2t + 1
-      int ft = 0;  // position in the item's tile sequence
+      int w = static_cast<int>(blockIdx.x) < n_work ? static_cast<int>(blockIdx.x) : -1;
+      int n = 0;   // K/V load index over the CTA's life: K, V of each tile in turn
+      int qn = 0;  // units with tiles so far (Q loads)
       bool ok = true;
-      for (int s = a.step_begin; s < a.step_end && ok && ft < sch.t_hi; ++s) {
-        int j, kt0, kt1;
-        sch.tiles(s, j, kt0, kt1);
-        for (int kt = kt0; kt <= kt1 && ok; ++kt, ++ft) {
-          if (ft < sch.t_lo) continue;
-          if (ft >= sch.t_hi) break;
-          int c2, c3;
-          coord_rows(j, kt * kBN, c2, c3);
-          for (int kv = 0; kv < 2; ++kv, ++n) {
-            const int slot = n % kSlots;
-            const uint32_t parity = ((n / kSlots) & 1) ^ 1;
-            if (!mbar_wait(smem_u32(&bars.kv_empty[slot]), parity, abort_flag, a.err,
-                           kErrKvEmpty)) {
-              ok = false;
-              break;
-            }
-            const uint32_t full = smem_u32(&bars.kv_full[slot]);
-            mbar_arrive_expect_tx(full, kTileBytes);
-            const CUtensorMap* map = kv == 0 ? &tm.k : &tm.v;
+      for (int seq = 0; ok; ++seq) {
+        const int x = seq & 1;
+        if (!mbar_wait(smem_u32(&bars.unit_empty[x]), ((seq >> 1) & 1) ^ 1, abort_flag, a.err,
+                       kErrUnit))
+          break;
+        Unit& U = units_s[x];
+        if (w >= 0)
+          make_unit(w, a, n_pairs, n_whole, split_k, U);
+        else
+          U.w = -1;
+        mbar_arrive(smem_u32(&bars.unit_full[x]));
+        if (w < 0) break;
+        if (U.n_tiles > 0) {
+          // this unit's Q replaces the previous one's once its S MMAs are done
+          if (!mbar_wait(smem_u32(&bars.q_empty), (qn & 1) ^ 1, abort_flag, a.err, kErrQEmpty))
+            break;
+          const uint32_t qf = smem_u32(&bars.q_full);
+          mbar_arrive_expect_tx(qf, kQTiles * kTileBytes);
+          for (int t = 0; t < kQTiles; ++t) {
+            int c2, c3;
+            coord_rows(U.i, U.u0 + t * kBM, c2, c3);
             for (int half = 0; half < 2; ++half)
-              tma_load_5d(smem_kv + slot * kTileBytes + half * kHalfBytes, map, full, half * 64,
-                          kvh, c2, c3, b);
+              tma_load_5d(smem_q + t * kTileBytes + half * kHalfBytes, &tm.q, qf, half * 64, U.hq,
+                          c2, c3, U.b);
+          }
+          ++qn;
+          int ft = 0;  // position in the item's tile sequence
+          for (int s = a.step_begin; s < a.step_end && ok && ft < U.sch.t_hi; ++s) {
+            int j, kt0, kt1;
+            U.sch.tiles(s, j, kt0, kt1);
+            for (int kt = kt0; kt <= kt1 && ok; ++kt, ++ft) {
+              if (ft < U.sch.t_lo) continue;
+              if (ft >= U.sch.t_hi) break;
+              int c2, c3;
+              coord_rows(j, kt * kBN, c2, c3);
+              for (int kv = 0; kv < 2; ++kv, ++n) {
+                const int slot = n % kSlots;
+                const uint32_t parity = ((n / kSlots) & 1) ^ 1;
+                if (!mbar_wait(smem_u32(&bars.kv_empty[slot]), parity, abort_flag, a.err,
+                               kErrKvEmpty)) {
+                  ok = false;
+                  break;
+                }
+                const uint32_t full = smem_u32(&bars.kv_full[slot]);
+                mbar_arrive_expect_tx(full, kTileBytes);
+                const CUtensorMap* map = kv == 0 ? &tm.k : &tm.v;
+                for (int half = 0; half < 2; ++half)
+                  tma_load_5d(smem_kv + slot * kTileBytes + half * kHalfBytes, map, full,
+                              half * 64, U.kvh, c2, c3, U.b);
+              }
+            }
           }
         }
+        w = static_cast<int>(gridDim.x) + atomicAdd(a.counter, 1);
+        if (w >= n_work) w = -1;
       }
       // drain: every copy this CTA started has landed before it may exit
-      mbar_wait(qf, 0, abort_flag, a.err, kErrDrain);
+      if (qn > 0) mbar_wait(smem_u32(&bars.q_full), (qn - 1) & 1, abort_flag, a.err, kErrDrain);
       for (int m = n - 1; m >= 0 && m >= n - kSlots; --m)
         mbar_wait(smem_u32(&bars.kv_full[m % kSlots]), (m / kSlots) & 1, abort_flag, a.err,
                   kErrDrain);
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------- MMA issuer
-    if (lane == 0 && n_tiles > 0) {
-      bool ok = mbar_wait(smem_u32(&bars.q_full), 0, abort_flag, a.err, kErrQFull);
-      tc_fence_after();
+    if (lane == 0) {
       // Descriptors are built once; a k-step only adds its byte offset >> 4
       // to the start-address field (all addresses stay below 256 KiB, so the
       // 14-bit field never carries).
@@ -317,49 +362,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O_t (+)= P_t V: P from TMEM (8 columns = 16 keys per k-step), V
       // MN-major: 16 keys = 2 swizzle atoms of 8 rows (stride 1024 B), the
       // two 64-column halves of d 16 KiB apart.
-      auto issue_pv = [&](int t, int it, int slot) {
+      auto issue_pv = [&](int t, bool first, int slot) {
         const uint64_t vb = dv0 + ((slot * kTileBytes) >> 4);
         const uint32_t d = tmem + 256 + t * 128;
         const uint32_t pa = tmem + t * 128;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           mma_ts(d, pa + kk * 8, vb + ((kk * 16 * 128) >> 4), kIdescPV,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+                 (!first || kk > 0) ? 1u : 0u);
       };
-      if (ok) ok = mbar_wait(smem_u32(&bars.kv_full[0]), 0, abort_flag, a.err, kErrKvFull);
-      tc_fence_after();
-      if (ok) {
-        issue_s(0, 0);
-        issue_s(1, 0);
-        mma_commit(smem_u32(&bars.kv_empty[0]));  // K_0 consumed
-      }
-      for (int it = 0; it < n_tiles && ok; ++it) {
-        const int v_idx = 2 * it + 1, k_next = 2 * it + 2;
-        const int v_slot = v_idx % kSlots, k_slot = k_next % kSlots;
-        if (!mbar_wait(smem_u32(&bars.kv_full[v_slot]), (v_idx / kSlots) & 1, abort_flag, a.err,
+      int n = 0;   // K/V load index (the producer's sequence)
+      int it = 0;  // tiles over the CTA's life (s_full / p_full phases)
+      int qn = 0;  // units with tiles so far
+      bool ok = true;
+      for (int seq = 0; ok; ++seq) {
+        const int x = seq & 1;
+        if (!mbar_wait(smem_u32(&bars.unit_full[x]), (seq >> 1) & 1, abort_flag, a.err, kErrUnit))
+          break;
+        const int nt = units_s[x].w < 0 ? -1 : units_s[x].n_tiles;
+        mbar_arrive(smem_u32(&bars.unit_empty[x]));  // everything it needs is in nt
+        if (nt < 0) break;
+        if (nt == 0) continue;
+        // first tile: S of both Q tiles as soon as Q and K_0 landed (the
+        // previous unit's PVs, issued before, read P from the same columns
+        // and complete first: tcgen05 MMAs of one thread run in order)
+        if (!mbar_wait(smem_u32(&bars.q_full), qn & 1, abort_flag, a.err, kErrQFull) ||
+            !mbar_wait(smem_u32(&bars.kv_full[n % kSlots]), (n / kSlots) & 1, abort_flag, a.err,
                        kErrKvFull))
           break;
-        const bool more = it + 1 < n_tiles;
-        if (more && !mbar_wait(smem_u32(&bars.kv_full[k_slot]), (k_next / kSlots) & 1,
-                               abort_flag, a.err, kErrKvFull))
-          break;
         tc_fence_after();
-        // tile 0: PV then next S
-        if (!mbar_wait(smem_u32(&bars.p_full[0]), it & 1, abort_flag, a.err, kErrPFull)) break;
-        tc_fence_after();
-        issue_pv(0, it, v_slot);
-        if (!more) mma_commit(smem_u32(&bars.o_full[0]));
-        if (more) issue_s(0, k_next);
-        // tile 1
-        if (!mbar_wait(smem_u32(&bars.p_full[1]), it & 1, abort_flag, a.err, kErrPFull)) break;
-        tc_fence_after();
-        issue_pv(1, it, v_slot);
-        mma_commit(smem_u32(&bars.kv_empty[v_slot]));  // V_it consumed
-        if (!more) mma_commit(smem_u32(&bars.o_full[1]));
-        if (more) {
-          issue_s(1, k_next);
-          mma_commit(smem_u32(&bars.kv_empty[k_slot]));  // K_{it+1} consumed
+        issue_s(0, n);
+        issue_s(1, n);
+        mma_commit(smem_u32(&bars.kv_empty[n % kSlots]));  // K_0 consumed
+        if (nt == 1) mma_commit(smem_u32(&bars.q_empty));
+        for (int lt = 0; lt < nt; ++lt, ++it, n += 2) {
+          const int v_idx = n + 1, k_next = n + 2;
+          const int v_slot = v_idx % kSlots, k_slot = k_next % kSlots;
+          const bool more = lt + 1 < nt;
+          if (!mbar_wait(smem_u32(&bars.kv_full[v_slot]), (v_idx / kSlots) & 1, abort_flag, a.err,
+                         kErrKvFull) ||
+              (more && !mbar_wait(smem_u32(&bars.kv_full[k_slot]), (k_next / kSlots) & 1,
+                                  abort_flag, a.err, kErrKvFull))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int t = 0; t < kQTiles; ++t) {
+            // PV_t(lt) once its P is in TMEM; the unit's first PV overwrites
+            // O_t, so it also waits for the previous unit's epilogue
+            if (!mbar_wait(smem_u32(&bars.p_full[t]), it & 1, abort_flag, a.err, kErrPFull) ||
+                (lt == 0 && !mbar_wait(smem_u32(&bars.o_free[t]), (qn & 1) ^ 1, abort_flag, a.err,
+                                       kErrOFree))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(t, lt == 0, v_slot);
+            if (t == kQTiles - 1) mma_commit(smem_u32(&bars.kv_empty[v_slot]));  // V_lt consumed
+            if (!more) {
+              mma_commit(smem_u32(&bars.o_full[t]));
+            } else {
+              issue_s(t, k_next);
+              if (t == kQTiles - 1) {
+                mma_commit(smem_u32(&bars.kv_empty[k_slot]));  // K_{lt+1} consumed
+                if (lt + 2 == nt) mma_commit(smem_u32(&bars.q_empty));  // last S of the unit
+              }
+            }
+          }
+          if (!ok) break;
         }
+        ++qn;
       }
       // every MMA issued has completed before TMEM is released
       mma_commit(smem_u32(&bars.done));
@@ -373,181 +445,185 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
     const uint32_t tO = tmem + lane_base + 256 + t * 128;
-    const int u = u0 + t * kBM + row;  // local row in block i
-    const bool row_live = u < Lb;
-    const int tq = row_live ? static_cast<int>(block_token(a.order, a.S, a.P, i, u)) : 0;
-    int lo, hi;
-    if (a.doc_start && row_live) {
-      lo = a.doc_start[static_cast<long long>(b % a.pos_rows) * a.S + tq];
-      hi = tq;
-    } else {
-      lo = 0;
-      hi = a.S - 1;
-    }
-    float m_run = -INFINITY;   // running max (log2 units, scaled)
-    float m_use = -INFINITY;   // exponent base actually applied
-    float l = 0.f;
-    int it = 0;  // tiles processed by this CTA
-    int ft = 0;  // position in the item's tile sequence
+    int it = 0;  // tiles over the CTA's life
+    int qn = 0;  // units with tiles so far
     bool ok = true;
-    for (int s = a.step_begin; s < a.step_end && ok && ft < sch.t_hi; ++s) {
-      int j, kt0, kt1;
-      sch.tiles(s, j, kt0, kt1);
-      for (int kt = kt0; kt <= kt1; ++kt, ++ft) {
-        if (ft < sch.t_lo) continue;
-        if (ft >= sch.t_hi) break;
-        // warp-uniform outcome: the tcgen05.ld below is warp-collective
-        const bool got = mbar_wait(smem_u32(&bars.s_full[t]), it & 1, abort_flag, a.err, kErrSFull);
-        if (!__all_sync(0xffffffffu, got)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // the whole score row: four 32-column loads in flight, one wait
-        uint32_t x[kBN];
+    for (int seq = 0; ok; ++seq) {
+      const int xs = seq & 1;
+      const bool got_unit =
+          mbar_wait(smem_u32(&bars.unit_full[xs]), (seq >> 1) & 1, abort_flag, a.err, kErrUnit);
+      if (!__all_sync(0xffffffffu, got_unit)) break;
+      const Unit& U = units_s[xs];  // read in place; released after the epilogue
+      if (U.w < 0) break;
+      const Schedule& sch = U.sch;
+      const int u = U.u0 + t * kBM + row;  // local row in block i
+      const bool row_live = u < Lb;
+      const int tq = row_live ? static_cast<int>(block_token(a.order, a.S, a.P, U.i, u)) : 0;
+      int lo, hi;
+      if (a.doc_start && row_live) {
+        lo = a.doc_start[static_cast<long long>(U.b % a.pos_rows) * a.S + tq];
+        hi = tq;
+      } else {
+        lo = 0;
+        hi = a.S - 1;
+      }
+      float m_run = -INFINITY;   // running max (log2 units, scaled)
+      float m_use = -INFINITY;   // exponent base actually applied
+      float l = 0.f;
+      int ft = 0;  // position in the item's tile sequence
+      for (int s = a.step_begin; s < a.step_end && ok && ft < sch.t_hi; ++s) {
+        int j, kt0, kt1;
+        sch.tiles(s, j, kt0, kt1);
+        for (int kt = kt0; kt <= kt1; ++kt, ++ft) {
+          if (ft < sch.t_lo) continue;
+          if (ft >= sch.t_hi) break;
+          // warp-uniform outcome: the tcgen05.ld below is warp-collective
+          const bool got =
+              mbar_wait(smem_u32(&bars.s_full[t]), it & 1, abort_flag, a.err, kErrSFull);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // the whole score row: four 32-column loads in flight, one wait
+          uint32_t x[kBN];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32_at(tS + c * 32, x, c * 32);
+          for (int c = 0; c < 4; ++c) tmem_ld32_at(tS + c * 32, x, c * 32);
+          tmem_wait_ld();
+          // allowed columns [c_lo, c_hi] of this tile for this row
+          int c_lo, c_hi;
+          {
+            int lo_c, hi_c;
+            const int w_base = kt * kBN;
+            if (a.order == SP_ORDER_STRIPED) {
+              lo_c = -floor_div(-(lo - j), a.P) - w_base;
+              hi_c = floor_div(hi - j, a.P) - w_base;
+            } else {
+              const int base = j * Lb + w_base;
+              lo_c = lo - base;
+              hi_c = hi - base;
+            }
+            const int c_valid = Lb - w_base - 1;
+            if (hi_c > c_valid) hi_c = c_valid;
+            c_lo = lo_c < 0 ? 0 : (lo_c > kBN ? kBN : lo_c);
+            c_hi = hi_c < -1 ? -1 : (hi_c > kBN - 1 ? kBN - 1 : hi_c);
+          }
+          if (c_lo > 0 || c_hi < kBN - 1) {
+#pragma unroll
+            for (int c = 0; c < kBN; ++c)
+              if (c < c_lo || c > c_hi) x[c] = 0xff800000u;  // -inf
+          }
+          // row max: 8 independent chains of 3-input max
+          float mx[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(x[k]);
+#pragma unroll
+          for (int c = 8; c < kBN - 8; c += 16) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mx[k] = fmax3(mx[k], __uint_as_float(x[c + k]), __uint_as_float(x[c + 8 + k]));
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(x[kBN - 8 + k]));
+          const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                 fmaxf(mx[6], mx[7]));
+          m_run = fmaxf(m_run, mt * scale_log2);
+          float alpha = 1.f;
+          bool rescale = false;
+          if (m_use == -INFINITY) {
+            m_use = m_run;  // first allowed key: O and l are still zero
+          } else if (m_run > m_use + kRescaleThreshold) {
+            alpha = ex2(m_use - m_run);
+            m_use = m_run;
+            rescale = true;
+          }
+          const float nbase = (m_use == -INFINITY) ? 0.f : -m_use;
+          // p = 2^(s * scale_log2 - base), two lanes per FFMA; 4 pair sums
+          float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < kBN; c += 2) {
+            float e0, e1;
+            ffma2(e0, e1, __uint_as_float(x[c]), __uint_as_float(x[c + 1]), scale_log2,
+                  scale_log2, nbase, nbase);
+            e0 = ex2(e0);
+            e1 = ex2(e1);
+            const int k = (c >> 1) & 3;
+            fadd2(sa[k], sb[k], sa[k], sb[k], e0, e1);
+            x[c >> 1] = pack_bf16(e0, e1);  // P row, packed in place (c/2 <= c)
+          }
+          l = l * alpha + ((sa[0] + sb[0]) + (sa[1] + sb[1])) + ((sa[2] + sb[2]) + (sa[3] + sb[3]));
+          tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+          tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+          // O *= alpha in TMEM (after the scores are dead, to keep registers
+          // free); the PV MMA that adds this tile waits for p_full below.
+          if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              uint32_t r[32];
+              tmem_ld32(tO + c * 32, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+              tmem_st32(tO + c * 32, r);
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bars.p_full[t]));
+          ++it;
+        }
+      }
+      // ---------------------------------------------------------- epilogue
+      const bool have = U.n_tiles > 0 && ok;
+      if (have) {
+        const bool got = mbar_wait(smem_u32(&bars.o_full[t]), qn & 1, abort_flag, a.err, kErrOFull);
+        if (!__all_sync(0xffffffffu, got)) ok = false;
+      }
+      tc_fence_after();
+      const bool any = have && ok && l > 0.f;
+      const float inv = any ? 1.f / l : 0.f;
+      const float row_lse = any ? (m_use + lg2(l)) * 0.69314718055994530942f : -INFINITY;
+      // the whole O row in one round trip, then O goes back to the MMA warp
+      // (the next unit's first PV overwrites it) before the stores
+      uint32_t r[kD];
+      if (have && ok) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32_at(tO + c * 32, r, c * 32);
         tmem_wait_ld();
-        // allowed columns [c_lo, c_hi] of this tile for this row
-        int c_lo, c_hi;
-        {
-          int lo_c, hi_c;
-          const int w_base = kt * kBN;
-          if (a.order == SP_ORDER_STRIPED) {
-            lo_c = -floor_div(-(lo - j), a.P) - w_base;
-            hi_c = floor_div(hi - j, a.P) - w_base;
-          } else {
-            const int base = j * Lb + w_base;
-            lo_c = lo - base;
-            hi_c = hi - base;
-          }
-          const int c_valid = Lb - w_base - 1;
-          if (hi_c > c_valid) hi_c = c_valid;
-          c_lo = lo_c < 0 ? 0 : (lo_c > kBN ? kBN : lo_c);
-          c_hi = hi_c < -1 ? -1 : (hi_c > kBN - 1 ? kBN - 1 : hi_c);
-        }
-        if (c_lo > 0 || c_hi < kBN - 1) {
+      } else {
 #pragma unroll
-          for (int c = 0; c < kBN; ++c)
-            if (c < c_lo || c > c_hi) x[c] = 0xff800000u;  // -inf
-        }
-        // row max: 8 independent chains of 3-input max
-        float mx[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(x[k]);
-#pragma unroll
-        for (int c = 8; c < kBN - 8; c += 16) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mx[k] = fmax3(mx[k], __uint_as_float(x[c + k]), __uint_as_float(x[c + 8 + k]));
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(x[kBN - 8 + k]));
-        const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                               fmaxf(mx[6], mx[7]));
-        m_run = fmaxf(m_run, mt * scale_log2);
-        float alpha = 1.f;
-        bool rescale = false;
-        if (m_use == -INFINITY) {
-          m_use = m_run;  // first allowed key: O and l are still zero
-        } else if (m_run > m_use + kRescaleThreshold) {
-          alpha = ex2(m_use - m_run);
-          m_use = m_run;
-          rescale = true;
-        }
-        const float nbase = (m_use == -INFINITY) ? 0.f : -m_use;
-        // p = 2^(s * scale_log2 - base), two lanes per FFMA; 4 pair sums
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < kBN; c += 2) {
-          float e0, e1;
-          ffma2(e0, e1, __uint_as_float(x[c]), __uint_as_float(x[c + 1]), scale_log2, scale_log2,
-                nbase, nbase);
-          e0 = ex2(e0);
-          e1 = ex2(e1);
-          const int k = (c >> 1) & 3;
-          fadd2(sa[k], sb[k], sa[k], sb[k], e0, e1);
-          x[c >> 1] = pack_bf16(e0, e1);  // P row, packed in place (c/2 <= c)
-        }
-        l = l * alpha + ((sa[0] + sb[0]) + (sa[1] + sb[1])) + ((sa[2] + sb[2]) + (sa[3] + sb[3]));
-        tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-        tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-        // O *= alpha in TMEM (after the scores are dead, to keep registers
-        // free); the PV MMA that adds this tile waits for p_full below.
-        if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tO + c * 32, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-            tmem_st32(tO + c * 32, r);
-          }
-        }
-        tmem_wait_st();
+        for (int e = 0; e < kD; ++e) r[e] = 0u;
+      }
+      if (U.n_tiles > 0) {
         tc_fence_before();
-        mbar_arrive(smem_u32(&bars.p_full[t]));
-        ++it;
+        mbar_arrive(smem_u32(&bars.o_free[t]));
+        ++qn;
       }
-    }
-    // ------------------------------------------------------------ epilogue
-    const bool have = n_tiles > 0 && ok;
-    if (have) {
-      const bool got = mbar_wait(smem_u32(&bars.o_full[t]), 0, abort_flag, a.err, kErrOFull);
-      if (!__all_sync(0xffffffffu, got)) ok = false;
-    }
-    tc_fence_after();
-    const bool any = have && ok && l > 0.f;
-    const float inv = any ? 1.f / l : 0.f;
-    const float row_lse = any ? (m_use + lg2(l)) * 0.69314718055994530942f : -INFINITY;
-    if (split > 1) {
-      // one piece of a split item: normalized partial O and its lse (fp32),
-      // combined afterwards by merge_split_kernel
-      const long long prow = static_cast<long long>(sidx) * kRowsPerCta + t * kBM + row;
-      float4* po = reinterpret_cast<float4*>(part_o + prow * kD);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        if (have && ok) {
-          tmem_ld32(tO + c * 32, r);
-          tmem_wait_ld();
-        } else {
+      if (U.split > 1) {
+        // one piece of a split item: normalized partial O and its lse (fp32),
+        // combined afterwards by merge_split_kernel
+        const long long prow = static_cast<long long>(U.sidx) * kRowsPerCta + t * kBM + row;
+        float4* po = reinterpret_cast<float4*>(part_o + prow * kD);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = 0u;
-        }
+        for (int e = 0; e < kD / 4; ++e)
+          po[e] = make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
+                              __uint_as_float(r[4 * e + 2]) * inv,
+                              __uint_as_float(r[4 * e + 3]) * inv);
+        part_lse[prow] = row_lse;
+      } else if (row_live) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+        uint4* orow = reinterpret_cast<uint4*>(
+            out + ((static_cast<long long>(U.b) * a.S + tq) * a.Hq + U.hq) * kD);
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          po[c * 8 + e] =
-              make_float4(__uint_as_float(r[4 * e]) * inv, __uint_as_float(r[4 * e + 1]) * inv,
-                          __uint_as_float(r[4 * e + 2]) * inv, __uint_as_float(r[4 * e + 3]) * inv);
+        for (int e = 0; e < kD / 8; ++e)
+          orow[e] = make_uint4(
+              pack_bf16(__uint_as_float(r[8 * e]) * inv, __uint_as_float(r[8 * e + 1]) * inv),
+              pack_bf16(__uint_as_float(r[8 * e + 2]) * inv, __uint_as_float(r[8 * e + 3]) * inv),
+              pack_bf16(__uint_as_float(r[8 * e + 4]) * inv, __uint_as_float(r[8 * e + 5]) * inv),
+              pack_bf16(__uint_as_float(r[8 * e + 6]) * inv, __uint_as_float(r[8 * e + 7]) * inv));
+        if (a.lse) a.lse[(static_cast<long long>(U.b) * a.Hq + U.hq) * a.S + tq] = row_lse;
       }
-      part_lse[prow] = row_lse;
-    } else {
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-      uint4* orow = reinterpret_cast<uint4*>(
-          out + ((static_cast<long long>(b) * a.S + tq) * a.Hq + hq) * kD);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        if (have && ok) {
-          tmem_ld32(tO + c * 32, r);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = 0u;
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
-        if (row_live) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            orow[c * 4 + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-        }
-      }
-      if (row_live && a.lse) a.lse[(static_cast<long long>(b) * a.Hq + hq) * a.S + tq] = row_lse;
+      mbar_arrive(smem_u32(&bars.unit_empty[xs]));
     }
   }
 
@@ -640,15 +716,20 @@ int launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
     const size_t need = static_cast<size_t>(rem * k) * kRowsPerCta * (kD + 1) * sizeof(float);
     if (k >= 2 && need <= a.scratch_bytes) split = static_cast<int>(k);
   }
+  // persistent grid: one CTA per SM (fewer when there is less work)
+  const long long n_work = split == 1 ? items : full + rem * split;
+  const unsigned grid = static_cast<unsigned>(n_work < G ? n_work : G);
   if (split == 1) {
-    attn_bf16_kernel<<<static_cast<unsigned>(items), kThreads, smem, stream>>>(
-        tm, a, scale_log2, n_pairs, static_cast<int>(items), 1, nullptr, nullptr);
+    attn_bf16_kernel<<<grid, kThreads, smem, stream>>>(tm, a, scale_log2, n_pairs,
+                                                       static_cast<int>(items), 1,
+                                                       static_cast<int>(n_work), nullptr, nullptr);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
   }
   float* part_o = static_cast<float*>(a.scratch);
   float* part_lse = part_o + static_cast<size_t>(rem * split) * kRowsPerCta * kD;
-  attn_bf16_kernel<<<static_cast<unsigned>(full + rem * split), kThreads, smem, stream>>>(
-      tm, a, scale_log2, n_pairs, static_cast<int>(full), split, part_o, part_lse);
+  attn_bf16_kernel<<<grid, kThreads, smem, stream>>>(tm, a, scale_log2, n_pairs,
+                                                     static_cast<int>(full), split,
+                                                     static_cast<int>(n_work), part_o, part_lse);
   merge_split_kernel<<<static_cast<unsigned>(rem * (kRowsPerCta / 8)), 256, 0, stream>>>(
       a, n_pairs, static_cast<int>(full), split, part_o, part_lse);
   return cudaGetLastError() == cudaSuccess ? 2 : -1;

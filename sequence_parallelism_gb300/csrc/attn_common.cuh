@@ -18,6 +18,7 @@ struct AttnArgs {
   void* out;                   // [B][S][Hq][d]
   float* lse;                  // [B][Hq][S] or nullptr
   int* err;                    // device error word
+  int* counter;                // work-unit counter of the persistent kernel (zeroed per call)
   int B, S, Hq, Hkv, d, P;
   int pos_rows;                // batch b reads doc_start row b % pos_rows
   int order;                   // sp_block_order
