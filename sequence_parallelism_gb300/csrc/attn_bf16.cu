@@ -51,7 +51,8 @@ constexpr int kRowsPerCta = kBM * kQTiles;
 constexpr int kSlots = 4;             // K/V ring depth
 constexpr int kTileBytes = kBN * kD * 2;          // 32 KiB
 constexpr int kHalfBytes = kTileBytes / 2;        // one 64-column half
-constexpr int kSmemBytes = (kQTiles + kSlots) * kTileBytes;
+constexpr int kStageBytes = kBM * 64 * 2;    // one 64-column half of an output tile
+constexpr int kSmemBytes = (kQTiles + kSlots) * kTileBytes + kQTiles * kStageBytes;
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -69,7 +70,7 @@ enum : int {
 };
 
 struct Tmaps {
-  CUtensorMap q, k, v;
+  CUtensorMap q, k, v, o;
 };
 
 // Token indices fit in int (S is an int), so the schedule works in 32 bits.
@@ -218,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t smem_q = smem_u32(smem);                         // Q0, Q1
   const uint32_t smem_kv = smem_q + kQTiles * kTileBytes;         // ring slots
+  const uint32_t smem_stage = smem_kv + kSlots * kTileBytes;      // output staging, per tile
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -610,21 +612,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                               __uint_as_float(r[4 * e + 2]) * inv,
                               __uint_as_float(r[4 * e + 3]) * inv);
         part_lse[prow] = row_lse;
-      } else if (row_live) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-        uint4* orow = reinterpret_cast<uint4*>(
-            out + ((static_cast<long long>(U.b) * a.S + tq) * a.Hq + U.hq) * kD);
+      } else {
+        // bf16 rows through a swizzled 16 KiB stage (one 64-column half at a
+        // time, the layout a 64 x 128-row TMA box with 128-byte swizzle has)
+        // and one bulk tensor store per half: coalesced, and asynchronous
+        // for the warpgroup
+        const uint32_t stage = smem_stage + t * kStageBytes;
+        const bool leader = row == 0;
+        int c2, c3;
+        coord_rows(U.i, U.u0 + t * kBM, c2, c3);
 #pragma unroll
-        for (int e = 0; e < kD / 8; ++e)
-          orow[e] = make_uint4(
-              pack_bf16(__uint_as_float(r[8 * e]) * inv, __uint_as_float(r[8 * e + 1]) * inv),
-              pack_bf16(__uint_as_float(r[8 * e + 2]) * inv, __uint_as_float(r[8 * e + 3]) * inv),
-              pack_bf16(__uint_as_float(r[8 * e + 4]) * inv, __uint_as_float(r[8 * e + 5]) * inv),
-              pack_bf16(__uint_as_float(r[8 * e + 6]) * inv, __uint_as_float(r[8 * e + 7]) * inv));
-        if (a.lse) a.lse[(static_cast<long long>(U.b) * a.Hq + U.hq) * a.S + tq] = row_lse;
+        for (int h = 0; h < 2; ++h) {
+          if (leader) bulk_wait_group_read0();  // the stage's previous store has read it
+          named_bar_sync(1 + t, kBM);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int e = h * 64 + c * 8;
+            const uint4 v = make_uint4(
+                pack_bf16(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv),
+                pack_bf16(__uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv),
+                pack_bf16(__uint_as_float(r[e + 4]) * inv, __uint_as_float(r[e + 5]) * inv),
+                pack_bf16(__uint_as_float(r[e + 6]) * inv, __uint_as_float(r[e + 7]) * inv));
+            const uint32_t addr = stage + row * 128 + ((c ^ (row & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
+                         "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1 + t, kBM);
+          if (leader) {
+            tma_store_5d(&tm.o, stage, h * 64, U.hq, c2, c3, U.b);
+            bulk_commit_group();
+          }
+        }
+        if (row_live && a.lse) a.lse[(static_cast<long long>(U.b) * a.Hq + U.hq) * a.S + tq] = row_lse;
       }
       mbar_arrive(smem_u32(&bars.unit_empty[xs]));
     }
+    if (row == 0) bulk_wait_group0();  // output stores complete before the CTA exits
   }
 
   tc_fence_before();
@@ -687,7 +712,8 @@ int launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
   Tmaps tm;
   if (!tmap::make_map(&tm.q, a.q, a.B, a.S, a.Hq, a.P, a.order) ||
       !tmap::make_map(&tm.k, a.k, a.B, a.S, a.Hkv, a.P, a.order) ||
-      !tmap::make_map(&tm.v, a.v, a.B, a.S, a.Hkv, a.P, a.order))
+      !tmap::make_map(&tm.v, a.v, a.B, a.S, a.Hkv, a.P, a.order) ||
+      !tmap::make_map(&tm.o, a.out, a.B, a.S, a.Hq, a.P, a.order))
     return -1;
   const int Lb = a.S / a.P;
   const int n_pairs = (Lb + kRowsPerCta - 1) / kRowsPerCta;
