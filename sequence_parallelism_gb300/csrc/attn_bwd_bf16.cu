@@ -496,12 +496,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
 constexpr int kKvThreads = 192;             // warps 0-3 elementwise, 4 TMA, 5 MMA
 constexpr int kKvProducer = 4;
 constexpr int kKvMma = 5;
-constexpr int kQT = 64;                      // query rows per streamed tile
-constexpr int kQTileBytes = kQT * kD * 2;    // 16 KiB
-constexpr int kQHalf = kQTileBytes / 2;
-constexpr int kQSlots = 4;
-constexpr int kKvSmemBytes = 2 * kTileBytes + kQSlots * 2 * kQTileBytes;
-constexpr uint32_t kIdescST = idesc_bf16_f32(kT, kQT, false);  // 128 keys x 64 queries
+constexpr int kQT = 128;                     // query rows per streamed tile
+constexpr int kQSlots = 2;                   // Q + dO tile pairs in flight
+constexpr int kKvSmemBytes = 2 * kTileBytes + kQSlots * 2 * kTileBytes;
 static_assert(kQT == kBwdRowPad, "query tiles are the block-order padding unit");
 
 enum : int { kInfoEnd = 0, kInfoTile = 1, kInfoFull = 3 };
@@ -517,11 +514,19 @@ struct alignas(16) ColData {
   int pad;
 };
 
+// One CTA per 128-key tile (K, V resident).  Per 128-query tile:
+//   S^T = K Q^T, dP^T = V dO^T            (SS, into TMEM [0,128) / [128,256))
+//   elementwise, in two 64-column halves:  P^T, dS^T (bf16 pairs) written over
+//     the first 32 (half 0) / next 32 (half 1) columns of S^T / dP^T
+//   dV += P^T dO, dK += dS^T Q            (TS, one 64-query half at a time:
+//     half 0's products run while half 1 is being computed)
+// TMEM is full (S^T, dP^T, dV, dK), so S^T of the next tile waits for the
+// last dV/dK product of this one (tcgen05 MMAs of one thread run in order).
 __global__ void __launch_bounds__(kKvThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ BwdMaps tm, BwdArgs a, int n_tiles_k) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t q_full[kQSlots], q_empty[kQSlots], kv_full, s_full[2], ds_full[2],
-      dkv_full, done;
+  __shared__ uint64_t q_full[kQSlots], q_empty[kQSlots], kv_full, s_full, half_full[2], dkv_full,
+      done;
   __shared__ ColData cols[kQSlots];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
@@ -547,10 +552,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       mbar_init(smem_u32(&q_empty[s]), 1);
     }
     mbar_init(smem_u32(&kv_full), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&s_full[s]), 1);
-      mbar_init(smem_u32(&ds_full[s]), kT);
-    }
+    mbar_init(smem_u32(&s_full), 1);
+    mbar_init(smem_u32(&half_full[0]), kT);
+    mbar_init(smem_u32(&half_full[1]), kT);
     mbar_init(smem_u32(&dkv_full), 1);
     mbar_init(smem_u32(&done), 1);
     abort_s = 0;
@@ -565,9 +569,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
   volatile int* abort_flag = &abort_s;
-  // TMEM columns: S^T buffers [0,64) [64,128), dP^T buffers [128,192) [192,256),
-  // dV [256,384), dK [384,512).  P^T and dS^T (bf16 pairs) overwrite the
-  // first 32 columns of their S^T / dP^T buffer.
+  // TMEM columns: S^T [0,128), dP^T [128,256), dV [256,384), dK [384,512)
   const uint32_t cdP = 128, cdV = 256, cdK = 384;
 
   if (warp == kKvProducer) {
@@ -626,10 +628,10 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               cd.i = i;
               cd.u0 = u0;
               const uint32_t bar = smem_u32(&q_full[slot]);
-              const uint32_t dst = sslot + slot * 2 * kQTileBytes;
-              mbar_arrive_expect_tx(bar, 2 * kQTileBytes + col_bytes);
-              row_tma(dst, &tm.q, bar, h, a.order, i, u0, b, kQHalf);
-              row_tma(dst + kQTileBytes, &tm.dout, bar, h, a.order, i, u0, b, kQHalf);
+              const uint32_t dst = sslot + slot * 2 * kTileBytes;
+              mbar_arrive_expect_tx(bar, 2 * kTileBytes + col_bytes);
+              row_tma(dst, &tm.q, bar, h, a.order, i, u0, b);
+              row_tma(dst + kTileBytes, &tm.dout, bar, h, a.order, i, u0, b);
               const long long off = blk_index(bhq, a.P, a.Lbp, i, u0);
               bulk_load(smem_u32(cd.lse2), a.lse2_blk + off, kQT * 4, bar);
               bulk_load(smem_u32(cd.D), a.D_blk + off, kQT * 4, bar);
@@ -664,8 +666,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       const uint64_t dk0 = smem_desc_sw128(sk, 16, 1024), dv0 = smem_desc_sw128(sv, 16, 1024);
-      const uint64_t dkq = smem_desc_sw128(sslot, 16, 1024);      // K-major Q / dO views
-      const uint64_t dmn = smem_desc_sw128(sslot, kQHalf, 1024);  // MN-major Q / dO views
+      const uint64_t dkq = smem_desc_sw128(sslot, 16, 1024);          // K-major Q / dO views
+      const uint64_t dmn = smem_desc_sw128(sslot, kHalfBytes, 1024);  // MN-major Q / dO views
       // info of tile t once its slot is full; -1 when the wait gave up
       auto tile_info = [&](int t) -> int {
         const int slot = t % kQSlots;
@@ -674,56 +676,53 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           return -1;
         return cols[slot].info;
       };
-      // S^T = K Q^T and dP^T = V dO^T for tile t, into buffer t & 1
+      // S^T = K Q^T and dP^T = V dO^T for tile t (N = 128 queries)
       auto issue_sdp = [&](int t) {
         tc_fence_after();
-        const uint64_t qb = dkq + (((t % kQSlots) * 2 * kQTileBytes) >> 4);
-        const uint64_t ob = qb + (kQTileBytes >> 4);
-        const uint32_t buf = (t & 1) * 64;
+        const uint64_t qb = dkq + (((t % kQSlots) * 2 * kTileBytes) >> 4);
+        const uint64_t ob = qb + (kTileBytes >> 4);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tmem + buf, kmaj_desc(dk0, kk), kmaj_desc(qb, kk, kQHalf), kIdescST,
-                 kk > 0 ? 1u : 0u);
+          mma_ss(tmem, kmaj_desc(dk0, kk), kmaj_desc(qb, kk), kIdescKmaj, kk > 0 ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tmem + cdP + buf, kmaj_desc(dv0, kk), kmaj_desc(ob, kk, kQHalf), kIdescST,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(smem_u32(&s_full[t & 1]));
+          mma_ss(tmem + cdP, kmaj_desc(dv0, kk), kmaj_desc(ob, kk), kIdescKmaj, kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&s_full));
       };
-      // dV += P^T dO and dK += dS^T Q for tile t (64 queries: 4 k-steps)
-      auto issue_grad = [&](int t) {
-        const int slot = t % kQSlots;
-        const uint64_t qb = dmn + ((slot * 2 * kQTileBytes) >> 4);
-        const uint64_t ob = qb + (kQTileBytes >> 4);
-        const uint32_t buf = (t & 1) * 64;
+      // dV += P^T dO and dK += dS^T Q over the 64 queries of half h of tile t
+      auto issue_grad = [&](int t, int h) {
+        const uint64_t qb = dmn + (((t % kQSlots) * 2 * kTileBytes) >> 4);
+        const uint64_t ob = qb + (kTileBytes >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kQT / 16; ++kk)
-          mma_ts(tmem + cdV, tmem + buf + kk * 8, ob + ((kk * 16 * 128) >> 4), kIdescBmn,
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = h * 4 + k4;  // 16-query step within the tile
+          mma_ts(tmem + cdV, tmem + kk * 8, ob + ((kk * 16 * 128) >> 4), kIdescBmn,
                  (t > 0 || kk > 0) ? 1u : 0u);
+        }
 #pragma unroll
-        for (int kk = 0; kk < kQT / 16; ++kk)
-          mma_ts(tmem + cdK, tmem + cdP + buf + kk * 8, qb + ((kk * 16 * 128) >> 4), kIdescBmn,
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = h * 4 + k4;
+          mma_ts(tmem + cdK, tmem + cdP + kk * 8, qb + ((kk * 16 * 128) >> 4), kIdescBmn,
                  (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&q_empty[slot]));
+        }
       };
       bool ok = mbar_wait(smem_u32(&kv_full), 0, abort_flag, a.err, kErrBwdKvFull);
       int cur = ok ? tile_info(0) : -1;
       if (cur > 0) issue_sdp(0);
-      int nxt = cur > 0 ? tile_info(1) : 0;
-      if (nxt > 0) issue_sdp(1);
       for (int t = 0; cur > 0; ++t) {
-        if (!mbar_wait(smem_u32(&ds_full[t & 1]), (t >> 1) & 1, abort_flag, a.err,
-                       kErrBwdDsFull))
-          break;
-        tc_fence_after();
-        issue_grad(t);
-        int nn = 0;
-        if (nxt > 0) {
-          nn = tile_info(t + 2);
-          if (nn > 0) issue_sdp(t + 2);
+        bool got = true;
+        for (int h = 0; h < 2 && got; ++h) {
+          got = mbar_wait(smem_u32(&half_full[h]), t & 1, abort_flag, a.err, kErrBwdDsFull);
+          if (got) {
+            tc_fence_after();
+            issue_grad(t, h);
+          }
         }
+        if (!got) break;
+        mma_commit(smem_u32(&q_empty[t % kQSlots]));  // Q_t, dO_t consumed
+        const int nxt = tile_info(t + 1);
+        if (nxt > 0) issue_sdp(t + 1);
         cur = nxt;
-        nxt = nn;
       }
       mma_commit(smem_u32(&dkv_full));
       mma_commit(smem_u32(&done));
@@ -750,17 +749,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const ColData& cd = cols[slot];
       const int info = cd.info;
       if (info == kInfoEnd) break;
-      if (!wait_warp(smem_u32(&s_full[t & 1]), (t >> 1) & 1, abort_flag, a.err, kErrBwdSFull)) {
+      if (!wait_warp(smem_u32(&s_full), t & 1, abort_flag, a.err, kErrBwdSFull)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t buf = (t & 1) * 64;
-      uint32_t sx[64], px[64];
-      tmem_ld32_at(tmem + lane_base + buf, sx, 0);
-      tmem_ld32_at(tmem + lane_base + buf + 32, sx, 32);
-      tmem_ld32_at(tmem + lane_base + cdP + buf, px, 0);
-      tmem_ld32_at(tmem + lane_base + cdP + buf + 32, px, 32);
       const bool full = info == kInfoFull;
       // causal part of the mask: column c holds a query token >= ktok iff c >= c_min
       int c_min = 0;
@@ -768,39 +761,51 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         c_min = a.order == SP_ORDER_STRIPED ? -floor_div_i(-(ktok - cd.i), a.P) - cd.u0
                                             : ktok - (cd.i * Lb + cd.u0);
       }
-      tmem_wait_ld();
-      uint32_t pk[32], dk[32];
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sx[64], px[64];
+        tmem_ld32_at(tmem + lane_base + h * 64, sx, 0);
+        tmem_ld32_at(tmem + lane_base + h * 64 + 32, sx, 32);
+        tmem_ld32_at(tmem + lane_base + cdP + h * 64, px, 0);
+        tmem_ld32_at(tmem + lane_base + cdP + h * 64 + 32, px, 32);
+        tmem_wait_ld();
+        uint32_t pk[32], dk[32];
 #pragma unroll
-      for (int c = 0; c < kQT; c += 4) {
-        const float4 l2 = *reinterpret_cast<const float4*>(&cd.lse2[c]);
-        const float4 D = *reinterpret_cast<const float4*>(&cd.D[c]);
-        float x0, x1, x2, x3;
-        ffma2(x0, x1, __uint_as_float(sx[c]), __uint_as_float(sx[c + 1]), sl2, sl2, -l2.x, -l2.y);
-        ffma2(x2, x3, __uint_as_float(sx[c + 2]), __uint_as_float(sx[c + 3]), sl2, sl2, -l2.z,
-              -l2.w);
-        float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-        if (!full) {
-          const int4 lo = *reinterpret_cast<const int4*>(&cd.lo[c]);
-          if (c < c_min || lo.x > ktok) p0 = 0.f;
-          if (c + 1 < c_min || lo.y > ktok) p1 = 0.f;
-          if (c + 2 < c_min || lo.z > ktok) p2 = 0.f;
-          if (c + 3 < c_min || lo.w > ktok) p3 = 0.f;
+        for (int c4 = 0; c4 < 64; c4 += 4) {
+          const int c = h * 64 + c4;  // column of the tile
+          const float4 l2 = *reinterpret_cast<const float4*>(&cd.lse2[c]);
+          const float4 D = *reinterpret_cast<const float4*>(&cd.D[c]);
+          float x0, x1, x2, x3;
+          ffma2(x0, x1, __uint_as_float(sx[c4]), __uint_as_float(sx[c4 + 1]), sl2, sl2, -l2.x,
+                -l2.y);
+          ffma2(x2, x3, __uint_as_float(sx[c4 + 2]), __uint_as_float(sx[c4 + 3]), sl2, sl2, -l2.z,
+                -l2.w);
+          float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+          if (!full) {
+            const int4 lo = *reinterpret_cast<const int4*>(&cd.lo[c]);
+            if (c < c_min || lo.x > ktok) p0 = 0.f;
+            if (c + 1 < c_min || lo.y > ktok) p1 = 0.f;
+            if (c + 2 < c_min || lo.z > ktok) p2 = 0.f;
+            if (c + 3 < c_min || lo.w > ktok) p3 = 0.f;
+          }
+          float d0, d1, d2, d3;
+          fadd2(d0, d1, __uint_as_float(px[c4]), __uint_as_float(px[c4 + 1]), -D.x, -D.y);
+          fadd2(d2, d3, __uint_as_float(px[c4 + 2]), __uint_as_float(px[c4 + 3]), -D.z, -D.w);
+          fmul2(d0, d1, d0, d1, p0, p1);
+          fmul2(d2, d3, d2, d3, p2, p3);
+          pk[c4 >> 1] = pack_bf16(p0, p1);
+          pk[(c4 >> 1) + 1] = pack_bf16(p2, p3);
+          dk[c4 >> 1] = pack_bf16(d0, d1);
+          dk[(c4 >> 1) + 1] = pack_bf16(d2, d3);
         }
-        float d0, d1, d2, d3;
-        fadd2(d0, d1, __uint_as_float(px[c]), __uint_as_float(px[c + 1]), -D.x, -D.y);
-        fadd2(d2, d3, __uint_as_float(px[c + 2]), __uint_as_float(px[c + 3]), -D.z, -D.w);
-        fmul2(d0, d1, d0, d1, p0, p1);
-        fmul2(d2, d3, d2, d3, p2, p3);
-        pk[c >> 1] = pack_bf16(p0, p1);
-        pk[(c >> 1) + 1] = pack_bf16(p2, p3);
-        dk[c >> 1] = pack_bf16(d0, d1);
-        dk[(c >> 1) + 1] = pack_bf16(d2, d3);
+        // half h's 64 queries as 32 bf16-pair columns; S^T / dP^T columns
+        // [32h, 32h + 32) were read in half 0
+        tmem_st32(tmem + lane_base + h * 32, pk);
+        tmem_st32(tmem + lane_base + cdP + h * 32, dk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&half_full[h]));
       }
-      tmem_st32(tmem + lane_base + buf, pk);
-      tmem_st32(tmem + lane_base + cdP + buf, dk);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&ds_full[t & 1]));
     }
     // epilogue: dK * scale and dV, rows of key token ktok
     const bool have = t > 0 && ok;
@@ -848,16 +853,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
 
 // prep, then dQ and dK/dV (independent of each other) on the tensor cores.
 int launch_attn_bwd_bf16(const BwdArgs& a, cudaStream_t st) {
-  BwdMaps tm, tk;
+  BwdMaps tm;  // 128-row boxes for both kernels
   if (!tmap::make_map(&tm.q, a.q, a.B, a.S, a.Hq, a.P, a.order) ||
       !tmap::make_map(&tm.dout, a.dout, a.B, a.S, a.Hq, a.P, a.order) ||
       !tmap::make_map(&tm.k, a.k, a.B, a.S, a.Hkv, a.P, a.order) ||
-      !tmap::make_map(&tm.v, a.v, a.B, a.S, a.Hkv, a.P, a.order) ||
-      !tmap::make_map(&tk.q, a.q, a.B, a.S, a.Hq, a.P, a.order, kQT) ||
-      !tmap::make_map(&tk.dout, a.dout, a.B, a.S, a.Hq, a.P, a.order, kQT))
+      !tmap::make_map(&tm.v, a.v, a.B, a.S, a.Hkv, a.P, a.order))
     return -1;
-  tk.k = tm.k;
-  tk.v = tm.v;
   const int Lb = a.S / a.P;
   PrepArgs pa;
   pa.out = static_cast<const uint4*>(a.out);
@@ -888,7 +889,7 @@ int launch_attn_bwd_bf16(const BwdArgs& a, cudaStream_t st) {
   const unsigned n_q = static_cast<unsigned>(a.P) * n_tiles * a.B * a.Hq;
   bwd_dq_kernel<<<n_q, kQThreads, dq_smem, st>>>(tm, a, n_tiles);
   const unsigned n_kv = static_cast<unsigned>(a.P) * n_tiles * a.B * a.Hkv;
-  bwd_dkdv_kernel<<<n_kv, kKvThreads, kv_smem, st>>>(tk, a, n_tiles);
+  bwd_dkdv_kernel<<<n_kv, kKvThreads, kv_smem, st>>>(tm, a, n_tiles);
   return cudaGetLastError() == cudaSuccess ? 3 : -1;
 }
 

@@ -60,7 +60,7 @@ struct BwdArgs {
 
 int launch_attn_bwd_simt(const BwdArgs& a, cudaStream_t stream);
 int launch_attn_bwd_bf16(const BwdArgs& a, cudaStream_t stream);  // d == 128
-constexpr int kBwdRowPad = 64;  // Lbp = S / P rounded up to a multiple of this
+constexpr int kBwdRowPad = 128;  // Lbp = S / P rounded up to a multiple of this
 
 // Validates and runs one blockwise-attention call (doc_start scan when
 // position_ids != NULL, then the f32 or bf16 kernel).  position_ids has
