@@ -1,7 +1,6 @@
 """Shared test helpers: tensor conversion and the parity bars.
 
-Bars (from the task's parity requirements, compared against the float64
-oracle on the same inputs):
+Bars, against the float64 oracle on the same inputs:
   * permutations and doc_start: bit-exact;
   * bf16 attention (fp32 accumulation): max |out - ref| <= 2e-2 and
     mean |out - ref| <= 2e-3;
