@@ -129,6 +129,13 @@ __device__ __forceinline__ uint64_t kmaj_desc(uint64_t base, int kk, int half = 
   return base + ((((kk >> 2) * half) + (kk & 3) * 32) >> 4);
 }
 
+// Wait that first tests without blocking: loads that usually landed long ago
+// then cost the issuing thread little (a blocking wait costs ~150 cycles).
+__device__ __forceinline__ bool wait_ready(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           int* err, int code) {
+  return mbar_test_wait(bar, parity) || mbar_wait(bar, parity, abort_flag, err, code);
+}
+
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int* err, int code) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err, code));
@@ -344,14 +351,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
       // S = Q K^T, then dP = dO V^T for tile t, each as soon as its operand landed
       auto issue_sdp = [&](int t) -> bool {
         const int ks = t % kKSlots, vs = t % kVSlots;
-        if (!mbar_wait(smem_u32(&k_full[ks]), (t / kKSlots) & 1, abort_flag, a.err, kErrBwdKvFull))
+        if (!wait_ready(smem_u32(&k_full[ks]), (t / kKSlots) & 1, abort_flag, a.err, kErrBwdKvFull))
           return false;
         tc_fence_after();
         const uint64_t kb = dk0 + ((ks * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
           mma_ss(tmem + cS, kmaj_desc(dq_, kk), kmaj_desc(kb, kk), kIdescKmaj, kk > 0 ? 1u : 0u);
-        if (!mbar_wait(smem_u32(&v_full[vs]), (t / kVSlots) & 1, abort_flag, a.err, kErrBwdKvFull))
+        if (!wait_ready(smem_u32(&v_full[vs]), (t / kVSlots) & 1, abort_flag, a.err, kErrBwdKvFull))
           return false;
         tc_fence_after();
         const uint64_t vb = dv0 + ((vs * kTileBytes) >> 4);
@@ -671,8 +678,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       // info of tile t once its slot is full; -1 when the wait gave up
       auto tile_info = [&](int t) -> int {
         const int slot = t % kQSlots;
-        if (!mbar_wait(smem_u32(&q_full[slot]), (t / kQSlots) & 1, abort_flag, a.err,
-                       kErrBwdQFull))
+        if (!wait_ready(smem_u32(&q_full[slot]), (t / kQSlots) & 1, abort_flag, a.err,
+                        kErrBwdQFull))
           return -1;
         return cols[slot].info;
       };
