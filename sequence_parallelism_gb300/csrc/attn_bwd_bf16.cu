@@ -439,7 +439,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
         c_lo -= col0;
         c_hi -= col0;
-        const bool whole = c_lo <= 0 && c_hi >= 63;
+        // masked scores become -inf (p = 0), outside the exp loop
+        if (c_lo > 0 || c_hi < 63) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < c_lo || c > c_hi) sx[c] = 0xff800000u;
+        }
         uint32_t dsw[32];  // dS, bf16 pairs
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
@@ -448,10 +453,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
                 -lse2);
           p0 = ex2(x0);
           p1 = ex2(x1);
-          if (!whole) {
-            if (c < c_lo || c > c_hi) p0 = 0.f;
-            if (c + 1 < c_lo || c + 1 > c_hi) p1 = 0.f;
-          }
           fadd2(d0, d1, __uint_as_float(px[c]), __uint_as_float(px[c + 1]), -Drow, -Drow);
           fmul2(d0, d1, d0, d1, p0, p1);
           dsw[c >> 1] = pack_bf16(d0, d1);
@@ -776,6 +777,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         tmem_ld32_at(tmem + lane_base + cdP + h * 64, px, 0);
         tmem_ld32_at(tmem + lane_base + cdP + h * 64 + 32, px, 32);
         tmem_wait_ld();
+        if (!full) {  // masked scores become -inf (p = 0), outside the exp loop
+#pragma unroll
+          for (int c4 = 0; c4 < 64; c4 += 4) {
+            const int c = h * 64 + c4;
+            const int4 lo = *reinterpret_cast<const int4*>(&cd.lo[c]);
+            if (c < c_min || lo.x > ktok) sx[c4] = 0xff800000u;
+            if (c + 1 < c_min || lo.y > ktok) sx[c4 + 1] = 0xff800000u;
+            if (c + 2 < c_min || lo.z > ktok) sx[c4 + 2] = 0xff800000u;
+            if (c + 3 < c_min || lo.w > ktok) sx[c4 + 3] = 0xff800000u;
+          }
+        }
         uint32_t pk[32], dk[32];
 #pragma unroll
         for (int c4 = 0; c4 < 64; c4 += 4) {
@@ -787,14 +799,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
                 -l2.y);
           ffma2(x2, x3, __uint_as_float(sx[c4 + 2]), __uint_as_float(sx[c4 + 3]), sl2, sl2, -l2.z,
                 -l2.w);
-          float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
-          if (!full) {
-            const int4 lo = *reinterpret_cast<const int4*>(&cd.lo[c]);
-            if (c < c_min || lo.x > ktok) p0 = 0.f;
-            if (c + 1 < c_min || lo.y > ktok) p1 = 0.f;
-            if (c + 2 < c_min || lo.z > ktok) p2 = 0.f;
-            if (c + 3 < c_min || lo.w > ktok) p3 = 0.f;
-          }
+          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
           float d0, d1, d2, d3;
           fadd2(d0, d1, __uint_as_float(px[c4]), __uint_as_float(px[c4 + 1]), -D.x, -D.y);
           fadd2(d2, d3, __uint_as_float(px[c4 + 2]), __uint_as_float(px[c4 + 3]), -D.z, -D.w);
