@@ -399,23 +399,26 @@ def extra_measurements(args, peaks):
             "note": "doc_start scan + attention kernel, median of reps"}
         del q, k, v, out
     res["llama8b_32k_causal_backward"] = backward_measurement(peaks, flush, stream)
-    x = torch.randn((1, 32768, 32, 128), device="cuda").to(torch.bfloat16)
-    y = torch.empty((8, 1, 32768, 4, 128), dtype=torch.bfloat16, device="cuda")
-    for _ in range(3):
-        _lib.sp_ulysses_seq_to_head(x, y, 8)
-    ms = []
-    for _ in range(20):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        _lib.sp_ulysses_seq_to_head(x, y, 8)
-        b.record(stream)
-        ms.append((a, b))
-    torch.cuda.synchronize()
-    t = statistics.median([a.elapsed_time(b) for a, b in ms])
-    gbs = 2.0 * x.numel() * 2 / (t * 1e-3) / 1e9
-    res["permute_256MiB"] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
-                             "shape": "[1][32768][32][128] bf16, P=8"}
+    # the q shapes of llama8b_32k (256 MiB) and packed_128k (1 GiB)
+    for S_, label in ((32768, "permute_256MiB"), (131072, "permute_1GiB")):
+        x = torch.randn((1, S_, 32, 128), device="cuda").to(torch.bfloat16)
+        y = torch.empty((8, 1, S_, 4, 128), dtype=torch.bfloat16, device="cuda")
+        for _ in range(3):
+            _lib.sp_ulysses_seq_to_head(x, y, 8)
+        ms = []
+        for _ in range(20):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            _lib.sp_ulysses_seq_to_head(x, y, 8)
+            b.record(stream)
+            ms.append((a, b))
+        torch.cuda.synchronize()
+        t = statistics.median([a.elapsed_time(b) for a, b in ms])
+        gbs = 2.0 * x.numel() * 2 / (t * 1e-3) / 1e9
+        res[label] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                      "shape": f"[1][{S_}][32][128] bf16, P=8"}
+        del x, y
     return res
 
 

@@ -156,8 +156,10 @@ sp_status sp_segment_starts(const int32_t* position_ids, int32_t* doc_start, int
  *
  * workspace: device scratch of at least
  * sp_blockwise_attn_workspace_bytes(B, S, position_ids != NULL) bytes,
- * 256-byte aligned; it holds the device error word and the doc_start
- * array.  Its contents need not be initialised.  A non-causal bf16 call given
+ * 256-byte aligned; it holds the device error word, the persistent kernel's
+ * work counter (both reset by the call) and the doc_start array, so calls
+ * that may run concurrently (different streams) need separate workspaces.
+ * Its contents need not be initialised.  A non-causal bf16 call given
  * sp_blockwise_attn_split_workspace_bytes(...) bytes (about 21 MiB more) may
  * also split the items of its last, partly filled wave of CTAs into pieces
  * whose fp32 partial results are merged by their log-sum-exp (the ring's
