@@ -10,6 +10,7 @@ without the built library raises ImportError -- there is no CPU path.
     ring_step(q, k, v, P, step, ...)           one ring step's partial result
     merge_partials(outs, lses)                 log-sum-exp combine of partials
     ulysses_attention(q, k, v, P, ...)         permute -> attention -> permute back
+    ulysses_attention_backward(ctx, dout)      its gradients (permute, backward, permute)
     ulysses_ring_attention(q, k, v, P_u, P_r)  Ulysses + Ring hybrid (heads < devices)
     blockwise_attention_backward(...)          dq, dk, dv from out, dout and lse
     doc_starts(position_ids)                   O(n) causal-mask carrier
@@ -21,7 +22,8 @@ from . import _lib
 from ._lib import SPError  # noqa: F401
 
 __all__ = ["seq_to_head", "head_to_seq", "blockwise_attention", "ring_step", "merge_partials",
-           "ulysses_attention", "ulysses_ring_attention", "blockwise_attention_backward",
+           "ulysses_attention", "ulysses_attention_backward", "ulysses_ring_attention",
+           "blockwise_attention_backward",
            "doc_starts", "attention_workspace",
            "SPError"]
 
@@ -107,29 +109,64 @@ def doc_starts(position_ids):
     return _lib.sp_segment_starts(position_ids, ds, ws)
 
 
-def ulysses_attention(q, k, v, P, ring_blocks=None, order="contiguous", scale=0.0, fused=False):
+def ulysses_attention(q, k, v, P, ring_blocks=None, order="contiguous", scale=0.0, fused=False,
+                      position_ids=None, return_context=False):
     """One Ulysses attention layer simulated on one GPU.
 
     q [B][S][Hq][d], k/v [B][S][Hkv][d] in sequence-sharded layout: permute to
     head groups ([P][B][S][H/P][d] = batch P*B), run blockwise attention with
-    `ring_blocks` blocks per head group (default P), permute back.  Non-causal.
+    `ring_blocks` blocks per head group (default P), permute back.
+    position_ids [B][S] (optional) makes it causal; every head group sees all
+    positions, so each group uses the same rows.
 
     fused=True skips both permutations: on one GPU, attention on the
     sequence-sharded tensors computes every head group's result in place and
     writes the output already in sequence-sharded layout (bit-identical).
+
+    return_context=True also returns what ulysses_attention_backward needs
+    (the head-sharded q, k, v, output and lse).
     """
     B, S, Hq, d = q.shape
+    rb = ring_blocks or P
     if fused:
-        out, _ = blockwise_attention(q, k, v, ring_blocks or P, order, None, scale)
-        return out
+        out, lse = blockwise_attention(q, k, v, rb, order, position_ids, scale)
+        ctx = dict(fused=True, q=q, k=k, v=v, out=out, lse=lse, P=P, rb=rb, order=order,
+                   pos=position_ids, scale=scale)
+        return (out, ctx) if return_context else out
     G, Gk = Hq // P, k.shape[2] // P
     yq = torch.empty((P, B, S, G, d), dtype=q.dtype, device=q.device)
     yk = torch.empty((P, B, S, Gk, d), dtype=k.dtype, device=k.device)
     yv = torch.empty_like(yk)
     _lib.sp_ulysses_seq_to_head_qkv(q, k, v, yq, yk, yv, P)
-    yo, _ = blockwise_attention(yq.view(P * B, S, G, d), yk.view(P * B, S, Gk, d),
-                                yv.view(P * B, S, Gk, d), ring_blocks or P, order, None, scale)
-    return head_to_seq(yo.view(P, B, S, G, d))
+    ypos = None if position_ids is None else position_ids.repeat(P, 1)
+    yo, ylse = blockwise_attention(yq.view(P * B, S, G, d), yk.view(P * B, S, Gk, d),
+                                   yv.view(P * B, S, Gk, d), rb, order, ypos, scale)
+    out = head_to_seq(yo.view(P, B, S, G, d))
+    if not return_context:
+        return out
+    ctx = dict(fused=False, yq=yq, yk=yk, yv=yv, yo=yo, ylse=ylse, P=P, rb=rb, order=order,
+               pos=ypos, scale=scale)
+    return out, ctx
+
+
+def ulysses_attention_backward(ctx, dout):
+    """Gradients (dq, dk, dv) of a Ulysses layer, in sequence-sharded layout:
+    dout goes to the head groups (the layer's second all-to-all, transposed),
+    every group runs the blockwise attention backward, and the gradients come
+    back (the first all-to-all, transposed)."""
+    P, rb, order, pos, scale = ctx["P"], ctx["rb"], ctx["order"], ctx["pos"], ctx["scale"]
+    if ctx["fused"]:
+        return blockwise_attention_backward(ctx["q"], ctx["k"], ctx["v"], ctx["out"], dout,
+                                            ctx["lse"], rb, order, pos, scale)
+    yq, yk, yv, yo, ylse = ctx["yq"], ctx["yk"], ctx["yv"], ctx["yo"], ctx["ylse"]
+    _, B, S, G, d = yq.shape
+    Gk = yk.shape[3]
+    ydo = seq_to_head(dout, P)
+    dyq, dyk, dyv = blockwise_attention_backward(
+        yq.view(P * B, S, G, d), yk.view(P * B, S, Gk, d), yv.view(P * B, S, Gk, d),
+        yo.view(P * B, S, G, d), ydo.view(P * B, S, G, d), ylse, rb, order, pos, scale)
+    return (head_to_seq(dyq.view(P, B, S, G, d)), head_to_seq(dyk.view(P, B, S, Gk, d)),
+            head_to_seq(dyv.view(P, B, S, Gk, d)))
 
 
 def ulysses_ring_attention(q, k, v, P_u, P_r, order="contiguous", position_ids=None, scale=0.0,
