@@ -59,11 +59,16 @@ def test_backward_bf16(sp, B, S, Hq, Hkv, P, order, pos):
     _run_bwd(sp, "bf16", B, S, Hq, Hkv, 128, P, order, pos, 850 + S)
 
 
-@pytest.mark.parametrize("pos_kind,fused", [("causal", False), ("packed", False), ("none", True)])
-def test_ulysses_layer_backward(sp, pos_kind, fused):
+@pytest.mark.parametrize("pos_kind,fused,ring_blocks", [("causal", False, None),
+                                                      ("packed", False, None),
+                                                      ("none", True, None),
+                                                      ("causal", False, 2)])
+def test_ulysses_layer_backward(sp, pos_kind, fused, ring_blocks):
     """Gradients of a whole Ulysses layer (seq->head, blockwise attention per
     head group, head->seq; GQA with one key/value head per group) against the
-    oracle's derivatives of plain attention on the sequence-sharded tensors."""
+    oracle's derivatives of plain attention on the sequence-sharded tensors.
+    ring_blocks=2 is the Ulysses + Ring hybrid (4 head groups x 2 ring
+    blocks)."""
     B, S, Hq, Hkv, d, P = 1, 768, 8, 4, 128, 4
     q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 990, "bf16")
     g = torch.Generator(device="cuda")
@@ -71,12 +76,12 @@ def test_ulysses_layer_backward(sp, pos_kind, fused):
     dout = torch.randn(q.shape, generator=g, device="cuda").to(q.dtype)
     pos = _positions(pos_kind, B, S, 992)
     tpos = None if pos is None else torch.from_numpy(pos).cuda()
-    out, ctx = sp.ulysses_attention(q, k, v, P, position_ids=tpos, fused=fused,
-                                    return_context=True)
+    out, ctx = sp.ulysses_attention(q, k, v, P, ring_blocks=ring_blocks, position_ids=tpos,
+                                    fused=fused, return_context=True)
     dq, dk, dv = sp.ulysses_attention_backward(ctx, dout)
     torch.cuda.synchronize()
     rq, rk, rv = oracle.attention_backward(np32(q), np32(k), np32(v), np32(dout), pos)
-    tag = f"ulysses {pos_kind} fused={fused}"
+    tag = f"ulysses {pos_kind} fused={fused} ring_blocks={ring_blocks}"
     check_grad(np32(dq), rq, "bf16", "dq " + tag)
     check_grad(np32(dk), rk, "bf16", "dk " + tag)
     check_grad(np32(dv), rv, "bf16", "dv " + tag)
