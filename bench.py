@@ -590,8 +590,12 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     if not os.path.exists(os.path.join(ROOT, "sequence_parallelism_gb300", "libsp_gb300.so")):
-        import __graft_entry__
-        __graft_entry__.build()
+        if rank == 0:  # one rank compiles; the others wait for it
+            import __graft_entry__
+            __graft_entry__.build()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
     res = run_ours(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(res), flush=True)
