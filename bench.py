@@ -12,11 +12,14 @@ doc_start from position_ids + causal blockwise attention.
 
 Reported value: attention TFLOP/s over the whole step (algorithmic FLOPs:
 4*d per allowed (query, key) pair per query head), aggregated over ranks.
-L2 (129 MB) is flushed between timed steps by writing a 512 MiB buffer,
-outside the timed events.  The JSON line also carries the dominant kernel's
-roofline, the permutation's bandwidth, the causal Llama-3.1-8B-shaped
-attention rate, an end-to-end number with host buffers, the CPU oracle
-baseline, and the SM clocks sampled during the timed region.
+L2 (129 MB) is flushed between timed steps, outside the timed events, by
+writing a 512 MiB buffer and then reading another 512 MiB buffer: the read
+evicts the dirty lines the write leaves behind, so that their write-back does
+not land in the next timed kernel (the flush leaves L2 cold and clean).
+The JSON line also carries the dominant kernel's roofline, the
+permutation's bandwidth, the causal Llama-3.1-8B-shaped attention rate, an
+end-to-end number with host buffers, the CPU oracle baseline, and the SM
+clocks sampled during the timed region.
 
 Multi-GPU: every rank runs its own independent replica of the step (the
 head groups / batches of the path are independent; no collective on the data
@@ -77,6 +80,21 @@ def attention_flops(cfg, pos):
 def rank_seed(seed, rank):
     """Each rank draws its own replica of the workload (weak scaling)."""
     return seed + 7919 * rank
+
+
+class L2Flush:
+    """Evicts L2 (129 MB) between timed iterations: write 512 MiB, then read
+    512 MiB of another buffer so that no dirty line of the write is left to be
+    written back inside the next timed kernel."""
+
+    def __init__(self, device="cuda"):
+        import torch
+        self.wr = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+        self.rd = torch.zeros(128 << 20, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.wr.zero_()
+        self.rd.sum()
 
 
 def max_over_ranks(value, world, device=None):
@@ -217,7 +235,7 @@ def run_ours(args, rank, world, local_rank):
     def step(ev=None):
         return enqueue(q, k, v, out, ev)
 
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     def barrier():
         if world > 1:
@@ -240,7 +258,7 @@ def run_ours(args, rank, world, local_rank):
     wall0 = time.perf_counter()
     launches = 0
     for i in range(args.steps):
-        flush.zero_()  # evict L2 between steps (outside the timed events)
+        flush()  # evict L2 between steps (outside the timed events)
         launches += step(evs[i])
     torch.cuda.synchronize()
     barrier()
@@ -276,7 +294,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": args.workload, "B": B, "S": S, "Hq": Hq, "Hkv": Hkv, "d": d,
                    "P": P, "order": order, "causal": pos is not None,
                    "parallelism": f"replicas{world}" if world > 1 else "single GPU",
-                   "l2": "flushed between timed steps (512 MiB write)"},
+                   "l2": "flushed between timed steps (512 MiB write, then 512 MiB read)"},
         "roofline": roofline,
         "gpu_launches": launches,
         "clocks": clocks,
@@ -368,7 +386,7 @@ def extra_measurements(args, peaks):
 
     res = {}
     stream = torch.cuda.current_stream()
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     if args.workload != "llama8b_32k":
         cfg = workloads.CONFIGS["llama8b_32k"]
         B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
@@ -383,7 +401,7 @@ def extra_measurements(args, peaks):
         reps = 20
         ms = []
         for _ in range(reps):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             _lib.sp_blockwise_attn_fwd(q, k, v, pos, P, "contiguous", 0.0, out, lse, ws)
@@ -407,7 +425,7 @@ def extra_measurements(args, peaks):
             _lib.sp_ulysses_seq_to_head(x, y, 8)
         ms = []
         for _ in range(20):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             _lib.sp_ulysses_seq_to_head(x, y, 8)
@@ -450,7 +468,7 @@ def backward_measurement(peaks, flush, stream, reps=20):
     launches = _lib.sp_last_launch_count()
     ms = []
     for _ in range(reps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         call()
