@@ -494,10 +494,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          // the whole score row: four 32-column loads in flight, one wait
+          // the whole score row: four 32-column loads in flight, one wait;
+          // each load also returns the max of its 32 scores
           uint32_t x[kBN];
+          float hm[4];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32_at(tS + c * 32, x, c * 32);
+          for (int c = 0; c < 4; ++c) tmem_ld32_max_at(tS + c * 32, x, c * 32, hm[c]);
           tmem_wait_ld();
           // allowed columns [c_lo, c_hi] of this tile for this row
           int c_lo, c_hi;
@@ -517,25 +519,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             c_lo = lo_c < 0 ? 0 : (lo_c > kBN ? kBN : lo_c);
             c_hi = hi_c < -1 ? -1 : (hi_c > kBN - 1 ? kBN - 1 : hi_c);
           }
+          // row max: on a tile with every column allowed, the loads' own
+          // maxima; on a masked tile, over the allowed columns only (8
+          // independent chains of 3-input max)
+          float mt = fmax3(hm[0], hm[1], fmaxf(hm[2], hm[3]));
           if (c_lo > 0 || c_hi < kBN - 1) {
 #pragma unroll
             for (int c = 0; c < kBN; ++c)
               if (c < c_lo || c > c_hi) x[c] = 0xff800000u;  // -inf
+            float mx[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(x[k]);
+#pragma unroll
+            for (int c = 8; c < kBN - 8; c += 16) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                mx[k] = fmax3(mx[k], __uint_as_float(x[c + k]), __uint_as_float(x[c + 8 + k]));
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(x[kBN - 8 + k]));
+            mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                       fmaxf(mx[6], mx[7]));
           }
-          // row max: 8 independent chains of 3-input max
-          float mx[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) mx[k] = __uint_as_float(x[k]);
-#pragma unroll
-          for (int c = 8; c < kBN - 8; c += 16) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mx[k] = fmax3(mx[k], __uint_as_float(x[c + k]), __uint_as_float(x[c + 8 + k]));
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], __uint_as_float(x[kBN - 8 + k]));
-          const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                 fmaxf(mx[6], mx[7]));
           m_run = fmaxf(m_run, mt * scale_log2);
           float alpha = 1.f;
           bool rescale = false;
