@@ -92,9 +92,14 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 // abort_flag: CTA-shared flag; err: global error word; code: what to record.
 // Two limits: wall time (timeout_ns of %globaltimer) and, as a second guard
 // in case the timer misbehaves, a cap on the number of polling rounds.
+// A phase that has already completed is detected with the non-blocking
+// test_wait: a satisfied try_wait in a thread with tcgen05.mma instructions
+// in flight was measured to hold that thread for thousands of cycles, while
+// a test_wait returns in about 20.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int* abort_flag, int* err, int code,
                                           uint64_t timeout_ns = SP_WAIT_TIMEOUT_NS) {
+  if (mbar_test_wait(bar, parity)) return true;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   const uint32_t sleep_ns = timeout_ns < 4000000ull ? 1000u : 1000000u;
