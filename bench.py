@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
 # kernel from the committed ncu capture (profiles/attn_bf16_kernel.md; None
 # for workloads not captured at their own size).
-NCU_TRAFFIC_BYTES = {}  # ncu dram bytes per launch of the current kernel, per workload
+NCU_TRAFFIC_BYTES = {"ulysses_4k": 233173760}  # ncu dram read + write bytes per launch
 
 
 def load_peaks():

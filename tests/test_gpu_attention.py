@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import check_attention, np32, torch_dtype
+from helpers import BF16_MAX_ABS, F32_MAX_ABS, check_attention, np32, torch_dtype
 from sequence_parallelism_gb300 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -88,6 +88,38 @@ def test_f32_parity(sp, B, S, Hq, Hkv, d, P, order, pos):
 ])
 def test_bf16_parity(sp, B, S, Hq, Hkv, P, order, pos):
     _run(sp, "bf16", B, S, Hq, Hkv, 128, P, order, pos, 200 + S + P)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("order", ["contiguous", "striped"])
+def test_masked_scores_never_set_the_exponent_base(sp, dtype, order):
+    """Causal rows t < 1000 share key tiles with keys j >= 1000 that they may
+    not see and whose scores are about 102 (147 in log2 units) while every
+    key they may see scores about N(0, 1).  Had a masked score entered a
+    row's running max, the allowed weights (2^-140 and below) would flush to
+    zero and the row would come out as zeros; rows t >= 1000 see the large
+    keys and average their values uniformly."""
+    B, S, H, d, P = 1, 2048, 1, 128, 2
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4242)
+    q = torch.ones((B, S, H, d), device="cuda")
+    k = torch.randn((B, S, H, d), generator=g, device="cuda")
+    k[:, 1000:] = 9.0
+    v = torch.randn((B, S, H, d), generator=g, device="cuda")
+    q, k, v = (x.to(torch_dtype(dtype)).contiguous() for x in (q, k, v))
+    pos = _positions("causal", B, S, 0)
+    out, lse = sp.blockwise_attention(q, k, v, P, order, torch.from_numpy(pos).cuda())
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.full_attention(np32(q), np32(k), np32(v), pos)
+    o, l = np32(out), lse.cpu().numpy()
+    check_attention(o[:, :1000], l[:, :, :1000], ref_out[:, :1000], ref_lse[:, :, :1000], dtype,
+                    f"{dtype} {order} rows beside large masked scores")
+    assert np.abs(o[0, 990:1000]).max() > 0.05
+    # rows that see the large keys: lse near 105, compared relatively
+    tol = BF16_MAX_ABS if dtype == "bf16" else F32_MAX_ABS
+    assert np.abs(o[:, 1000:] - ref_out[:, 1000:]).max() <= tol
+    rel = np.abs(l[:, :, 1000:] - ref_lse[:, :, 1000:]) / np.abs(ref_lse[:, :, 1000:])
+    assert rel.max() <= 1e-5
 
 
 @pytest.mark.parametrize("dtype,d", [("bf16", 128), ("f32", 32)])
