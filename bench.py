@@ -291,10 +291,8 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 q/k/v; seeded packed-document position_ids)",
-        "config": {"workload": args.workload, "B": B, "S": S, "Hq": Hq, "Hkv": Hkv, "d": d,
-                   "P": P, "order": order, "causal": pos is not None,
-                   "parallelism": f"replicas{world}" if world > 1 else "single GPU",
-                   "l2": "flushed between timed steps (512 MiB write, then 512 MiB read)"},
+        "config": dict(workload_config(args.workload, cfg, order, world),
+                       l2="flushed between timed steps (512 MiB write, then 512 MiB read)"),
         "roofline": roofline,
         "gpu_launches": launches,
         "clocks": clocks,
@@ -546,6 +544,13 @@ def cpu_baseline(cfg, workload, order, budget_s=15.0):
             "seconds": round(sec, 2)}
 
 
+def workload_config(name, cfg, order, world):
+    """The `config` keys both arms report for a workload."""
+    return {"workload": name, "B": cfg["B"], "S": cfg["S"], "Hq": cfg["Hq"], "Hkv": cfg["Hkv"],
+            "d": cfg["d"], "P": cfg["P"], "order": order, "causal": bool(cfg.get("causal")),
+            "parallelism": f"replicas{world}" if world > 1 else "single GPU"}
+
+
 def run_reference(args, rank, world):
     """The oracle as it stands, timed on the host cores: each step one bounded
     sample of the workload, sized so K + W steps take about two minutes."""
@@ -570,7 +575,8 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(tot_s * 1e3 / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "order": order},
+            "config": dict(workload_config(args.workload, cfg, order, world),
+                           l2="not applicable (host cores)"),
             "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "kind": "oracle",
                              "cores": os.cpu_count(), "sample": sample},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
