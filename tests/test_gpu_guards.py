@@ -202,3 +202,19 @@ def test_hybrid_writes_stay_inside(sp):
     # lse in the head-sharded layout: group r holds heads r*Hq/P_u ...
     ref_lse_h = ref_lse.reshape(B, P_u, Hq // P_u, S).transpose(1, 0, 2, 3)
     check_attention(np32(out.t), lse.t.cpu().numpy(), ref_out, ref_lse_h, "bf16", "hybrid")
+
+
+def test_noalloc_writes_stay_inside_out_lse():
+    """The allocation-free entry point keeps its scratch in a static device
+    array; its outputs must still be written exactly within out and lse."""
+    B, S, Hq, Hkv, d, P = 1, 1536, 2, 1, 128, 3
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 780, "bf16")
+    pos = _positions("packed", B, S, 780)
+    tpos = torch.from_numpy(pos).cuda()
+    out = Guarded(q.shape, q.dtype)
+    lse = Guarded((B, Hq, S), torch.float32)
+    _lib.sp_blockwise_attn_fwd_noalloc(q, k, v, tpos, P, "striped", 0.0, out.t, lse.t)
+    _assert_guarded("noalloc", ("out", out), ("lse", lse))
+    _no_nan("noalloc", out=out.t)
+    ref_out, ref_lse = oracle.full_attention(np32(q), np32(k), np32(v), pos)
+    check_attention(np32(out.t), lse.t.cpu().numpy(), ref_out, ref_lse, "bf16", "noalloc")
