@@ -719,16 +719,26 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       if (cur > 0) issue_sdp(0);
       for (int t = 0; cur > 0; ++t) {
         bool got = true;
+        int nxt = -2;  // tile t+1's info, once known
         for (int h = 0; h < 2 && got; ++h) {
           got = mbar_wait(smem_u32(&half_full[h]), t & 1, abort_flag, a.err, kErrBwdDsFull);
           if (got) {
+            // Tile t+1's Q and dO have usually landed by now: test it here,
+            // where the thread has just woken, rather than after the
+            // gradient MMAs, where a barrier access waits for the issue
+            // queue to drain while the tensor pipe runs dry.
+            if (h == 0) {
+              const int ns = (t + 1) % kQSlots;
+              if (mbar_test_wait(smem_u32(&q_full[ns]), ((t + 1) / kQSlots) & 1))
+                nxt = cols[ns].info;
+            }
             tc_fence_after();
             issue_grad(t, h);
           }
         }
         if (!got) break;
         mma_commit(smem_u32(&q_empty[t % kQSlots]));  // Q_t, dO_t consumed
-        const int nxt = tile_info(t + 1);
+        if (nxt == -2) nxt = tile_info(t + 1);
         if (nxt > 0) issue_sdp(t + 1);
         cur = nxt;
       }
