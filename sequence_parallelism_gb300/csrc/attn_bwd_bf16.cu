@@ -353,14 +353,20 @@ __global__ void __launch_bounds__(kQThreads, 1)
         const int ks = t % kKSlots, vs = t % kVSlots;
         if (!wait_ready(smem_u32(&k_full[ks]), (t / kKSlots) & 1, abort_flag, a.err, kErrBwdKvFull))
           return false;
+        // V_t has usually landed too: test it now, so that dP follows S
+        // without a barrier access between the two batches of MMAs
+        const bool v_ready = mbar_test_wait(smem_u32(&v_full[vs]), (t / kVSlots) & 1);
         tc_fence_after();
         const uint64_t kb = dk0 + ((ks * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
           mma_ss(tmem + cS, kmaj_desc(dq_, kk), kmaj_desc(kb, kk), kIdescKmaj, kk > 0 ? 1u : 0u);
-        if (!wait_ready(smem_u32(&v_full[vs]), (t / kVSlots) & 1, abort_flag, a.err, kErrBwdKvFull))
-          return false;
-        tc_fence_after();
+        if (!v_ready) {
+          if (!wait_ready(smem_u32(&v_full[vs]), (t / kVSlots) & 1, abort_flag, a.err,
+                          kErrBwdKvFull))
+            return false;
+          tc_fence_after();
+        }
         const uint64_t vb = dv0 + ((vs * kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk)
