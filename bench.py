@@ -327,6 +327,8 @@ def e2e(args, inputs, out, enqueue, flops, world, dev):
     direction on this machine, is the bound)."""
     import torch
     comp = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    ref = out.cpu()  # the device-timed steps' result on the same inputs
     hosts = [t.cpu().pin_memory() for t in inputs]
     bufs_in = [tuple(inputs), tuple(torch.empty_like(t) for t in inputs)]
     bufs_out = [out, torch.empty_like(out)]
@@ -365,11 +367,16 @@ def e2e(args, inputs, out, enqueue, flops, world, dev):
     e1.record(comp)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    # what came back to the host is what the device-timed steps computed
+    # (the kernels are deterministic): both download buffers, bit for bit
+    for b in range(2):
+        if not torch.equal(hout[b], ref):
+            raise RuntimeError(f"end-to-end output (buffer {b}) differs from the device result")
     h2d = sum(t.numel() * t.element_size() for t in inputs)
     d2h = out.numel() * out.element_size()
     return {"value": round(job_tflops(flops, world, n, ms), 2), "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(ms / n, 4), "steps": n,
+            "ms_per_step": round(ms / n, 4), "steps": n, "checked": True,
             "note": "uploads and downloads on two copy streams, double-buffered, overlapping "
                     "the kernels of the neighbouring steps"}
 
