@@ -95,6 +95,9 @@ def test_attention_rejects_bad_arguments(lib):
     assert _attn(lib, order=2) == SP_ERR_INVALID_ARG
     assert _attn(lib, dt=5) == SP_ERR_INVALID_ARG
     assert _attn(lib, P=0) == SP_ERR_INVALID_ARG
+    assert _attn(lib, S=0) == SP_ERR_INVALID_ARG              # empty sequence
+    assert _attn(lib, B=0) == SP_ERR_INVALID_ARG              # empty batch
+    assert _attn(lib, Hq=0, Hkv=0) == SP_ERR_INVALID_ARG      # no heads
     assert _attn(lib, scale=float("nan")) == SP_ERR_INVALID_ARG
     assert _attn(lib, d=64) == SP_ERR_UNSUPPORTED              # bf16 needs d == 128
     assert _attn(lib, d=512, dt=1) == SP_ERR_UNSUPPORTED       # f32 d <= 256

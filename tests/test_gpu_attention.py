@@ -90,6 +90,21 @@ def test_bf16_parity(sp, B, S, Hq, Hkv, P, order, pos):
     _run(sp, "bf16", B, S, Hq, Hkv, 128, P, order, pos, 200 + S + P)
 
 
+@pytest.mark.parametrize("dtype,B,S,Hq,Hkv,P,order,pos", [
+    ("bf16", 2, 1, 2, 1, 1, "contiguous", "causal"),     # a single token
+    ("bf16", 1, 1, 1, 1, 1, "striped", "none"),
+    ("bf16", 1, 256, 2, 1, 256, "contiguous", "causal"),  # one token per block
+    ("bf16", 1, 256, 2, 2, 256, "striped", "packed"),
+    ("bf16", 1, 256, 4, 1, 256, "striped", "none"),       # ... with the tail split
+    ("f32", 2, 1, 2, 1, 1, "contiguous", "causal"),
+    ("f32", 1, 64, 2, 1, 64, "striped", "packed"),
+])
+def test_degenerate_shapes(sp, dtype, B, S, Hq, Hkv, P, order, pos):
+    """The smallest shapes the method admits: one token in all, and blocks of
+    one token each (every ring step then brings a single key)."""
+    _run(sp, dtype, B, S, Hq, Hkv, 128 if dtype == "bf16" else 16, P, order, pos, 900 + S + P)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("order", ["contiguous", "striped"])
 def test_masked_scores_never_set_the_exponent_base(sp, dtype, order):

@@ -59,6 +59,17 @@ def test_backward_bf16(sp, B, S, Hq, Hkv, P, order, pos):
     _run_bwd(sp, "bf16", B, S, Hq, Hkv, 128, P, order, pos, 850 + S)
 
 
+@pytest.mark.parametrize("dtype,B,S,Hq,Hkv,P,order,pos", [
+    ("bf16", 2, 1, 2, 1, 1, "contiguous", "causal"),     # a single token
+    ("bf16", 1, 256, 2, 1, 256, "striped", "causal"),    # one token per block
+    ("f32", 1, 1, 1, 1, 1, "contiguous", "none"),
+    ("f32", 1, 64, 2, 1, 64, "striped", "packed"),
+])
+def test_backward_degenerate_shapes(sp, dtype, B, S, Hq, Hkv, P, order, pos):
+    _run_bwd(sp, dtype, B, S, Hq, Hkv, 128 if dtype == "bf16" else 16, P, order, pos,
+             950 + S + P)
+
+
 @pytest.mark.parametrize("pos_kind,fused,ring_blocks", [("causal", False, None),
                                                       ("packed", False, None),
                                                       ("none", True, None),
