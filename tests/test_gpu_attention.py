@@ -218,6 +218,64 @@ def test_no_device_error_reported(sp):
     assert _lib.sp_last_launch_count() == 1
 
 
+def test_repeated_calls_share_one_workspace(sp):
+    """Calls of different shapes and kinds, repeated and interleaved, through
+    one workspace: each call resets the work counter and the error word it
+    keeps there, so every repeat reproduces its first result bit for bit
+    (the kernels are deterministic) and the first results match the oracle."""
+    from sequence_parallelism_gb300 import _lib
+    shapes = [  # (B, S, Hq, Hkv, P, order, pos kind)
+        (1, 2048, 4, 2, 4, "contiguous", "causal"),
+        (2, 1000, 4, 2, 2, "contiguous", "none"),     # takes the tail split
+        (1, 1536, 2, 1, 3, "striped", "packed"),
+    ]
+    n = max(_lib.sp_blockwise_attn_split_workspace_bytes(B, S, pos != "none")
+            for B, S, _, _, _, _, pos in shapes)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    cases, first = [], []
+    for c, (B, S, Hq, Hkv, P, order, kind) in enumerate(shapes):
+        q, k, v = workloads.small_case(B, S, Hq, Hkv, 128, 600 + c, "bf16")
+        pos = _positions(kind, B, S, 600 + c)
+        cases.append((q, k, v, P, order, None if pos is None else torch.from_numpy(pos).cuda(),
+                      pos))
+    for rep in range(4):
+        for c, (q, k, v, P, order, tpos, pos) in enumerate(cases):
+            out, lse = sp.blockwise_attention(q, k, v, P, order, tpos, workspace=ws)
+            torch.cuda.synchronize()
+            st, code = _lib.sp_get_device_error(ws)
+            assert st == 0 and code == 0
+            if rep == 0:
+                first.append((out.clone(), lse.clone()))
+                ref_out, ref_lse = oracle.full_attention(np32(q), np32(k), np32(v), pos)
+                check_attention(np32(out), lse.cpu().numpy(), ref_out, ref_lse, "bf16",
+                                f"shape {c}")
+            else:
+                assert torch.equal(out.view(torch.int16), first[c][0].view(torch.int16)), (rep, c)
+                assert torch.equal(lse, first[c][1]), (rep, c)
+
+
+def test_calls_on_a_side_stream(sp):
+    """The binding launches on torch's current stream: work queued on a side
+    stream is ordered after that stream's earlier work and gives the same
+    result as on the default stream."""
+    B, S, Hq, Hkv, P = 1, 2048, 4, 2, 4
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, 128, 610, "bf16")
+    pos = _positions("causal", B, S, 610)
+    tpos = torch.from_numpy(pos).cuda()
+    out0, lse0 = sp.blockwise_attention(q, k, v, P, "contiguous", tpos)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        q2 = q.clone()             # produced on the side stream ...
+        out1, lse1 = sp.blockwise_attention(q2, k, v, P, "contiguous", tpos)  # ... and read there
+        y = sp.seq_to_head(q2, P)
+        back = sp.head_to_seq(y)
+    side.synchronize()
+    assert torch.equal(out1.view(torch.int16), out0.view(torch.int16))
+    assert torch.equal(lse1, lse0)
+    assert torch.equal(back, q)
+
+
 def test_fused_ulysses_is_bit_identical_to_permuted_pipeline(sp):
     """On one GPU, attention on the sequence-sharded tensors computes every
     Ulysses head group in place: same result, bit for bit, with no
