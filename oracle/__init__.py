@@ -27,7 +27,7 @@ Sources (web pages, cited by title and section):
   ("6ステップ"): causal mask carried by position_ids in O(n) memory instead
   of a 4D mask.
 
-Readings of points the pages leave open (all listed in the design doc):
+Readings of points the pages leave open:
 
 * causal semantics of position_ids: a document restarts wherever
   position_ids does not continue by +1 (and at token 0); token i may attend
