@@ -422,6 +422,7 @@ def extra_measurements(args, peaks):
             "note": "doc_start scan + attention kernel, median of reps"}
         del q, k, v, out
     res["llama8b_32k_causal_backward"] = backward_measurement(peaks, flush, stream)
+    res.update(next_row_measurements(peaks, flush, stream))
     # the q shapes of llama8b_32k (256 MiB) and packed_128k (1 GiB)
     for S_, label in ((32768, "permute_256MiB"), (131072, "permute_1GiB")):
         x = torch.randn((1, S_, 32, 128), device="cuda").to(torch.bfloat16)
@@ -442,6 +443,73 @@ def extra_measurements(args, peaks):
         res[label] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
                       "shape": f"[1][{S_}][32][128] bf16, P=8"}
         del x, y
+    return res
+
+
+def _median_ms(call, flush, stream, reps):
+    import torch
+    for _ in range(3):
+        call()
+    ms = []
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        ms.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median([a.elapsed_time(b) for a, b in ms])
+
+
+def next_row_measurements(peaks, flush, stream):
+    """The permutation-free Ulysses path (attention run directly on the
+    sequence-sharded ulysses_4k tensors: every head group in place, output
+    already in sequence-sharded layout) and the Ulysses + Ring hybrid on
+    halfmil_512k (P_u = 8 head groups x P_r = 2 striped ring blocks), timed
+    like the rest (events, L2 flushed, median of reps)."""
+    import torch
+
+    import sequence_parallelism_gb300 as sp
+    from sequence_parallelism_gb300 import _lib, workloads
+
+    res = {}
+    cfg = workloads.CONFIGS["ulysses_4k"]
+    B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
+    q, k, v = workloads.qkv_torch(B, S, Hq, Hkv, d, cfg["seed"], torch.bfloat16, "cuda")
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    ws = sp.attention_workspace(B, S, False)
+    t = _median_ms(lambda: _lib.sp_blockwise_attn_fwd(q, k, v, None, P, "contiguous", 0.0, out,
+                                                       lse, ws), flush, stream, 50)
+    fl = attention_flops(cfg, None)
+    tf = fl / (t * 1e-3) / 1e12
+    res["ulysses_4k_fused"] = {
+        "ms": round(t, 4), "TFLOP/s": round(tf, 1),
+        "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4), "flops": fl,
+        "note": "attention on the sequence-sharded tensors, no permutation launches"}
+    del q, k, v, out, lse, ws
+    cfg = workloads.CONFIGS["halfmil_512k"]
+    B, S, Hq, Hkv, d = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d"))
+    P_u, P_r = 8, 2
+    q, k, v = workloads.qkv_torch(B, S, Hq, Hkv, d, cfg["seed"], torch.bfloat16, "cuda")
+    pos_np = workloads.position_ids(cfg)
+    pos = torch.from_numpy(pos_np).cuda()
+    out = torch.empty_like(q)
+    lse = torch.empty((P_u, B, Hq // P_u, S), dtype=torch.float32, device="cuda")
+    ws = torch.empty(_lib.sp_ulysses_ring_attn_workspace_bytes(B, S, Hq, Hkv, d, True,
+                                                               _lib._dtype(q)),
+                     dtype=torch.uint8, device="cuda")
+    t = _median_ms(lambda: _lib.sp_ulysses_ring_attn_fwd(q, k, v, pos, P_u, P_r, "striped", 0.0,
+                                                          out, lse, ws), flush, stream, 3)
+    fl = attention_flops(cfg, pos_np)
+    tf = fl / (t * 1e-3) / 1e12
+    res["halfmil_512k_hybrid_8x2"] = {
+        "ms": round(t, 2), "TFLOP/s": round(tf, 1),
+        "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4), "flops": fl,
+        "note": "seq->head with 8 groups, striped ring attention over 2 blocks per group, "
+                "head->seq; one call"}
+    del q, k, v, out, lse, ws
     return res
 
 
