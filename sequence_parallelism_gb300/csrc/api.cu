@@ -142,6 +142,7 @@ extern "C" sp_status sp_blockwise_attn_fwd(const void* q, const void* k, const v
                                            float scale, sp_dtype dtype, void* out, float* lse,
                                            void* workspace, size_t workspace_bytes,
                                            sp_stream_t stream) {
+  sp::NvtxRange nvtx_range("sp_blockwise_attn_fwd");
   return sp::attn(q, k, v, position_ids, B, B, S, Hq, Hkv, d, P, order, 0, P, scale, dtype, out,
                   lse, workspace, workspace_bytes, stream);
 }
@@ -152,6 +153,7 @@ extern "C" sp_status sp_blockwise_attn_step(const void* q, const void* k, const 
                                             float scale, sp_dtype dtype, void* out, float* lse,
                                             void* workspace, size_t workspace_bytes,
                                             sp_stream_t stream) {
+  sp::NvtxRange nvtx_range("sp_blockwise_attn_step");
   sp::g_last_launches = 0;
   if (step < 0 || step >= P) return SP_ERR_INVALID_ARG;
   return sp::attn(q, k, v, position_ids, B, B, S, Hq, Hkv, d, P, order, step, step + 1, scale,

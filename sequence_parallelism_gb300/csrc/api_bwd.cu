@@ -54,6 +54,7 @@ extern "C" sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const v
                                            float scale, sp_dtype dtype, void* dq, void* dk,
                                            void* dv, void* workspace, size_t workspace_bytes,
                                            sp_stream_t stream) {
+  sp::NvtxRange nvtx_range("sp_blockwise_attn_bwd");
   sp::g_last_launches = 0;
   if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return SP_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || d < 1 || P < 1) return SP_ERR_INVALID_ARG;

@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "sp_gb300.h"
 
@@ -22,6 +23,16 @@ inline bool aligned(const void* p, size_t a) {
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 inline size_t dtype_size(sp_dtype t) { return t == SP_BF16 ? 2 : (t == SP_F32 ? 4 : 0); }
+
+// NVTX range around an entry point, named after it, so that a timeline
+// (Nsight Systems) shows each library call; without an attached tool a push
+// or pop is a test of a null function pointer.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 inline sp_status launch_status() {
   return cudaPeekAtLastError() == cudaSuccess ? SP_OK : SP_ERR_CUDA;

@@ -34,6 +34,7 @@ __global__ void barrier_timeout_kernel(int* err, unsigned long long timeout_ns) 
 
 extern "C" sp_status sp_check_barrier_timeout(void* workspace, int timeout_us,
                                               sp_stream_t stream) {
+  sp::NvtxRange nvtx_range("sp_check_barrier_timeout");
   sp::g_last_launches = 0;
   if (!workspace || !sp::aligned(workspace, 256)) return SP_ERR_WORKSPACE;
   if (timeout_us < 1 || timeout_us > 1000000) return SP_ERR_INVALID_ARG;

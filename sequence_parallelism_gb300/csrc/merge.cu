@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const T* __restrict__ outs,
 extern "C" sp_status sp_attn_merge_partials(const void* outs, const float* lses, int P, int B,
                                             int S, int H, int d, sp_dtype dtype, void* out,
                                             float* lse, sp_stream_t stream) {
+  sp::NvtxRange nvtx_range("sp_attn_merge_partials");
   sp::g_last_launches = 0;
   if (!outs || !lses || !out) return SP_ERR_INVALID_ARG;
   if (P < 1 || B < 1 || S < 1 || H < 1 || d < 1) return SP_ERR_INVALID_ARG;

@@ -64,6 +64,7 @@ extern "C" sp_status sp_blockwise_attn_fwd_noalloc(const void* q, const void* k,
                                                    sp_block_order order, float scale,
                                                    sp_dtype dtype, void* out, float* lse,
                                                    sp_stream_t stream) {
+  sp::NvtxRange nvtx_range("sp_blockwise_attn_fwd_noalloc");
   sp::g_last_launches = 0;
   if (B < 1 || S < 1) return SP_ERR_INVALID_ARG;
   const size_t need = sp_blockwise_attn_workspace_bytes(B, S, position_ids != nullptr);

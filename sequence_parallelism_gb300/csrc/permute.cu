@@ -164,11 +164,13 @@ sp_status permute(const void* src, void* dst, int B, int S, int H, int d, int P,
 
 extern "C" sp_status sp_ulysses_seq_to_head(const void* x, void* y, int B, int S, int H, int d,
                                             int P, sp_dtype dtype, sp_stream_t stream) {
+  sp::NvtxRange nvtx_range("sp_ulysses_seq_to_head");
   return sp::permute(x, y, B, S, H, d, P, dtype, stream, true);
 }
 
 extern "C" sp_status sp_ulysses_head_to_seq(const void* y, void* x, int B, int S, int H, int d,
                                             int P, sp_dtype dtype, sp_stream_t stream) {
+  sp::NvtxRange nvtx_range("sp_ulysses_head_to_seq");
   return sp::permute(y, x, B, S, H, d, P, dtype, stream, false);
 }
 
@@ -176,6 +178,7 @@ extern "C" sp_status sp_ulysses_seq_to_head_qkv(const void* q, const void* k, co
                                                 void* yq, void* yk, void* yv, int B, int S, int Hq,
                                                 int Hkv, int d, int P, sp_dtype dtype,
                                                 sp_stream_t stream) {
+  sp::NvtxRange nvtx_range("sp_ulysses_seq_to_head_qkv");
   const void* src[3] = {q, k, v};
   void* dst[3] = {yq, yk, yv};
   const int H[3] = {Hq, Hkv, Hkv};

@@ -124,6 +124,7 @@ extern "C" size_t sp_segment_starts_workspace_bytes(int B, int S) {
 extern "C" sp_status sp_segment_starts(const int32_t* position_ids, int32_t* doc_start, int B,
                                        int S, void* workspace, size_t workspace_bytes,
                                        sp_stream_t stream) {
+  sp::NvtxRange nvtx_range("sp_segment_starts");
   sp::g_last_launches = 0;
   if (!position_ids || !doc_start || B < 1 || S < 1) return SP_ERR_INVALID_ARG;
   if (B > 65535) return SP_ERR_UNSUPPORTED;

@@ -45,6 +45,7 @@ extern "C" sp_status sp_ulysses_ring_attn_fwd(const void* q, const void* k, cons
                                               sp_block_order order, float scale, sp_dtype dtype,
                                               void* out, float* lse, void* workspace,
                                               size_t workspace_bytes, sp_stream_t stream) {
+  sp::NvtxRange nvtx_range("sp_ulysses_ring_attn_fwd");
   sp::g_last_launches = 0;
   if (!q || !k || !v || !out) return SP_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || d < 1 || P_u < 1 || P_r < 1)
