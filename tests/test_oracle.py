@@ -365,6 +365,23 @@ def test_permutation_elementwise_tiny():
                         assert y[r, b, t, hl, c] == x[b, t, r * G + hl, c]
 
 
+def test_block_tokens_partition():
+    """Both block orders cut the tokens 0..S-1 into P blocks of S/P tokens:
+    contiguous block p is [p*S/P, (p+1)*S/P) (GPU i holds [i*n/P,
+    (i+1)*n/P) on the Ulysses pages); striped block p is {t : t mod P = p}
+    (tokens spread uniformly, stripe width 1)."""
+    S, P = 24, 4
+    for order in ("contiguous", "striped"):
+        blocks = [oracle.block_tokens(S, P, p, order) for p in range(P)]
+        assert sorted(np.concatenate(blocks).tolist()) == list(range(S))
+        assert all(len(b) == S // P for b in blocks)
+        assert all(np.all(np.diff(b) > 0) for b in blocks)  # natural order inside a block
+    assert oracle.block_tokens(S, P, 1, "contiguous").tolist() == list(range(6, 12))
+    assert oracle.block_tokens(S, P, 1, "striped").tolist() == [1, 5, 9, 13, 17, 21]
+    with pytest.raises(ValueError):
+        oracle.block_tokens(10, 4, 0, "striped")
+
+
 def test_permutation_rejects_indivisible():
     with pytest.raises(ValueError):
         oracle.seq_to_head(np.zeros((1, 4, 6, 2)), 4)
