@@ -169,7 +169,8 @@ def run_ours(args, rank, world, local_rank):
     import torch
 
     import sequence_parallelism_gb300 as sp
-    from sequence_parallelism_gb300 import _lib, workloads
+    import workloads
+    from sequence_parallelism_gb300 import _lib
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -387,7 +388,8 @@ def extra_measurements(args, peaks):
     import torch
 
     import sequence_parallelism_gb300 as sp
-    from sequence_parallelism_gb300 import _lib, workloads
+    import workloads
+    from sequence_parallelism_gb300 import _lib
 
     res = {}
     stream = torch.cuda.current_stream()
@@ -471,7 +473,8 @@ def next_row_measurements(peaks, flush, stream):
     import torch
 
     import sequence_parallelism_gb300 as sp
-    from sequence_parallelism_gb300 import _lib, workloads
+    import workloads
+    from sequence_parallelism_gb300 import _lib
 
     res = {}
     cfg = workloads.CONFIGS["ulysses_4k"]
@@ -520,7 +523,8 @@ def backward_measurement(peaks, flush, stream, reps=20):
     import torch
 
     import sequence_parallelism_gb300 as sp
-    from sequence_parallelism_gb300 import _lib, workloads
+    import workloads
+    from sequence_parallelism_gb300 import _lib
 
     cfg = workloads.CONFIGS["llama8b_32k"]
     B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
@@ -560,7 +564,7 @@ def backward_measurement(peaks, flush, stream, reps=20):
 
 # ------------------------------------------------------- CPU oracle leg
 def _oracle_inputs(cfg):
-    from sequence_parallelism_gb300 import workloads
+    import workloads
     B, S, Hq, Hkv, d = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d"))
     rng = np.random.default_rng(cfg["seed"])
     q = rng.standard_normal((B, S, Hq, d)).astype(np.float32)
@@ -573,7 +577,7 @@ def _oracle_sample(cfg, order, rows, inputs):
     """One bounded sample of the workload through the oracle (inputs drawn
     beforehand); returns (algorithmic FLOPs done, seconds)."""
     import oracle
-    from sequence_parallelism_gb300 import workloads
+    import workloads
 
     B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
     q, k, v, pos = inputs
@@ -631,7 +635,7 @@ def run_reference(args, rank, world):
     sample of the workload, sized so K + W steps take about two minutes."""
     if rank != 0:
         return None
-    from sequence_parallelism_gb300 import workloads
+    import workloads
     cfg = dict(workloads.CONFIGS[args.workload])
     order = cfg["orders"][-1] if args.order is None else args.order
     inputs = _oracle_inputs(cfg)

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from helpers import BF16_MAX_ABS, F32_MAX_ABS, check_attention, np32, torch_dtype
-from sequence_parallelism_gb300 import workloads
+import workloads
 
 pytestmark = pytest.mark.gpu
 

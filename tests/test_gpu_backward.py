@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from helpers import check_grad, np32
-from sequence_parallelism_gb300 import workloads
+import workloads
 from test_gpu_attention import _positions
 
 pytestmark = pytest.mark.gpu

@@ -17,7 +17,7 @@ import torch
 
 import oracle
 from helpers import check_grad, np32
-from sequence_parallelism_gb300 import workloads
+import workloads
 
 pytestmark = pytest.mark.gpu
 

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from helpers import check_attention, np32
-from sequence_parallelism_gb300 import workloads
+import workloads
 
 pytestmark = pytest.mark.gpu
 

@@ -14,7 +14,8 @@ import torch
 
 import oracle
 from helpers import BF16_MAX_ABS, F32_MAX_ABS, check_attention, check_grad, np32
-from sequence_parallelism_gb300 import _lib, workloads
+import workloads
+from sequence_parallelism_gb300 import _lib
 from test_gpu_attention import _positions
 
 pytestmark = pytest.mark.gpu

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from helpers import npi
-from sequence_parallelism_gb300 import workloads
+import workloads
 
 pytestmark = pytest.mark.gpu
 

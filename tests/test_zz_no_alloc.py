@@ -17,7 +17,7 @@ import pytest
 import torch
 
 from helpers import BF16_MAX_ABS, BF16_MEAN_ABS, F32_MAX_ABS, LSE_BF16, np32
-from sequence_parallelism_gb300 import workloads
+import workloads
 
 pytestmark = pytest.mark.gpu
 

@@ -2,7 +2,9 @@
 
 Input generation only -- nothing here computes attention or a permutation.
 Tests and bench.py draw the inputs from here, so the CUDA path and the CPU
-oracle always see the same numbers.
+oracle always see the same numbers.  The module stands apart from both the
+library package and oracle/: importing it loads neither the CUDA library nor
+the oracle (torch is imported only by the functions that draw on a device).
 
 The five workloads (q, k, v ~ N(0, 1), then rounded to the storage dtype):
   ring_tiny     P=4 blocks x 8 tokens, d=16, 1 head, fp32, non-causal; the Ring
@@ -25,7 +27,7 @@ import os
 
 import numpy as np
 
-_ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+_ROOT = os.path.dirname(os.path.abspath(__file__))
 GOLDEN_RING_TINY = os.path.join(_ROOT, "tests", "golden", "ring_tiny_seed0.json")
 
 CONFIGS = {
