@@ -1,14 +1,16 @@
-"""Benchmark of the hot path: Ulysses permutation + blockwise ring attention.
+"""Benchmark of the hot path: blockwise ring attention + Ulysses permutation.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
 One step = one pass of the whole path over one batch of synthetic input.
-For the default workload (ulysses_4k: B=1, S=4096, H=32, d=128, P=4, bf16):
-    seq_to_head(q), seq_to_head(k), seq_to_head(v)      Ulysses all-to-all #1
+The default workload is the causal Llama-3.1-8B-shaped attention the metric
+names (llama8b_32k: B=1, S=32768, Hq=32, Hkv=8, d=128, P=8 contiguous ring
+blocks, position_ids 0..S-1, bf16): a step is the doc_start scan of
+position_ids plus causal blockwise attention (one library call).  The
+ulysses_4k workload (--workload ulysses_4k) times the Ulysses layer instead:
+    seq_to_head(q, k, v)                                 Ulysses all-to-all #1
     blockwise attention, batch P*B, H/P heads, P ring blocks (online merge)
     head_to_seq(out)                                     Ulysses all-to-all #2
-For the causal workloads (llama8b_32k, packed_128k, halfmil_512k) a step is
-doc_start from position_ids + causal blockwise attention.
 
 Reported value: attention TFLOP/s over the whole step (algorithmic FLOPs:
 4*d per allowed (query, key) pair per query head), aggregated over ranks.
@@ -16,10 +18,14 @@ L2 (129 MB) is flushed between timed steps, outside the timed events, by
 writing a 512 MiB buffer and then reading another 512 MiB buffer: the read
 evicts the dirty lines the write leaves behind, so that their write-back does
 not land in the next timed kernel (the flush leaves L2 cold and clean).
-The JSON line also carries the dominant kernel's roofline, the
-permutation's bandwidth, the causal Llama-3.1-8B-shaped attention rate, an
-end-to-end number with host buffers, the CPU oracle baseline, and the SM
-clocks sampled during the timed region.
+The JSON line also carries the attention kernel's roofline, an end-to-end
+number with host buffers, the CPU oracle baseline and the SM clocks sampled
+during the timed region; under "extra", each other timed workload with its
+own roofline fraction and clock record: the Ulysses layer of ulysses_4k
+(with the permutation's bandwidth in both directions, also reported under
+"permute"), packed_128k in both block orders, halfmil_512k striped, the
+llama8b_32k backward, the fused Ulysses path, the Ulysses + Ring hybrid and
+two large permutations.
 
 Multi-GPU: every rank runs its own independent replica of the step (the
 head groups / batches of the path are independent; no collective on the data
@@ -42,10 +48,35 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("causal blockwise-attention TFLOP/s (% BF16 peak); seq↔head permute GB/s")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant
-# kernel from the committed ncu capture (profiles/attn_bf16_kernel.md; None
-# for workloads not captured at their own size).
-NCU_TRAFFIC_BYTES = {"ulysses_4k": 233173760}  # ncu dram read + write bytes per launch
+DEFAULT_WORKLOAD = "llama8b_32k"
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the attention
+# kernel, recorded from an ncu capture together with a SHA-256 of the kernel's
+# sources at capture time; reported only while the sources still match.
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "dram_traffic.json")
+KERNEL_SOURCES = ("attn_bf16.cu", "attn_common.cuh", "ptx.cuh", "common.cuh")
+
+
+def kernel_sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "sequence_parallelism_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload):
+    """(bytes per launch or None, note)."""
+    try:
+        with open(TRAFFIC_RECORD) as f:
+            rec = json.load(f)["attn_bf16_kernel"].get(workload)
+    except (OSError, ValueError, KeyError):
+        return None, "no capture recorded"
+    if rec is None:
+        return None, "no capture recorded for this workload"
+    if rec.get("sources_sha256") != kernel_sources_sha256():
+        return None, "kernel sources changed since the capture"
+    return rec["bytes_per_launch"], rec.get("note", "ncu capture of the current sources")
 
 
 def load_peaks():
@@ -165,6 +196,17 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ our arm
+def _attn_roofline(flops, ms, peaks, peak_kind, workload):
+    achieved = flops / (ms * 1e-3) / 1e12
+    traffic, note = recorded_traffic(workload)
+    return {"kernel": "attn_bf16_kernel", "bound": "tensor", "achieved": round(achieved, 1),
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(achieved / peaks["bf16_tflops"], 4),
+            "peak_source": f"{peak_kind} bf16 dense (burst)",
+            "traffic": traffic, "traffic_note": note,
+            "algorithmic_flops_per_launch": flops}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -197,7 +239,7 @@ def run_ours(args, rank, world, local_rank):
         perm_bytes = 2.0 * 3 * q.numel() * 2  # read + write of q, k, v
         inv_bytes = 2.0 * q.numel() * 2
 
-        def enqueue(qq, kk, vv, oo, ev=None):
+        def enqueue(qq, kk, vv, pp, oo, ev=None):
             n = 0
             if ev:
                 ev[0].record(stream)
@@ -222,11 +264,11 @@ def run_ours(args, rank, world, local_rank):
         ws = sp.attention_workspace(B, S, pos is not None, dev)
         perm_bytes = inv_bytes = 0.0
 
-        def enqueue(qq, kk, vv, oo, ev=None):
+        def enqueue(qq, kk, vv, pp, oo, ev=None):
             if ev:
                 ev[0].record(stream)
                 ev[1].record(stream)
-            _lib.sp_blockwise_attn_fwd(qq, kk, vv, pos, P, order, 0.0, oo, lse, ws)
+            _lib.sp_blockwise_attn_fwd(qq, kk, vv, pp, P, order, 0.0, oo, lse, ws)
             n = _lib.sp_last_launch_count()
             if ev:
                 ev[2].record(stream)
@@ -234,7 +276,7 @@ def run_ours(args, rank, world, local_rank):
             return n
 
     def step(ev=None):
-        return enqueue(q, k, v, out, ev)
+        return enqueue(q, k, v, pos, out, ev)
 
     flush = L2Flush(dev)
 
@@ -278,14 +320,9 @@ def run_ours(args, rank, world, local_rank):
     value = job_tflops(flops, world, args.steps, tot_ms)
 
     peaks, peak_kind = load_peaks()
-    attn_mean = statistics.mean(attn_ms)
-    achieved = flops / (attn_mean * 1e-3) / 1e12
-    roofline = {"kernel": "attn_bf16_kernel", "bound": "tensor", "achieved": round(achieved, 1),
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["bf16_tflops"], 4),
-                "peak_source": f"{peak_kind} bf16 dense (burst)",
-                "traffic": NCU_TRAFFIC_BYTES.get(args.workload),
-                "algorithmic_flops_per_launch": flops}
+    roofline = _attn_roofline(flops, statistics.mean(attn_ms), peaks, peak_kind, args.workload)
+    roofline["timed_segment"] = ("the library call: doc_start scan + attention kernel" if pos
+                                 is not None else "the attention call (kernel + tail-split merge)")
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -300,33 +337,46 @@ def run_ours(args, rank, world, local_rank):
         "wall_s_timed_region": round(wall, 3),
     }
     if ulysses:
-        perm_mean = statistics.mean(perm_ms)
-        gbs = perm_bytes / (perm_mean * 1e-3) / 1e9
-        inv_gbs = inv_bytes / (statistics.mean(inv_ms) * 1e-3) / 1e9
-        result["permute"] = {
-            "kernel": "permute_kernel (seq_to_head of q,k,v in one launch; head_to_seq)",
-            "bound": "hbm",
-            "seq_to_head_GBps": round(gbs, 1), "head_to_seq_GBps": round(inv_gbs, 1),
-            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-            "bytes_per_step": perm_bytes + inv_bytes,
-            "note": "L2 flushed before each step; 32 MiB tensors"}
-    result["e2e"] = e2e(args, inputs=(q, k, v), out=out, enqueue=enqueue, flops=flops,
+        result["permute"] = permute_summary(perm_bytes / (statistics.mean(perm_ms) * 1e-3) / 1e9,
+                                            inv_bytes / (statistics.mean(inv_ms) * 1e-3) / 1e9,
+                                            peaks)
+    result["e2e"] = e2e(args, inputs=(q, k, v, pos), out=out, enqueue=enqueue, flops=flops,
                         world=world, dev=dev)
     if not args.skip_extra and rank == 0 and world == 1:
-        result["extra"] = extra_measurements(args, peaks)
+        del q, k, v, out
+        if ulysses:
+            del yq, yk, yv, yo
+        result["extra"] = extra_measurements(args, peaks, peak_kind, flush)
+        if "permute" not in result and "ulysses_4k_layer" in result["extra"]:
+            result["permute"] = result["extra"]["ulysses_4k_layer"]["permute"]
     if rank == 0 and world == 1 and not args.skip_cpu:
         result["cpu_baseline"] = cpu_baseline(cfg, args.workload, order, budget_s=args.cpu_budget)
     return result
 
 
+def permute_summary(s2h_gbs, h2s_gbs, peaks):
+    """Both directions of the Ulysses permutation against measured HBM
+    bandwidth; `frac` is the slower direction's."""
+    f1, f2 = s2h_gbs / peaks["hbm_gbs"], h2s_gbs / peaks["hbm_gbs"]
+    return {"kernel": "permute_kernel (seq_to_head of q,k,v in one launch; head_to_seq)",
+            "bound": "hbm", "seq_to_head_GBps": round(s2h_gbs, 1),
+            "head_to_seq_GBps": round(h2s_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac_seq_to_head": round(f1, 4), "frac_head_to_seq": round(f2, 4),
+            "frac": round(min(f1, f2), 4),
+            "note": "ulysses_4k: 3 x 32 MiB seq->head, 32 MiB head->seq; L2 flushed before each "
+                    "step; bytes = read + write"}
+
+
 def e2e(args, inputs, out, enqueue, flops, world, dev):
     """Same step through the public API with host buffers: every step uploads
-    its q, k, v from pinned host memory and downloads its output to pinned
-    host memory, all inside the timed region.  The copies run on their own
-    streams against double-buffered device tensors, so step n+1's upload and
-    step n-1's download overlap step n's kernels (the host link, ~210 GB/s per
-    direction on this machine, is the bound)."""
+    its inputs (q, k, v and, for causal workloads, position_ids) from pinned
+    host memory and downloads its output to pinned host memory, all inside
+    the timed region.  The copies run on their own streams against
+    double-buffered device tensors, so step n+1's upload and step n-1's
+    download overlap step n's kernels (the host link, ~210 GB/s per direction
+    on this machine, is the bound when the kernels are short)."""
     import torch
+    inputs = [t for t in inputs if t is not None]
     comp = torch.cuda.current_stream()
     torch.cuda.synchronize()
     ref = out.cpu()  # the device-timed steps' result on the same inputs
@@ -348,7 +398,8 @@ def e2e(args, inputs, out, enqueue, flops, world, dev):
         ev_in[b].record(s_up)
         comp.wait_event(ev_in[b])
         comp.wait_event(ev_out[b])           # its output buffer has been downloaded
-        enqueue(*bufs_in[b], bufs_out[b])
+        bi = bufs_in[b]
+        enqueue(bi[0], bi[1], bi[2], bi[3] if len(bi) > 3 else None, bufs_out[b])
         ev_done[b].record(comp)
         s_down.wait_event(ev_done[b])
         with torch.cuda.stream(s_down):
@@ -382,76 +433,16 @@ def e2e(args, inputs, out, enqueue, flops, world, dev):
                     "the kernels of the neighbouring steps"}
 
 
-def extra_measurements(args, peaks):
-    """Causal Llama-3.1-8B-shaped attention (llama8b_32k) and a large-tensor
-    permutation, timed the same way (events, L2 flushed between reps)."""
+def _timed(call, flush, stream, reps, warm=3):
+    """Median and list of CUDA-event times (ms) of `call` over reps, L2
+    flushed before each, with the SM clocks sampled meanwhile."""
     import torch
-
-    import sequence_parallelism_gb300 as sp
-    import workloads
-    from sequence_parallelism_gb300 import _lib
-
-    res = {}
-    stream = torch.cuda.current_stream()
-    flush = L2Flush()
-    if args.workload != "llama8b_32k":
-        cfg = workloads.CONFIGS["llama8b_32k"]
-        B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
-        q, k, v = workloads.qkv_torch(B, S, Hq, Hkv, d, cfg["seed"], torch.bfloat16, "cuda")
-        pos_np = workloads.position_ids(cfg)
-        pos = torch.from_numpy(pos_np).cuda()
-        out = torch.empty_like(q)
-        lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
-        ws = sp.attention_workspace(B, S, True)
-        for _ in range(3):
-            _lib.sp_blockwise_attn_fwd(q, k, v, pos, P, "contiguous", 0.0, out, lse, ws)
-        reps = 20
-        ms = []
-        for _ in range(reps):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            _lib.sp_blockwise_attn_fwd(q, k, v, pos, P, "contiguous", 0.0, out, lse, ws)
-            b.record(stream)
-            ms.append((a, b))
-        torch.cuda.synchronize()
-        t = statistics.median([a.elapsed_time(b) for a, b in ms])
-        fl = attention_flops(cfg, pos_np)
-        tf = fl / (t * 1e-3) / 1e12
-        res["llama8b_32k_causal_attention"] = {
-            "ms": round(t, 4), "TFLOP/s": round(tf, 1), "frac_of_bf16_peak": round(
-                tf / peaks["bf16_tflops"], 4), "flops": fl, "reps": reps,
-            "note": "doc_start scan + attention kernel, median of reps"}
-        del q, k, v, out
-    res["llama8b_32k_causal_backward"] = backward_measurement(peaks, flush, stream)
-    res.update(next_row_measurements(peaks, flush, stream))
-    # the q shapes of llama8b_32k (256 MiB) and packed_128k (1 GiB)
-    for S_, label in ((32768, "permute_256MiB"), (131072, "permute_1GiB")):
-        x = torch.randn((1, S_, 32, 128), device="cuda").to(torch.bfloat16)
-        y = torch.empty((8, 1, S_, 4, 128), dtype=torch.bfloat16, device="cuda")
-        for _ in range(3):
-            _lib.sp_ulysses_seq_to_head(x, y, 8)
-        ms = []
-        for _ in range(20):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            _lib.sp_ulysses_seq_to_head(x, y, 8)
-            b.record(stream)
-            ms.append((a, b))
-        torch.cuda.synchronize()
-        t = statistics.median([a.elapsed_time(b) for a, b in ms])
-        gbs = 2.0 * x.numel() * 2 / (t * 1e-3) / 1e9
-        res[label] = {"GB/s": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
-                      "shape": f"[1][{S_}][32][128] bf16, P=8"}
-        del x, y
-    return res
-
-
-def _median_ms(call, flush, stream, reps):
-    import torch
-    for _ in range(3):
+    for _ in range(warm):
         call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.2)
     ms = []
     for _ in range(reps):
         flush()
@@ -461,7 +452,132 @@ def _median_ms(call, flush, stream, reps):
         b.record(stream)
         ms.append((a, b))
     torch.cuda.synchronize()
-    return statistics.median([a.elapsed_time(b) for a, b in ms])
+    clocks = sampler.stop()
+    t = [a.elapsed_time(b) for a, b in ms]
+    return statistics.median(t), t, clocks
+
+
+def causal_attention_measurement(name, order, peaks, peak_kind, flush, stream, reps):
+    """One causal workload's attention call (doc_start scan + kernel), with
+    its roofline fraction and clock record."""
+    import torch
+
+    import sequence_parallelism_gb300 as sp
+    import workloads
+    from sequence_parallelism_gb300 import _lib
+
+    cfg = workloads.CONFIGS[name]
+    B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
+    q, k, v = workloads.qkv_torch(B, S, Hq, Hkv, d, cfg["seed"], torch.bfloat16, "cuda")
+    pos_np = workloads.position_ids(cfg)
+    pos = torch.from_numpy(pos_np).cuda()
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
+    ws = sp.attention_workspace(B, S, True)
+    t, _, clocks = _timed(lambda: _lib.sp_blockwise_attn_fwd(q, k, v, pos, P, order, 0.0, out,
+                                                              lse, ws), flush, stream, reps)
+    st, code = _lib.sp_get_device_error(ws)
+    if st != 0:
+        raise RuntimeError(f"device error word {code:#x} in {name} {order}")
+    fl = attention_flops(cfg, pos_np)
+    rl = _attn_roofline(fl, t, peaks, peak_kind, name)
+    return {"workload": name, "order": order, "P": P, "ms": round(t, 4),
+            "TFLOP/s": rl["achieved"], "frac_of_bf16_peak": rl["frac"], "roofline": rl,
+            "flops": fl, "reps": reps, "clocks": clocks,
+            "note": "doc_start scan + attention kernel, median of reps, L2 flushed"}
+
+
+def ulysses_layer_measurement(peaks, peak_kind, flush, stream, reps=50):
+    """The Ulysses layer of ulysses_4k: seq->head of q, k, v (one launch),
+    attention per head group, head->seq; each segment timed with events."""
+    import torch
+
+    import sequence_parallelism_gb300 as sp
+    import workloads
+    from sequence_parallelism_gb300 import _lib
+
+    cfg = workloads.CONFIGS["ulysses_4k"]
+    B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
+    G = Hq // P
+    q, k, v = workloads.qkv_torch(B, S, Hq, Hkv, d, cfg["seed"], torch.bfloat16, "cuda")
+    yq = torch.empty((P, B, S, G, d), dtype=torch.bfloat16, device="cuda")
+    yk, yv, yo = torch.empty_like(yq), torch.empty_like(yq), torch.empty_like(yq)
+    ylse = torch.empty((P * B, G, S), dtype=torch.float32, device="cuda")
+    out = torch.empty_like(q)
+    ws = sp.attention_workspace(P * B, S, False)
+
+    def layer(ev=None):
+        if ev:
+            ev[0].record(stream)
+        _lib.sp_ulysses_seq_to_head_qkv(q, k, v, yq, yk, yv, P)
+        if ev:
+            ev[1].record(stream)
+        _lib.sp_blockwise_attn_fwd(yq.view(P * B, S, G, d), yk.view(P * B, S, G, d),
+                                   yv.view(P * B, S, G, d), None, P, "contiguous", 0.0,
+                                   yo.view(P * B, S, G, d), ylse, ws)
+        if ev:
+            ev[2].record(stream)
+        _lib.sp_ulysses_head_to_seq(yo, out, P)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(3):
+        layer()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.2)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+    for i in range(reps):
+        flush()
+        layer(evs[i])
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    seg = lambda a, b: statistics.mean([e[a].elapsed_time(e[b]) for e in evs])
+    step, perm, attn, inv = seg(0, 3), seg(0, 1), seg(1, 2), seg(2, 3)
+    fl = attention_flops(cfg, None)
+    rl = _attn_roofline(fl, attn, peaks, peak_kind, "ulysses_4k")
+    perm_gbs = 2.0 * 3 * q.numel() * 2 / (perm * 1e-3) / 1e9
+    inv_gbs = 2.0 * q.numel() * 2 / (inv * 1e-3) / 1e9
+    return {"ms_per_step": round(step, 4), "TFLOP/s_step": round(fl / (step * 1e-3) / 1e12, 1),
+            "attention_ms": round(attn, 4), "frac_of_bf16_peak": rl["frac"], "roofline": rl,
+            "permute": permute_summary(perm_gbs, inv_gbs, peaks), "reps": reps,
+            "clocks": clocks, "note": "mean of reps, L2 flushed before each step"}
+
+
+def extra_measurements(args, peaks, peak_kind, flush):
+    """Every other timed workload, each with its own roofline fraction and
+    clock record (events, L2 flushed between reps)."""
+    import torch
+
+    import workloads
+    from sequence_parallelism_gb300 import _lib
+
+    res = {}
+    stream = torch.cuda.current_stream()
+    if args.workload != "ulysses_4k":
+        res["ulysses_4k_layer"] = ulysses_layer_measurement(peaks, peak_kind, flush, stream)
+    for name, order, reps in (("llama8b_32k", "contiguous", 20), ("packed_128k", "contiguous", 20),
+                              ("packed_128k", "striped", 20), ("halfmil_512k", "striped", 5)):
+        if name == args.workload and order == (args.order or workloads.CONFIGS[name]["orders"][-1]):
+            continue
+        res[f"{name}_{order}"] = causal_attention_measurement(name, order, peaks, peak_kind, flush,
+                                                              stream, reps)
+    res["llama8b_32k_causal_backward"] = backward_measurement(peaks, flush, stream)
+    res.update(next_row_measurements(peaks, flush, stream))
+    # the q shapes of llama8b_32k (256 MiB) and packed_128k (1 GiB)
+    for S_, label in ((32768, "permute_256MiB"), (131072, "permute_1GiB")):
+        x = torch.randn((1, S_, 32, 128), device="cuda").to(torch.bfloat16)
+        y = torch.empty((8, 1, S_, 4, 128), dtype=torch.bfloat16, device="cuda")
+        t1, _, _ = _timed(lambda: _lib.sp_ulysses_seq_to_head(x, y, 8), flush, stream, 20)
+        t2, _, _ = _timed(lambda: _lib.sp_ulysses_head_to_seq(y, x, 8), flush, stream, 20)
+        g1 = 2.0 * x.numel() * 2 / (t1 * 1e-3) / 1e9
+        g2 = 2.0 * x.numel() * 2 / (t2 * 1e-3) / 1e9
+        res[label] = {"seq_to_head_GBps": round(g1, 1), "head_to_seq_GBps": round(g2, 1),
+                      "frac_of_hbm": round(min(g1, g2) / peaks["hbm_gbs"], 4),
+                      "shape": f"[1][{S_}][32][128] bf16, P=8"}
+        del x, y
+    return res
 
 
 def next_row_measurements(peaks, flush, stream):
@@ -483,13 +599,13 @@ def next_row_measurements(peaks, flush, stream):
     out = torch.empty_like(q)
     lse = torch.empty((B, Hq, S), dtype=torch.float32, device="cuda")
     ws = sp.attention_workspace(B, S, False)
-    t = _median_ms(lambda: _lib.sp_blockwise_attn_fwd(q, k, v, None, P, "contiguous", 0.0, out,
-                                                       lse, ws), flush, stream, 50)
+    t, _, clocks = _timed(lambda: _lib.sp_blockwise_attn_fwd(q, k, v, None, P, "contiguous", 0.0,
+                                                              out, lse, ws), flush, stream, 50)
     fl = attention_flops(cfg, None)
     tf = fl / (t * 1e-3) / 1e12
     res["ulysses_4k_fused"] = {
         "ms": round(t, 4), "TFLOP/s": round(tf, 1),
-        "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4), "flops": fl,
+        "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4), "flops": fl, "clocks": clocks,
         "note": "attention on the sequence-sharded tensors, no permutation launches"}
     del q, k, v, out, lse, ws
     cfg = workloads.CONFIGS["halfmil_512k"]
@@ -503,13 +619,14 @@ def next_row_measurements(peaks, flush, stream):
     ws = torch.empty(_lib.sp_ulysses_ring_attn_workspace_bytes(B, S, Hq, Hkv, d, True,
                                                                _lib._dtype(q)),
                      dtype=torch.uint8, device="cuda")
-    t = _median_ms(lambda: _lib.sp_ulysses_ring_attn_fwd(q, k, v, pos, P_u, P_r, "striped", 0.0,
-                                                          out, lse, ws), flush, stream, 3)
+    t, _, clocks = _timed(lambda: _lib.sp_ulysses_ring_attn_fwd(q, k, v, pos, P_u, P_r, "striped",
+                                                                 0.0, out, lse, ws),
+                          flush, stream, 3)
     fl = attention_flops(cfg, pos_np)
     tf = fl / (t * 1e-3) / 1e12
     res["halfmil_512k_hybrid_8x2"] = {
         "ms": round(t, 2), "TFLOP/s": round(tf, 1),
-        "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4), "flops": fl,
+        "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4), "flops": fl, "clocks": clocks,
         "note": "seq->head with 8 groups, striped ring attention over 2 blocks per group, "
                 "head->seq; one call"}
     del q, k, v, out, lse, ws
@@ -540,24 +657,13 @@ def backward_measurement(peaks, flush, stream, reps=20):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     call = lambda: _lib.sp_blockwise_attn_bwd(q, k, v, out, dout, lse, pos, P, "contiguous", 0.0,
                                               dq, dk, dv, ws)
-    for _ in range(3):
-        call()
+    t, _, clocks = _timed(call, flush, stream, reps)
     launches = _lib.sp_last_launch_count()
-    ms = []
-    for _ in range(reps):
-        flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        call()
-        b.record(stream)
-        ms.append((a, b))
-    torch.cuda.synchronize()
-    t = statistics.median([a.elapsed_time(b) for a, b in ms])
     fl = 2.5 * attention_flops(cfg, pos_np)
     tf = fl / (t * 1e-3) / 1e12
     return {"ms": round(t, 4), "TFLOP/s": round(tf, 1),
             "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4), "flops": fl,
-            "reps": reps, "launches_per_call": launches,
+            "reps": reps, "launches_per_call": launches, "clocks": clocks,
             "note": "doc_start scan + prep + dQ + dK/dV kernels, median of reps; "
                     "flops = 2.5 x forward (S, dP, dV, dQ, dK)"}
 
@@ -667,7 +773,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="ulysses_4k")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--order", default=None, choices=[None, "contiguous", "striped"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-extra", action="store_true")

@@ -1,16 +1,25 @@
 """Full-size parity at the benchmark workloads, in the launch configuration
-bench.py times, on seeded sampled query rows that the oracle computes one by
-one (all heads of each sampled row)."""
+bench.py times, against the float64 oracle computed on the host cores
+(tests/fullsize_oracle.py runs it in the background from the session's
+start):
 
-import concurrent.futures
-import os
+  ulysses_4k     every row of every head (4096 x 32), through the permute ->
+                 attention -> permute pipeline;
+  llama8b_32k    every row of every head (32768 x 32);
+  packed_128k    every row of one query head per key/value group (8 of 32
+                 heads, the head's position in its group rotating), and the
+                 seeded sampled rows (both orders' block edges) of every head,
+                 for the contiguous and the striped order;
+  halfmil_512k   the workload's 4096 seeded sampled rows of every head, for the
+                 plain 16-block striped call and the 8 x 2 Ulysses + Ring
+                 hybrid.
+"""
 
 import numpy as np
 import pytest
 import torch
 
-import oracle
-from helpers import check_attention, np32
+from helpers import check_attention
 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -22,32 +31,31 @@ def sp():
     return m
 
 
-def oracle_rows(qn, kn, vn, rows, pos):
-    """oracle.attention_rows split over query heads on a thread pool (numpy
-    releases the GIL inside exp / matmul)."""
-    Hq, Hkv = qn.shape[2], kn.shape[2]
-    g = Hq // Hkv
-
-    def one(h):
-        kv = h // g
-        return oracle.attention_rows(qn[:, :, h:h + 1], kn[:, :, kv:kv + 1], vn[:, :, kv:kv + 1],
-                                     rows, pos)
-
-    workers = min(Hq, os.cpu_count() or 1)
-    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
-        parts = list(ex.map(one, range(Hq)))
-    out = np.concatenate([p[0] for p in parts], axis=2)
-    lse = np.concatenate([p[1] for p in parts], axis=1)
-    return out, lse
-
-
 def _inputs(cfg):
-    q, k, v = workloads.qkv_torch(cfg["B"], cfg["S"], cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["seed"],
-                                  torch.bfloat16, "cuda")
-    return q, k, v
+    return workloads.qkv_torch(cfg["B"], cfg["S"], cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["seed"],
+                               torch.bfloat16, "cuda")
 
 
-def test_ulysses_4k_pipeline(sp):
+def _check(out, lse, result, what):
+    """Compare out [B][S][Hq][d] (device) and lse [B][Hq][S] (device) with an
+    oracle result on its rows and heads, one head at a time; returns the
+    worst (max, mean, lse) over the heads."""
+    rows, heads, ref_out, ref_lse = result
+    trows = torch.from_numpy(rows).to(out.device)
+    worst = [0.0, 0.0, 0.0]
+    for i, h in enumerate(heads):
+        got = out[:, :, h].index_select(1, trows).float().cpu().numpy()
+        got_lse = lse[:, h].index_select(1, trows).cpu().numpy()
+        st = check_attention(got, got_lse, ref_out[:, :, i], ref_lse[:, i], "bf16",
+                             f"{what} head {h}")
+        worst = [max(a, b) for a, b in zip(worst, st)]
+    print(f"PARITY {what}: {len(rows)} rows x {len(heads)} heads "
+          "max=%.3e worst-head-mean=%.3e lse=%.3e" % tuple(worst))
+    return worst
+
+
+@pytest.mark.fullsize_oracle("ulysses_4k")
+def test_ulysses_4k_pipeline_every_row(sp, fullsize_oracle):
     cfg = workloads.CONFIGS["ulysses_4k"]
     B, S, H, d, P = cfg["B"], cfg["S"], cfg["Hq"], cfg["d"], cfg["P"]
     q, k, v = _inputs(cfg)
@@ -56,47 +64,71 @@ def test_ulysses_4k_pipeline(sp):
     yo, ylse = sp.blockwise_attention(yq.view(P * B, S, G, d), yk.view(P * B, S, G, d),
                                       yv.view(P * B, S, G, d), P, "contiguous")
     out = sp.head_to_seq(yo.view(P, B, S, G, d))
-    torch.cuda.synchronize()
-    rows = workloads.sample_rows(S, P, 512, cfg["seed"])
-    ref_out, ref_lse = oracle_rows(np32(q), np32(k), np32(v), rows, None)
     lse = ylse.view(P, B, G, S).permute(1, 0, 2, 3).reshape(B, H, S)
-    stats = check_attention(np32(out)[:, rows], lse.cpu().numpy()[:, :, rows], ref_out, ref_lse,
-                            "bf16", "ulysses_4k")
-    print("PARITY ulysses_4k contiguous max=%.3e mean=%.3e lse=%.3e" % stats)
-
-
-@pytest.mark.parametrize("name,order", [("llama8b_32k", "contiguous"),
-                                        ("packed_128k", "contiguous"),
-                                        ("packed_128k", "striped"),
-                                        ("halfmil_512k", "striped")])
-def test_causal_full_size(sp, name, order):
-    cfg = workloads.CONFIGS[name]
-    q, k, v = _inputs(cfg)
-    pos = workloads.position_ids(cfg)
-    out, lse = sp.blockwise_attention(q, k, v, cfg["P"], order, torch.from_numpy(pos).cuda())
     torch.cuda.synchronize()
-    n = cfg.get("sampled_rows", 256)
-    rows = workloads.sample_rows(cfg["S"], cfg["P"], n, cfg["seed"], order)
-    got_out = np32(out[:, rows])
-    got_lse = lse[:, :, rows].cpu().numpy()
-    del out, lse
-    ref_out, ref_lse = oracle_rows(np32(q), np32(k), np32(v), rows, pos)
-    stats = check_attention(got_out, got_lse, ref_out, ref_lse, "bf16", f"{name} {order}")
-    print(f"PARITY {name} {order} " + "max=%.3e mean=%.3e lse=%.3e" % stats)
+    res = fullsize_oracle.result("ulysses_4k")
+    assert len(res[0]) == S and len(res[1]) == H
+    _check(out, lse, res, "ulysses_4k pipeline")
 
 
-def test_halfmil_ulysses_ring_hybrid(sp):
-    """halfmil_512k has 8 heads for P = 16 devices (Ulysses alone would need
-    16 heads): 8 Ulysses head groups x 2 striped ring blocks."""
+@pytest.mark.fullsize_oracle("llama8b_32k")
+def test_llama8b_32k_every_row(sp, fullsize_oracle):
+    cfg = workloads.CONFIGS["llama8b_32k"]
+    q, k, v = _inputs(cfg)
+    pos = torch.from_numpy(workloads.position_ids(cfg)).cuda()
+    out, lse = sp.blockwise_attention(q, k, v, cfg["P"], "contiguous", pos)
+    torch.cuda.synchronize()
+    del q, k, v
+    res = fullsize_oracle.result("llama8b_32k")
+    assert len(res[0]) == cfg["S"] and len(res[1]) == cfg["Hq"]
+    _check(out, lse, res, "llama8b_32k contiguous")
+
+
+@pytest.mark.fullsize_oracle("packed_128k_heads", "packed_128k_rows")
+@pytest.mark.parametrize("order", ["contiguous", "striped"])
+def test_packed_128k(sp, fullsize_oracle, order):
+    cfg = workloads.CONFIGS["packed_128k"]
+    q, k, v = _inputs(cfg)
+    pos = torch.from_numpy(workloads.position_ids(cfg)).cuda()
+    out, lse = sp.blockwise_attention(q, k, v, cfg["P"], order, pos)
+    torch.cuda.synchronize()
+    del q, k, v
+    heads = fullsize_oracle.result("packed_128k_heads")
+    assert len(heads[0]) == cfg["S"] and len(heads[1]) == cfg["Hkv"]
+    assert sorted(h // (cfg["Hq"] // cfg["Hkv"]) for h in heads[1]) == list(range(cfg["Hkv"]))
+    _check(out, lse, heads, f"packed_128k {order} (every row)")
+    rows = fullsize_oracle.result("packed_128k_rows")
+    assert set(workloads.sample_rows(cfg["S"], cfg["P"], 256, cfg["seed"], order)) <= set(rows[0])
+    _check(out, lse, rows, f"packed_128k {order} (sampled rows)")
+
+
+@pytest.mark.fullsize_oracle("halfmil_512k")
+def test_halfmil_512k_striped(sp, fullsize_oracle):
     cfg = workloads.CONFIGS["halfmil_512k"]
     q, k, v = _inputs(cfg)
-    pos = workloads.position_ids(cfg)
-    out, lse = sp.ulysses_ring_attention(q, k, v, 8, 2, "striped", torch.from_numpy(pos).cuda())
+    pos = torch.from_numpy(workloads.position_ids(cfg)).cuda()
+    out, lse = sp.blockwise_attention(q, k, v, cfg["P"], "striped", pos)
     torch.cuda.synchronize()
-    rows = workloads.sample_rows(cfg["S"], 2, 512, cfg["seed"] + 1, "striped")
-    got_out = np32(out[:, rows])
-    got_lse = lse.permute(1, 0, 2, 3).reshape(1, cfg["Hq"], cfg["S"])[:, :, rows].cpu().numpy()
-    del out, lse
-    ref_out, ref_lse = oracle_rows(np32(q), np32(k), np32(v), rows, pos)
-    stats = check_attention(got_out, got_lse, ref_out, ref_lse, "bf16", "halfmil hybrid 8x2")
-    print("PARITY halfmil_512k hybrid-8x2 max=%.3e mean=%.3e lse=%.3e" % stats)
+    del q, k, v
+    res = fullsize_oracle.result("halfmil_512k")
+    assert len(res[0]) == cfg["sampled_rows"] and len(res[1]) == cfg["Hq"]
+    _check(out, lse, res, "halfmil_512k striped")
+
+
+@pytest.mark.fullsize_oracle("halfmil_512k")
+def test_halfmil_ulysses_ring_hybrid(sp, fullsize_oracle):
+    """halfmil_512k has 8 heads for P = 16 devices (Ulysses alone would need
+    16 heads): 8 Ulysses head groups x 2 striped ring blocks, on the same
+    4096 sampled rows (they include the first and last token of every
+    block of both the 16-block and the 2-block striped partitions)."""
+    cfg = workloads.CONFIGS["halfmil_512k"]
+    S = cfg["S"]
+    q, k, v = _inputs(cfg)
+    pos = torch.from_numpy(workloads.position_ids(cfg)).cuda()
+    out, lse = sp.ulysses_ring_attention(q, k, v, 8, 2, "striped", pos)
+    torch.cuda.synchronize()
+    del q, k, v
+    res = fullsize_oracle.result("halfmil_512k")
+    assert {0, 1, S - 2, S - 1} <= set(res[0].tolist())
+    lse = lse.permute(1, 0, 2, 3).reshape(1, cfg["Hq"], S)
+    _check(out, lse, res, "halfmil_512k hybrid 8x2")
