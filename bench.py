@@ -358,7 +358,8 @@ def permute_summary(s2h_gbs, h2s_gbs, peaks):
     """Both directions of the Ulysses permutation against measured HBM
     bandwidth; `frac` is the slower direction's."""
     f1, f2 = s2h_gbs / peaks["hbm_gbs"], h2s_gbs / peaks["hbm_gbs"]
-    return {"kernel": "permute_kernel (seq_to_head of q,k,v in one launch; head_to_seq)",
+    return {"kernel": "permute_kernel (vector copy; launches reading < 128 MiB): seq_to_head of "
+                      "q,k,v in one launch, head_to_seq of the output",
             "bound": "hbm", "seq_to_head_GBps": round(s2h_gbs, 1),
             "head_to_seq_GBps": round(h2s_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac_seq_to_head": round(f1, 4), "frac_head_to_seq": round(f2, 4),
@@ -573,7 +574,8 @@ def extra_measurements(args, peaks, peak_kind, flush):
         t2, _, _ = _timed(lambda: _lib.sp_ulysses_head_to_seq(y, x, 8), flush, stream, 20)
         g1 = 2.0 * x.numel() * 2 / (t1 * 1e-3) / 1e9
         g2 = 2.0 * x.numel() * 2 / (t2 * 1e-3) / 1e9
-        res[label] = {"seq_to_head_GBps": round(g1, 1), "head_to_seq_GBps": round(g2, 1),
+        res[label] = {"kernel": "permute_bulk_kernel (TMA-staged: launches reading >= 128 MiB)",
+                      "seq_to_head_GBps": round(g1, 1), "head_to_seq_GBps": round(g2, 1),
                       "frac_of_hbm": round(min(g1, g2) / peaks["hbm_gbs"], 4),
                       "shape": f"[1][{S_}][32][128] bf16, P=8"}
         del x, y

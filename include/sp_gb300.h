@@ -100,6 +100,28 @@ sp_status sp_ulysses_seq_to_head(const void* x, void* y, int B, int S, int H, in
 sp_status sp_ulysses_head_to_seq(const void* y, void* x, int B, int S, int H, int d, int P,
                                  sp_dtype dtype, sp_stream_t stream);
 
+/* The permutations have two kernels with the same results: a TMA-staged
+ * copy (chunks gathered and scattered through shared memory by tensor-map
+ * and bulk copies) and a vector copy (16-byte loads and stores by every
+ * thread).  The TMA-staged one runs when a launch reads at least
+ * `min_bytes` (default 128 MiB) and its rules hold (chunks of 256 B .. 8 KiB,
+ * a multiple of 16 B; every pointer 16-byte aligned); below that its longer
+ * request latency costs more than it gains.  Sets the threshold for the
+ * whole process (0: TMA-staged whenever the rules hold) and returns the
+ * previous value.  No counterpart on the pages (a tuning choice). */
+size_t sp_permute_set_bulk_min_bytes(size_t min_bytes);
+
+/* Error word of the TMA-staged permutation kernel (one per GPU, process
+ * wide): that kernel stages chunks through shared memory with bulk copies and
+ * waits on barriers with a bounded wait; a wait that runs out of time (which
+ * does not happen in a correct run) records 1 here and its CTA returns early,
+ * leaving the output undefined.  Writes the word to *code (must not be NULL)
+ * and clears it.  Synchronous (a copy from device memory on the current
+ * device).  Returns SP_OK when the word was 0, SP_ERR_DEVICE_TIMEOUT when it
+ * was set, SP_ERR_CUDA or SP_ERR_INVALID_ARG.  No counterpart on the pages
+ * (they name no failure detection for the kernels). */
+sp_status sp_get_permute_error(int* code);
+
 /* sp_ulysses_seq_to_head for the q, k and v of one layer in a single launch:
  * q [B][S][Hq][d] -> yq [P][B][S][Hq/P][d], k, v [B][S][Hkv][d] ->
  * yk, yv [P][B][S][Hkv/P][d].  Same results and errors as three

@@ -31,7 +31,9 @@ EXPORTS = (
     "sp_ulysses_ring_attn_workspace_bytes", "sp_ulysses_ring_attn_fwd",
     "sp_blockwise_attn_bwd_workspace_bytes", "sp_blockwise_attn_bwd",
     "sp_attn_merge_partials",
-    "sp_get_device_error", "sp_check_barrier_timeout", "sp_last_launch_count",
+    "sp_get_device_error", "sp_get_permute_error", "sp_permute_set_bulk_min_bytes",
+    "sp_check_barrier_timeout",
+    "sp_last_launch_count",
 )
 
 
@@ -69,6 +71,8 @@ def _load():
                                       vp, vp, vp, sz, vp]),
         "sp_attn_merge_partials": (i, [vp, vp, i, i, i, i, i, i, vp, vp, vp]),
         "sp_get_device_error": (i, [vp, ctypes.POINTER(ctypes.c_int), vp]),
+        "sp_get_permute_error": (i, [ctypes.POINTER(ctypes.c_int)]),
+        "sp_permute_set_bulk_min_bytes": (sz, [sz]),
         "sp_check_barrier_timeout": (i, [vp, i, vp]),
         "sp_last_launch_count": (i, []),
     }
@@ -252,6 +256,16 @@ def sp_get_device_error(workspace, stream=None):
     code = ctypes.c_int(0)
     st = _lib.sp_get_device_error(_ptr(workspace), ctypes.byref(code), _stream(stream))
     return st, code.value
+
+
+def sp_get_permute_error():
+    code = ctypes.c_int(0)
+    st = _lib.sp_get_permute_error(ctypes.byref(code))
+    return st, code.value
+
+
+def sp_permute_set_bulk_min_bytes(min_bytes):
+    return int(_lib.sp_permute_set_bulk_min_bytes(int(min_bytes)))
 
 
 def sp_check_barrier_timeout(workspace, timeout_us, stream=None):

@@ -97,9 +97,24 @@ def test_ring_step_writes_stay_inside(sp, order):
                         f"ring step {step} {order}")
 
 
-@pytest.mark.parametrize("dtype,H,d", [("bf16", 12, 128), ("bf16", 6, 40), ("f32", 8, 24)])
-def test_permutation_writes_stay_inside(sp, dtype, H, d):
-    B, S, P = 2, 300, 2 if H == 6 else 4
+@pytest.fixture(params=["tma_staged", "default"])
+def path(request):
+    """Every permutation that meets the bulk-copy rules on the TMA-staged
+    kernel, or the default size threshold (these small ones on the vector
+    kernel)."""
+    prev = _lib.sp_permute_set_bulk_min_bytes(0 if request.param == "tma_staged" else 128 << 20)
+    yield request.param
+    _lib.sp_permute_set_bulk_min_bytes(prev)
+
+
+@pytest.mark.parametrize("dtype,B,S,H,d,P", [
+    ("bf16", 2, 300, 12, 128, 4),   # 768 B chunks, 10 rows per item
+    ("bf16", 1, 292, 12, 128, 4),   # the last item of each head group is partial
+    ("bf16", 2, 300, 6, 40, 2),     # 240 B chunks: vector kernel only
+    ("f32", 2, 300, 8, 24, 4),      # 192 B chunks: vector kernel only
+    ("f32", 1, 260, 8, 64, 4),      # 512 B chunks, partial last item
+])
+def test_permutation_writes_stay_inside(sp, path, dtype, B, S, H, d, P):
     g = torch.Generator(device="cuda")
     g.manual_seed(720 + H)
     x = torch.randn((B, S, H, d), generator=g, device="cuda").to(
@@ -114,7 +129,7 @@ def test_permutation_writes_stay_inside(sp, dtype, H, d):
     assert torch.equal(back.t, x)
 
 
-def test_qkv_permutation_writes_stay_inside():
+def test_qkv_permutation_writes_stay_inside(path):
     B, S, H, d, P = 1, 520, 8, 128, 4
     g = torch.Generator(device="cuda")
     g.manual_seed(730)
