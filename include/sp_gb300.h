@@ -215,6 +215,45 @@ sp_status sp_blockwise_attn_step(const void* q, const void* k, const void* v,
                                  sp_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Per-device forms: what ONE device of a real ring computes from the blocks
+ * it holds ("Ring Attention", "Cómo funciona la atención en anillo": device i
+ * keeps query block i and at step s works on the key/value block
+ * j = (i - s) mod P that the ring has brought it).  The tensors hold single
+ * blocks, rows in block order (row u of block p is token p*S/P + u
+ * contiguous, u*P + p striped):
+ *   q_blk, out_blk: [B][S/P][Hq][d]   query block i and its partial result
+ *   k_blk, v_blk:   [B][S/P][Hkv][d]  key/value block j
+ *   lse_blk:        [B][Hq][S/P] fp32 (may be NULL)
+ * position_ids is the whole sequence's [B][S] (every device holds it: the
+ * mask needs global token indices and document starts; NULL = non-causal).
+ * Rows with no allowed key in block j get out = 0, lse = -inf (merging them
+ * with sp_attn_merge_partials gives them weight 0).  The workspace is the
+ * one sp_blockwise_attn_workspace_bytes(B, S, causal) sizes.  Errors as for
+ * sp_blockwise_attn_fwd, plus SP_ERR_INVALID_ARG unless 0 <= i, j < P.
+ *
+ * sp_ring_block_step: query block i against key/value block j only.
+ * sp_attn_merge_partials over the P steps of device i gives block i's rows
+ * of sp_blockwise_attn_fwd.
+ */
+sp_status sp_ring_block_step(const void* q_blk, const void* k_blk, const void* v_blk,
+                             const int32_t* position_ids, int B, int S, int Hq, int Hkv, int d,
+                             int P, sp_block_order order, int i, int j, float scale,
+                             sp_dtype dtype, void* out_blk, float* lse_blk, void* workspace,
+                             size_t workspace_bytes, sp_stream_t stream);
+
+/* Query block i against the whole sequence, visited in ring order: what a
+ * device computes once K and V have been all-gathered instead of passed
+ * around the ring ("Ulysses序列并行技术详解：ms-swift如何降低长序列显存占用":
+ * K and V reach every rank through all-gathers).  k, v: [B][S][Hkv][d] (the
+ * whole sequence); q_blk, out_blk, lse_blk as above.  Equals block i's rows
+ * of sp_blockwise_attn_fwd. */
+sp_status sp_query_block_attn_fwd(const void* q_blk, const void* k, const void* v,
+                                  const int32_t* position_ids, int B, int S, int Hq, int Hkv,
+                                  int d, int P, sp_block_order order, int i, float scale,
+                                  sp_dtype dtype, void* out_blk, float* lse_blk, void* workspace,
+                                  size_t workspace_bytes, sp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Ulysses + Ring hybrid, for fewer heads than devices.
  *
  * Ulysses needs num_heads >= sp_size ("Ulysses SP: entrenar modelos con

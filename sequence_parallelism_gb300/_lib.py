@@ -28,6 +28,7 @@ EXPORTS = (
     "sp_segment_starts_workspace_bytes", "sp_segment_starts", "sp_blockwise_attn_workspace_bytes",
     "sp_blockwise_attn_split_workspace_bytes",
     "sp_blockwise_attn_fwd", "sp_blockwise_attn_step", "sp_blockwise_attn_fwd_noalloc",
+    "sp_ring_block_step", "sp_query_block_attn_fwd",
     "sp_ulysses_ring_attn_workspace_bytes", "sp_ulysses_ring_attn_fwd",
     "sp_blockwise_attn_bwd_workspace_bytes", "sp_blockwise_attn_bwd",
     "sp_attn_merge_partials",
@@ -63,6 +64,10 @@ def _load():
                                        sz, vp]),
         "sp_blockwise_attn_fwd_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, vp,
                                               vp]),
+        "sp_ring_block_step": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, vp, vp, vp,
+                                   sz, vp]),
+        "sp_query_block_attn_fwd": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp,
+                                        sz, vp]),
         "sp_ulysses_ring_attn_workspace_bytes": (sz, [i, i, i, i, i, i, i]),
         "sp_ulysses_ring_attn_fwd": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp,
                                          sz, vp]),
@@ -206,6 +211,38 @@ def sp_blockwise_attn_step(q, k, v, position_ids, P, order, step, scale, out, ls
         float(scale), _dtype(q), _ptr(out), _ptr(lse), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out, lse
+
+
+def sp_ring_block_step(q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, scale, out_blk,
+                       lse_blk, workspace, stream=None):
+    """One device's ring step: query block i against key/value block j
+    (block tensors [B][S/P][H][d]; position_ids of the whole sequence)."""
+    _dense(q_blk, k_blk, v_blk, position_ids, out_blk, lse_blk, workspace)
+    B, Lb, Hq, d = q_blk.shape
+    Hkv = k_blk.shape[2]
+    if Lb * P != S or k_blk.shape[1] != Lb:
+        raise ValueError("block tensors must hold S/P rows")
+    _check("sp_ring_block_step", _lib.sp_ring_block_step(
+        _ptr(q_blk), _ptr(k_blk), _ptr(v_blk), _ptr(position_ids), B, S, Hq, Hkv, d, P,
+        _ORDERS[order], i, j, float(scale), _dtype(q_blk), _ptr(out_blk), _ptr(lse_blk),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out_blk, lse_blk
+
+
+def sp_query_block_attn_fwd(q_blk, k, v, position_ids, P, order, i, scale, out_blk, lse_blk,
+                            workspace, stream=None):
+    """Query block i (block tensor [B][S/P][Hq][d]) against the whole
+    sequence's k, v ([B][S][Hkv][d]) in ring order."""
+    _dense(q_blk, k, v, position_ids, out_blk, lse_blk, workspace)
+    B, Lb, Hq, d = q_blk.shape
+    S, Hkv = k.shape[1], k.shape[2]
+    if Lb * P != S:
+        raise ValueError("q_blk must hold S/P rows")
+    _check("sp_query_block_attn_fwd", _lib.sp_query_block_attn_fwd(
+        _ptr(q_blk), _ptr(k), _ptr(v), _ptr(position_ids), B, S, Hq, Hkv, d, P, _ORDERS[order],
+        i, float(scale), _dtype(q_blk), _ptr(out_blk), _ptr(lse_blk), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out_blk, lse_blk
 
 
 def sp_ulysses_ring_attn_workspace_bytes(B, S, Hq, Hkv, d, causal, dtype):

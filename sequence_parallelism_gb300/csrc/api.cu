@@ -39,12 +39,19 @@ size_t doc_start_bytes(int B, int S) {
 sp_status attn(const void* q, const void* k, const void* v, const int32_t* position_ids,
                int pos_rows, int B, int S, int Hq, int Hkv, int d, int P, sp_block_order order,
                int step_begin, int step_end, float scale, sp_dtype dtype, void* out, float* lse,
-               void* workspace, size_t workspace_bytes, sp_stream_t stream) {
+               void* workspace, size_t workspace_bytes, sp_stream_t stream, int q_block,
+               int kv_block) {
   g_last_launches = 0;
   if (!q || !k || !v || !out) return SP_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || d < 1 || P < 1) return SP_ERR_INVALID_ARG;
   if (S % P != 0 || Hq % Hkv != 0) return SP_ERR_INVALID_ARG;
   if (order != SP_ORDER_CONTIGUOUS && order != SP_ORDER_STRIPED) return SP_ERR_INVALID_ARG;
+  // per-device form: a single query block, and with it at most one key/value
+  // block, the one the (single) ring step visits
+  if (q_block < -1 || q_block >= P || kv_block < -1 || kv_block >= P) return SP_ERR_INVALID_ARG;
+  if (kv_block >= 0 && (q_block < 0 || step_end != step_begin + 1 ||
+                        ((q_block - step_begin) % P + P) % P != kv_block))
+    return SP_ERR_INVALID_ARG;
   if (dtype != SP_BF16 && dtype != SP_F32) return SP_ERR_INVALID_ARG;
   if (!(scale == scale) || isinf(scale)) return SP_ERR_INVALID_ARG;
   if (dtype == SP_BF16 && d != 128) return SP_ERR_UNSUPPORTED;
@@ -84,6 +91,8 @@ sp_status attn(const void* q, const void* k, const void* v, const int32_t* posit
   a.doc_start = doc_start;
   a.out = out;
   a.lse = lse;
+  a.q_block = q_block;
+  a.kv_block = kv_block;
   a.err = err;
   a.counter = err + 1;
   a.B = B;
@@ -158,6 +167,34 @@ extern "C" sp_status sp_blockwise_attn_step(const void* q, const void* k, const 
   if (step < 0 || step >= P) return SP_ERR_INVALID_ARG;
   return sp::attn(q, k, v, position_ids, B, B, S, Hq, Hkv, d, P, order, step, step + 1, scale,
                   dtype, out, lse, workspace, workspace_bytes, stream);
+}
+
+extern "C" sp_status sp_ring_block_step(const void* q_blk, const void* k_blk, const void* v_blk,
+                                        const int32_t* position_ids, int B, int S, int Hq, int Hkv,
+                                        int d, int P, sp_block_order order, int i, int j,
+                                        float scale, sp_dtype dtype, void* out_blk, float* lse_blk,
+                                        void* workspace, size_t workspace_bytes,
+                                        sp_stream_t stream) {
+  sp::NvtxRange nvtx_range("sp_ring_block_step");
+  sp::g_last_launches = 0;
+  if (P < 1 || i < 0 || i >= P || j < 0 || j >= P) return SP_ERR_INVALID_ARG;
+  const int step = ((i - j) % P + P) % P;
+  return sp::attn(q_blk, k_blk, v_blk, position_ids, B, B, S, Hq, Hkv, d, P, order, step,
+                  step + 1, scale, dtype, out_blk, lse_blk, workspace, workspace_bytes, stream, i,
+                  j);
+}
+
+extern "C" sp_status sp_query_block_attn_fwd(const void* q_blk, const void* k, const void* v,
+                                             const int32_t* position_ids, int B, int S, int Hq,
+                                             int Hkv, int d, int P, sp_block_order order, int i,
+                                             float scale, sp_dtype dtype, void* out_blk,
+                                             float* lse_blk, void* workspace,
+                                             size_t workspace_bytes, sp_stream_t stream) {
+  sp::NvtxRange nvtx_range("sp_query_block_attn_fwd");
+  sp::g_last_launches = 0;
+  if (P < 1 || i < 0 || i >= P) return SP_ERR_INVALID_ARG;
+  return sp::attn(q_blk, k, v, position_ids, B, B, S, Hq, Hkv, d, P, order, 0, P, scale, dtype,
+                  out_blk, lse_blk, workspace, workspace_bytes, stream, i, -1);
 }
 
 extern "C" sp_status sp_get_device_error(void* workspace, int* code, sp_stream_t stream) {

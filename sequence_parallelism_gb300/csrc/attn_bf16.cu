@@ -125,6 +125,7 @@ struct Schedule {
 // Work item of linear index L: heavy query positions first (the causal work
 // of a query block grows with its position), heads innermost so that the
 // query heads sharing a key/value head run side by side.
+// With a fixed query block (per-device form) only that block's items exist.
 __device__ __forceinline__ void item_coords(int L, const AttnArgs& a, int n_pairs, int& b, int& hq,
                                             int& i, int& pair) {
   const int BH = a.B * a.Hq;
@@ -132,8 +133,9 @@ __device__ __forceinline__ void item_coords(int L, const AttnArgs& a, int n_pair
   const int bh = L % BH;
   b = bh / a.Hq;
   hq = bh % a.Hq;
-  const int rev = a.P * n_pairs - 1 - pos;
-  i = rev / n_pairs;
+  const int nqb = a.q_block >= 0 ? 1 : a.P;
+  const int rev = nqb * n_pairs - 1 - pos;
+  i = a.q_block >= 0 ? a.q_block : rev / n_pairs;
   pair = rev % n_pairs;
 }
 
@@ -256,7 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base_s;
   volatile int* abort_flag = &abort_s;
 
-  // coordinates of local row u of block p in the 5-D tensor maps
+  // coordinates of local row u of block p in the 5-D tensor maps; a tensor
+  // that holds a single block (per-device form) is mapped as one contiguous
+  // block
   auto coord_rows = [&](int p, int u, int& c2, int& c3) {
     if (a.order == SP_ORDER_STRIPED) {
       c2 = p;
@@ -264,6 +268,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       c2 = u;
       c3 = p;
+    }
+  };
+  auto coord_q = [&](int p, int u, int& c2, int& c3) {
+    if (a.q_block >= 0) {
+      c2 = u;
+      c3 = 0;
+    } else {
+      coord_rows(p, u, c2, c3);
+    }
+  };
+  auto coord_kv = [&](int p, int u, int& c2, int& c3) {
+    if (a.kv_block >= 0) {
+      c2 = u;
+      c3 = 0;
+    } else {
+      coord_rows(p, u, c2, c3);
     }
   };
 
@@ -297,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(qf, kQTiles * kTileBytes);
           for (int t = 0; t < kQTiles; ++t) {
             int c2, c3;
-            coord_rows(U.i, U.u0 + t * kBM, c2, c3);
+            coord_q(U.i, U.u0 + t * kBM, c2, c3);
             for (int half = 0; half < 2; ++half)
               tma_load_5d(smem_q + t * kTileBytes + half * kHalfBytes, &tm.q, qf, half * 64, U.hq,
                           c2, c3, U.b);
@@ -311,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (ft < U.sch.t_lo) continue;
               if (ft >= U.sch.t_hi) break;
               int c2, c3;
-              coord_rows(j, kt * kBN, c2, c3);
+              coord_kv(j, kt * kBN, c2, c3);
               for (int kv = 0; kv < 2; ++kv, ++n) {
                 const int slot = n % kSlots;
                 const uint32_t parity = ((n / kSlots) & 1) ^ 1;
@@ -632,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stage = smem_stage + t * kStageBytes;
         const bool leader = row == 0;
         int c2, c3;
-        coord_rows(U.i, U.u0 + t * kBM, c2, c3);
+        coord_q(U.i, U.u0 + t * kBM, c2, c3);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (leader) bulk_wait_group_read0();  // the stage's previous store has read it
@@ -657,7 +677,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit_group();
           }
         }
-        if (row_live && a.lse) a.lse[(static_cast<long long>(U.b) * a.Hq + U.hq) * a.S + tq] = row_lse;
+        if (row_live && a.lse) {
+          const bool blk = a.q_block >= 0;  // per-device lse: [B][Hq][S/P]
+          a.lse[(static_cast<long long>(U.b) * a.Hq + U.hq) * (blk ? Lb : a.S) + (blk ? u : tq)] =
+              row_lse;
+        }
       }
       mbar_arrive(smem_u32(&bars.unit_empty[xs]));
     }
@@ -688,7 +712,10 @@ __global__ void __launch_bounds__(256) merge_split_kernel(AttnArgs a, int n_pair
   const int Lb = a.S / a.P;
   const int u = pair * kRowsPerCta + r;
   if (u >= Lb) return;
-  const long long tq = block_token(a.order, a.S, a.P, i, u);
+  // row of out / lse: the token, or the local row of a per-device query block
+  const bool blk = a.q_block >= 0;
+  const long long tq = blk ? u : block_token(a.order, a.S, a.P, i, u);
+  const long long rows = blk ? Lb : a.S;
   float m = -INFINITY;
   for (int p = 0; p < split; ++p)
     m = fmaxf(m, part_lse[(static_cast<long long>(x) * split + p) * kRowsPerCta + r]);
@@ -710,10 +737,10 @@ __global__ void __launch_bounds__(256) merge_split_kernel(AttnArgs a, int n_pair
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-  uint2* orow = reinterpret_cast<uint2*>(out + ((static_cast<long long>(b) * a.S + tq) * a.Hq + hq) * kD);
+  uint2* orow = reinterpret_cast<uint2*>(out + ((static_cast<long long>(b) * rows + tq) * a.Hq + hq) * kD);
   orow[lane] = make_uint2(pack_bf16(acc.x * inv, acc.y * inv), pack_bf16(acc.z * inv, acc.w * inv));
   if (a.lse && lane == 0)
-    a.lse[(static_cast<long long>(b) * a.Hq + hq) * a.S + tq] =
+    a.lse[(static_cast<long long>(b) * a.Hq + hq) * rows + tq] =
         wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
@@ -722,14 +749,20 @@ __global__ void __launch_bounds__(256) merge_split_kernel(AttnArgs a, int n_pair
 
 int launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
   Tmaps tm;
-  if (!tmap::make_map(&tm.q, a.q, a.B, a.S, a.Hq, a.P, a.order) ||
-      !tmap::make_map(&tm.k, a.k, a.B, a.S, a.Hkv, a.P, a.order) ||
-      !tmap::make_map(&tm.v, a.v, a.B, a.S, a.Hkv, a.P, a.order) ||
-      !tmap::make_map(&tm.o, a.out, a.B, a.S, a.Hq, a.P, a.order))
-    return -1;
   const int Lb = a.S / a.P;
+  // a tensor holding a single block is mapped as one contiguous block
+  const bool qb = a.q_block >= 0, kvb = a.kv_block >= 0;
+  if (!tmap::make_map(&tm.q, a.q, a.B, qb ? Lb : a.S, a.Hq, qb ? 1 : a.P,
+                      qb ? SP_ORDER_CONTIGUOUS : a.order) ||
+      !tmap::make_map(&tm.k, a.k, a.B, kvb ? Lb : a.S, a.Hkv, kvb ? 1 : a.P,
+                      kvb ? SP_ORDER_CONTIGUOUS : a.order) ||
+      !tmap::make_map(&tm.v, a.v, a.B, kvb ? Lb : a.S, a.Hkv, kvb ? 1 : a.P,
+                      kvb ? SP_ORDER_CONTIGUOUS : a.order) ||
+      !tmap::make_map(&tm.o, a.out, a.B, qb ? Lb : a.S, a.Hq, qb ? 1 : a.P,
+                      qb ? SP_ORDER_CONTIGUOUS : a.order))
+    return -1;
   const int n_pairs = (Lb + kRowsPerCta - 1) / kRowsPerCta;
-  const long long items = static_cast<long long>(a.B) * a.Hq * a.P * n_pairs;
+  const long long items = static_cast<long long>(a.B) * a.Hq * (qb ? 1 : a.P) * n_pairs;
   const size_t smem = kSmemBytes + 1024;
   if (cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)

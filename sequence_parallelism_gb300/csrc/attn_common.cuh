@@ -10,13 +10,20 @@ namespace sp {
 
 // One blockwise-attention launch.  Ring steps [step_begin, step_end) are
 // visited for every query block i: key/value block j = (i - s) mod P.
+// Per-device form (what one rank of a real ring holds): with q_block >= 0,
+// q and out hold only query block q_block ([B][S/P][Hq][d], rows in block
+// order) and lse is [B][Hq][S/P]; with kv_block >= 0, k and v hold only
+// key/value block kv_block ([B][S/P][Hkv][d]) and the steps visit only that
+// block.  Masks and doc_start stay in global token indices either way.
 struct AttnArgs {
-  const void* q;               // [B][S][Hq][d]
-  const void* k;               // [B][S][Hkv][d]
-  const void* v;               // [B][S][Hkv][d]
+  const void* q;               // [B][S][Hq][d]   ([B][S/P][Hq][d] when q_block >= 0)
+  const void* k;               // [B][S][Hkv][d]  ([B][S/P][Hkv][d] when kv_block >= 0)
+  const void* v;               // [B][S][Hkv][d]  (likewise)
   const int32_t* doc_start;    // [pos_rows][S] or nullptr (non-causal)
-  void* out;                   // [B][S][Hq][d]
-  float* lse;                  // [B][Hq][S] or nullptr
+  void* out;                   // [B][S][Hq][d]   ([B][S/P][Hq][d] when q_block >= 0)
+  float* lse;                  // [B][Hq][S] ([B][Hq][S/P] when q_block >= 0) or nullptr
+  int q_block;                 // -1: every query block
+  int kv_block;                // -1: k and v hold the whole sequence
   int* err;                    // device error word
   int* counter;                // work-unit counter of the persistent kernel (zeroed per call)
   int B, S, Hq, Hkv, d, P;
@@ -65,11 +72,13 @@ constexpr int kBwdRowPad = 128;  // Lbp = S / P rounded up to a multiple of this
 // Validates and runs one blockwise-attention call (doc_start scan when
 // position_ids != NULL, then the f32 or bf16 kernel).  position_ids has
 // pos_rows rows; attention batch b reads row b % pos_rows (pos_rows divides B).
+// q_block / kv_block: the per-device form of AttnArgs (-1: whole sequence).
 // Sets g_last_launches.
 sp_status attn(const void* q, const void* k, const void* v, const int32_t* position_ids,
                int pos_rows, int B, int S, int Hq, int Hkv, int d, int P, sp_block_order order,
                int step_begin, int step_end, float scale, sp_dtype dtype, void* out, float* lse,
-               void* workspace, size_t workspace_bytes, sp_stream_t stream);
+               void* workspace, size_t workspace_bytes, sp_stream_t stream, int q_block = -1,
+               int kv_block = -1);
 
 // Both return the number of kernels launched, or -1 on a CUDA error.
 int launch_attn_f32(const AttnArgs& a, cudaStream_t stream);

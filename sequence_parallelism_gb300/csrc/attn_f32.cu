@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(AttnArgs a, int n
   __shared__ long long hull_lo_s, hull_hi_s;
 
   const int tile = blockIdx.x % ntiles;
-  const int i = blockIdx.x / ntiles;
+  const int i = a.q_block >= 0 ? a.q_block : static_cast<int>(blockIdx.x / ntiles);
   const int h = blockIdx.y;
   const int b = blockIdx.z;
   const int kvh = h / (a.Hq / a.Hkv);
@@ -47,15 +47,21 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(AttnArgs a, int n
   const float* v = static_cast<const float*>(a.v);
   const long long qrow_stride = static_cast<long long>(a.Hq) * d;
   const long long krow_stride = static_cast<long long>(a.Hkv) * d;
-  const long long qbase = static_cast<long long>(b) * a.S * qrow_stride + static_cast<long long>(h) * d;
-  const long long kbase = static_cast<long long>(b) * a.S * krow_stride + static_cast<long long>(kvh) * d;
+  // rows per batch and the row of (block, local row) in q/out and in k/v:
+  // the token, or the local row when the tensor holds a single block
+  const bool qb = a.q_block >= 0, kvb = a.kv_block >= 0;
+  const long long q_rows = qb ? Lb : a.S, kv_rows = kvb ? Lb : a.S;
+  auto q_row = [&](long long u) { return qb ? u : block_token(a.order, a.S, a.P, i, u); };
+  auto kv_row = [&](int jb, long long w) { return kvb ? w : block_token(a.order, a.S, a.P, jb, w); };
+  const long long qbase = static_cast<long long>(b) * q_rows * qrow_stride + static_cast<long long>(h) * d;
+  const long long kbase = static_cast<long long>(b) * kv_rows * krow_stride + static_cast<long long>(kvh) * d;
 
   // resident query rows
   for (int idx = threadIdx.x; idx < kRows * d; idx += blockDim.x) {
     const int r = idx / d, c = idx % d;
     const long long u = static_cast<long long>(tile) * kRows + r;
     float val = 0.f;
-    if (u < Lb) val = q[qbase + block_token(a.order, a.S, a.P, i, u) * qrow_stride + c];
+    if (u < Lb) val = q[qbase + q_row(u) * qrow_stride + c];
     Qs[idx] = val;
   }
   // allowed key-token interval [lo, hi] of each of my rows
@@ -112,7 +118,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(AttnArgs a, int n
         const int r = idx / d, c = idx % d;
         float kv = 0.f, vv = 0.f;
         if (r < wn) {
-          const long long off = kbase + block_token(a.order, a.S, a.P, j, w0 + r) * krow_stride + c;
+          const long long off = kbase + kv_row(j, w0 + r) * krow_stride + c;
           kv = k[off];
           vv = v[off];
         }
@@ -161,10 +167,10 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(AttnArgs a, int n
   for (int rr = 0; rr < kRowsPerWarp; ++rr) {
     if (!live[rr]) continue;
     const long long u = static_cast<long long>(tile) * kRows + warp * kRowsPerWarp + rr;
-    const long long t = block_token(a.order, a.S, a.P, i, u);
+    const long long t = q_row(u);
     const bool any = l[rr] > 0.f;
     const float inv = any ? 1.f / l[rr] : 0.f;
-    float* orow = out + static_cast<long long>(b) * a.S * qrow_stride + t * qrow_stride +
+    float* orow = out + static_cast<long long>(b) * q_rows * qrow_stride + t * qrow_stride +
                   static_cast<long long>(h) * d;
 #pragma unroll
     for (int e = 0; e < kMaxE; ++e) {
@@ -172,7 +178,7 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(AttnArgs a, int n
       if (c < d) orow[c] = o[rr][e] * inv;
     }
     if (a.lse && lane == 0)
-      a.lse[(static_cast<long long>(b) * a.Hq + h) * a.S + t] = any ? m[rr] + logf(l[rr]) : -INFINITY;
+      a.lse[(static_cast<long long>(b) * a.Hq + h) * q_rows + t] = any ? m[rr] + logf(l[rr]) : -INFINITY;
   }
 }
 
@@ -187,7 +193,7 @@ int launch_attn_f32(const AttnArgs& a, cudaStream_t stream) {
   if (cudaFuncSetAttribute(attn_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return -1;
-  dim3 grid(static_cast<unsigned>(ntiles) * a.P, a.Hq, a.B);
+  dim3 grid(static_cast<unsigned>(ntiles) * (a.q_block >= 0 ? 1 : a.P), a.Hq, a.B);
   attn_f32_kernel<<<grid, kWarps * 32, smem, stream>>>(a, ntiles);
   return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }

@@ -1,0 +1,219 @@
+"""The multi-device data plane: ring attention and Ulysses across the ranks of
+a torch.distributed process group, one device per rank.
+
+The pages describe three ways to spread one attention layer over P devices:
+
+* Ring ("Ring Attention", "Cómo funciona la atención en anillo"): device i
+  keeps query block i; at every step it sends the key/value block it holds to
+  device i + 1 and receives one from device i - 1, so at step s it holds block
+  j = (i - s) mod P; the partial results are combined by the cumulative
+  softmax.  ring_attention() below: P - 1 point-to-point exchanges, the next
+  block in flight while the current one is multiplied.
+* Ulysses ("Ulysses SP: entrenar modelos con millones de tokens", "Cómo
+  funciona Ulysses Sequence Parallelism (SP)"; "DeepSpeed-Ulysses",
+  "Method"): an all-to-all turns every device's sequence shard of all heads
+  into the whole sequence of a head group, attention runs per head group, and
+  a second all-to-all turns the result back.  ulysses_attention() below.
+* All-gathered K/V ("Ulysses序列并行技术详解：ms-swift如何降低长序列显存占用"):
+  K and V reach every rank through two all-gathers and each rank attends its
+  own query block against the whole sequence.  allgather_kv_attention() below.
+
+torch.distributed moves the bytes (NCCL between GPUs); every arithmetic step
+runs in the library's kernels through `kernels`, an object with the per-device
+operations (LibraryKernels by default: the C entry points on the current CUDA
+stream).  Remote blocks always land in this device's memory before a kernel
+reads them.  Shapes: B batch rows, S the whole sequence, P = world size, Lb =
+S / P rows per block, block rows in block order (row u of block p is token
+p*Lb + u in the contiguous order, u*P + p in the striped one); position_ids is
+the whole sequence's [B][S] on every rank (O(S) integers: the mask needs
+global token indices).
+"""
+
+import torch
+import torch.distributed as dist
+
+from . import _lib
+
+
+class LibraryKernels:
+    """The per-device operations, on the library's kernels.  Each writes its
+    result into the tensors it is given."""
+
+    def __init__(self):
+        self._ws = {}
+
+    def workspace(self, B, S, causal, device):
+        key = (B, S, bool(causal), str(device))
+        if key not in self._ws:
+            n = _lib.sp_blockwise_attn_split_workspace_bytes(B, S, causal)
+            self._ws[key] = torch.empty(n, dtype=torch.uint8, device=device)
+        return self._ws[key]
+
+    def ring_step(self, q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, out, lse):
+        ws = self.workspace(q_blk.shape[0], S, position_ids is not None, q_blk.device)
+        _lib.sp_ring_block_step(q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, 0.0, out,
+                                lse, ws)
+
+    def merge(self, outs, lses, out, lse):
+        _lib.sp_attn_merge_partials(outs, lses, out, lse)
+
+    def query_block(self, q_blk, k, v, position_ids, P, order, i, out, lse):
+        ws = self.workspace(q_blk.shape[0], k.shape[1], position_ids is not None, q_blk.device)
+        _lib.sp_query_block_attn_fwd(q_blk, k, v, position_ids, P, order, i, 0.0, out, lse, ws)
+
+    def seq_to_head(self, x, y, P):
+        _lib.sp_ulysses_seq_to_head(x, y, P)
+
+    def head_to_seq(self, y, x, P):
+        _lib.sp_ulysses_head_to_seq(y, x, P)
+
+    def attention(self, q, k, v, position_ids, P, order, out, lse):
+        ws = self.workspace(q.shape[0], q.shape[1], position_ids is not None, q.device)
+        _lib.sp_blockwise_attn_fwd(q, k, v, position_ids, P, order, 0.0, out, lse, ws)
+
+
+_DEFAULT = None
+
+
+def _kernels(kernels):
+    global _DEFAULT
+    if kernels is not None:
+        return kernels
+    if _DEFAULT is None:
+        _DEFAULT = LibraryKernels()
+    return _DEFAULT
+
+
+def _lse_dtype(t):
+    """lse is float32 for the library's bf16 and fp32 tensors (float64 data,
+    which only a caller's own kernels can take, keeps float64)."""
+    return torch.float64 if t.dtype == torch.float64 else torch.float32
+
+
+def _world(group):
+    return dist.get_world_size(group), dist.get_rank(group)
+
+
+def _peer(group, r):
+    """Global rank of rank r of `group` (point-to-point ops take global ranks)."""
+    return r if group is None else dist.get_global_rank(group, r)
+
+
+def ring_attention(q_blk, k_blk, v_blk, position_ids, order="contiguous", group=None,
+                   kernels=None):
+    """Ring attention across the group: this rank (i of P) holds query,
+    key and value block i ([B][Lb][H][d]); returns its rows of the exact
+    attention, (out [B][Lb][Hq][d], lse [B][Hq][Lb]).
+
+    Step s: the partial of query block i against the key/value block held,
+    j = (i - s) mod P, is folded into the running result by the log-sum-exp
+    merge; meanwhile the held block goes to rank i + 1 and the next one
+    arrives from rank i - 1 into the second of two buffers.
+    """
+    kn = _kernels(kernels)
+    P, i = _world(group)
+    B, Lb, Hq, d = q_blk.shape
+    S = Lb * P
+    nxt_rank, prv_rank = _peer(group, (i + 1) % P), _peer(group, (i - 1) % P)
+    kv = [(k_blk, v_blk), (torch.empty_like(k_blk), torch.empty_like(v_blk))]
+    # two stacks [2][...]: slot 0 the running result, slot 1 the new partial;
+    # the merge of one stack writes slot 0 of the other
+    outs = [torch.empty((2, B, Lb, Hq, d), dtype=q_blk.dtype, device=q_blk.device)
+            for _ in range(2)]
+    lses = [torch.empty((2, B, Hq, Lb), dtype=_lse_dtype(q_blk), device=q_blk.device)
+            for _ in range(2)]
+    cur = 0
+    for s in range(P):
+        j = (i - s) % P
+        reqs = []
+        if s + 1 < P:
+            ck, cv = kv[s % 2]
+            nk, nv = kv[(s + 1) % 2]
+            reqs = dist.batch_isend_irecv([
+                dist.P2POp(dist.isend, ck, nxt_rank, group),
+                dist.P2POp(dist.isend, cv, nxt_rank, group),
+                dist.P2POp(dist.irecv, nk, prv_rank, group),
+                dist.P2POp(dist.irecv, nv, prv_rank, group)])
+        hk, hv = kv[s % 2]
+        slot = 0 if s == 0 else 1
+        kn.ring_step(q_blk, hk, hv, position_ids, S, P, order, i, j, outs[cur][slot],
+                     lses[cur][slot])
+        if s > 0:
+            kn.merge(outs[cur], lses[cur], outs[1 - cur][0], lses[1 - cur][0])
+            cur = 1 - cur
+        for r in reqs:
+            r.wait()
+    return outs[cur][0], lses[cur][0]
+
+
+def allgather_kv_attention(q_blk, k_blk, v_blk, position_ids, order="contiguous", group=None,
+                           kernels=None):
+    """The all-gathered variant: K and V of every rank are gathered (two
+    all-gathers), then this rank's query block attends the whole sequence.
+    Contiguous order only (the gathered blocks are then the sequence in
+    token order).  Returns (out [B][Lb][Hq][d], lse [B][Hq][Lb])."""
+    if order != "contiguous":
+        raise ValueError("the all-gathered variant takes the contiguous order")
+    kn = _kernels(kernels)
+    P, i = _world(group)
+    B, Lb, Hkv, d = k_blk.shape
+    S = Lb * P
+    k = torch.empty((B, S, Hkv, d), dtype=k_blk.dtype, device=k_blk.device)
+    v = torch.empty_like(k)
+    for b in range(B):  # [P][Lb] of batch row b is its whole sequence
+        dist.all_gather_into_tensor(k[b], k_blk[b].contiguous(), group=group)
+        dist.all_gather_into_tensor(v[b], v_blk[b].contiguous(), group=group)
+    out = torch.empty_like(q_blk)
+    lse = torch.empty((B, q_blk.shape[2], Lb), dtype=_lse_dtype(q_blk), device=q_blk.device)
+    kn.query_block(q_blk, k, v, position_ids, P, order, i, out, lse)
+    return out, lse
+
+
+def ulysses_attention(q, k, v, position_ids=None, ring_blocks=1, order="contiguous", group=None,
+                      kernels=None):
+    """One Ulysses attention layer across the group: this rank holds the
+    sequence shard r (tokens [r*S/P, (r+1)*S/P)) of every head, q
+    [B][S/P][Hq][d], k/v [B][S/P][Hkv][d]; returns its shard of the output
+    [B][S/P][Hq][d].
+
+    seq->head on the shard gives P head-group slices; the first all-to-all
+    sends slice g to rank g, so this rank holds head group r for the whole
+    sequence; attention (ring_blocks blocks, `order`) runs on it; the result
+    is cut into P sequence shards and the second all-to-all sends shard p back
+    to rank p, where head->seq restores [S/P][H].
+    """
+    kn = _kernels(kernels)
+    P, r = _world(group)
+    B, Sl, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if Hq % P or Hkv % P:
+        raise ValueError("Ulysses needs the head counts divisible by the group size")
+    S = Sl * P
+    G, Gk = Hq // P, Hkv // P
+    groups = []
+    for t, gh in ((q, G), (k, Gk), (v, Gk)):
+        y = torch.empty((P, B, Sl, gh, d), dtype=t.dtype, device=t.device)
+        kn.seq_to_head(t, y, P)
+        groups.append(y)
+    # first all-to-all, one batch row at a time: recv[p] = rank p's tokens
+    full = []
+    for y, gh in zip(groups, (G, Gk, Gk)):
+        f = torch.empty((B, S, gh, d), dtype=y.dtype, device=y.device)
+        for b in range(B):
+            dist.all_to_all_single(f[b].view(P, Sl, gh, d), y[:, b].contiguous(), group=group)
+        full.append(f)
+    out_g = torch.empty_like(full[0])
+    lse_g = torch.empty((B, G, S), dtype=_lse_dtype(q), device=q.device)
+    kn.attention(full[0], full[1], full[2], position_ids, ring_blocks, order, out_g, lse_g)
+    # second all-to-all: sequence shard p of this head group goes to rank p
+    back = torch.empty((P, B, Sl, G, d), dtype=q.dtype, device=q.device)
+    for b in range(B):
+        if B == 1:  # back[:, 0] is contiguous: receive in place
+            dist.all_to_all_single(back[:, 0], out_g[0].view(P, Sl, G, d), group=group)
+        else:
+            recv = torch.empty((P, Sl, G, d), dtype=q.dtype, device=q.device)
+            dist.all_to_all_single(recv, out_g[b].view(P, Sl, G, d), group=group)
+            back[:, b] = recv
+    out = torch.empty_like(q)
+    kn.head_to_seq(back, out, P)
+    return out

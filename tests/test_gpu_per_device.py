@@ -1,0 +1,150 @@
+"""GPU parity of the per-device entry points against the float64 oracle.
+
+A device of a real ring holds only its query block and, at each step, one
+key/value block ("Ring Attention", "Cómo funciona la atención en anillo"):
+sp_ring_block_step computes that block pair from block tensors, with the
+mask in global token indices.  Every (i, j) pair must equal block i's rows of
+the oracle's ring partial at step (i - j) mod P, merging device i's P steps
+must give block i's rows of full attention, and sp_query_block_attn_fwd (the
+all-gathered variant: query block i against the whole K, V) must give those
+rows directly.  Shapes span ragged 128-row tiles, GQA, packed documents and
+both block orders."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import check_attention, np32
+import workloads
+from test_gpu_attention import _positions
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sp():
+    import sequence_parallelism_gb300 as m
+    return m
+
+
+CASES = [
+    # dtype, B, S, Hq, Hkv, d, P, order, pos_kind
+    ("bf16", 1, 1024, 4, 2, 128, 4, "contiguous", "causal"),
+    ("bf16", 1, 1024, 4, 2, 128, 4, "striped", "packed"),
+    ("bf16", 2, 600, 2, 1, 128, 3, "contiguous", "packed"),
+    ("bf16", 1, 768, 2, 2, 128, 3, "striped", "none"),
+    ("f32", 1, 96, 2, 1, 32, 3, "contiguous", "packed"),
+    ("f32", 2, 64, 2, 2, 16, 4, "striped", "causal"),
+]
+
+
+def _block(t, tokens):
+    return t[:, torch.from_numpy(tokens).to(t.device)].contiguous()
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_ring_block_step_every_pair(sp, case):
+    from sequence_parallelism_gb300 import _lib
+    dtype, B, S, Hq, Hkv, d, P, order, pos_kind = case
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 4100 + S, dtype)
+    pos = _positions(pos_kind, B, S, 77)
+    tpos = None if pos is None else torch.from_numpy(pos).cuda()
+    qn, kn, vn = np32(q), np32(k), np32(v)
+    ws = sp.attention_workspace(B, S, pos is not None, minimal=True)
+    blocks = [oracle.block_tokens(S, P, p, order) for p in range(P)]
+    partials = {}
+    for s in range(P):
+        ref_o, ref_l = oracle.ring_partial(qn, kn, vn, P, s, order, pos)
+        for i in range(P):
+            j = (i - s) % P
+            out = torch.full((B, S // P, Hq, d), float("nan"), dtype=q.dtype, device="cuda")
+            lse = torch.full((B, Hq, S // P), float("nan"), dtype=torch.float32, device="cuda")
+            _lib.sp_ring_block_step(_block(q, blocks[i]), _block(k, blocks[j]), _block(v, blocks[j]),
+                                    tpos, S, P, order, i, j, 0.0, out, lse, ws)
+            torch.cuda.synchronize()
+            check_attention(np32(out), lse.cpu().numpy(), ref_o[:, blocks[i]],
+                            ref_l[:, :, blocks[i]], dtype, f"{case} i={i} j={j}")
+            partials[(i, s)] = (out, lse)
+    # device i merges its P steps: block i's rows of full attention
+    full_o, full_l = oracle.full_attention(qn, kn, vn, pos)
+    for i in range(P):
+        outs = torch.stack([partials[(i, s)][0] for s in range(P)])
+        lses = torch.stack([partials[(i, s)][1] for s in range(P)])
+        mo, ml = sp.merge_partials(outs, lses)
+        torch.cuda.synchronize()
+        check_attention(np32(mo), ml.cpu().numpy(), full_o[:, blocks[i]], full_l[:, :, blocks[i]],
+                        dtype, f"{case} merged device {i}")
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_query_block_against_whole_sequence(sp, case):
+    from sequence_parallelism_gb300 import _lib
+    dtype, B, S, Hq, Hkv, d, P, order, pos_kind = case
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 4200 + S, dtype)
+    pos = _positions(pos_kind, B, S, 78)
+    tpos = None if pos is None else torch.from_numpy(pos).cuda()
+    full_o, full_l = oracle.full_attention(np32(q), np32(k), np32(v), pos)
+    ws = sp.attention_workspace(B, S, pos is not None)
+    ref_out, ref_lse = sp.blockwise_attention(q, k, v, P, order, tpos)
+    for i in range(P):
+        tok = oracle.block_tokens(S, P, i, order)
+        out = torch.full((B, S // P, Hq, d), float("nan"), dtype=q.dtype, device="cuda")
+        lse = torch.full((B, Hq, S // P), float("nan"), dtype=torch.float32, device="cuda")
+        _lib.sp_query_block_attn_fwd(_block(q, tok), k, v, tpos, P, order, i, 0.0, out, lse, ws)
+        torch.cuda.synchronize()
+        check_attention(np32(out), lse.cpu().numpy(), full_o[:, tok], full_l[:, :, tok], dtype,
+                        f"{case} query block {i}")
+        if pos is not None:
+            # causal calls visit the same tiles in the same order as the
+            # whole-sequence call: the same bits
+            ti = torch.from_numpy(tok).cuda()
+            assert torch.equal(out, ref_out[:, ti]) and torch.equal(lse, ref_lse[:, :, ti])
+
+
+def test_per_device_argument_errors(sp):
+    from sequence_parallelism_gb300 import _lib
+    q, k, v = workloads.small_case(1, 512, 2, 1, 128, 5, "bf16")
+    blk = lambda t: t[:, :128].contiguous()
+    ws = sp.attention_workspace(1, 512, False)
+    out = torch.empty_like(blk(q))
+    lse = torch.empty((1, 2, 128), dtype=torch.float32, device="cuda")
+    for i, j in ((4, 0), (0, 4), (-1, 0)):
+        with pytest.raises(_lib.SPError):
+            _lib.sp_ring_block_step(blk(q), blk(k), blk(v), None, 512, 4, "contiguous", i, j, 0.0,
+                                    out, lse, ws)
+    with pytest.raises(_lib.SPError):
+        _lib.sp_query_block_attn_fwd(blk(q), k, v, None, 4, "contiguous", 4, 0.0, out, lse, ws)
+    assert _lib.sp_last_launch_count() == 0
+
+
+def test_data_plane_on_one_rank_runs_the_library_kernels(sp):
+    """sequence_parallelism_gb300.dist with its default kernels on a
+    one-rank NCCL group (the only group one GPU allows): the ring, the
+    all-gathered variant and the Ulysses layer reduce to their per-device
+    calls and must match the oracle.  The exchanges between ranks are
+    covered by tests/test_dist_cpu.py on gloo ranks."""
+    import socket
+    import torch.distributed as dist
+    from sequence_parallelism_gb300 import dist as spd
+    with socket.socket() as s_:
+        s_.bind(("127.0.0.1", 0))
+        port = s_.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                            device_id=torch.device("cuda", torch.cuda.current_device()))
+    try:
+        B, S, Hq, Hkv, d = 1, 640, 4, 2, 128
+        q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 4300, "bf16")
+        pos = _positions("packed", B, S, 79)
+        tpos = torch.from_numpy(pos).cuda()
+        ref_o, ref_l = oracle.full_attention(np32(q), np32(k), np32(v), pos)
+        for fn in (spd.ring_attention, spd.allgather_kv_attention):
+            out, lse = fn(q, k, v, tpos, "contiguous")
+            torch.cuda.synchronize()
+            check_attention(np32(out), lse.cpu().numpy(), ref_o, ref_l, "bf16", fn.__name__)
+        out = spd.ulysses_attention(q, k, v, tpos, ring_blocks=2)
+        torch.cuda.synchronize()
+        err = np.abs(np32(out).astype(np.float64) - ref_o)
+        assert err.max() <= 2e-2 and err.mean() <= 2e-3
+    finally:
+        dist.destroy_process_group()
