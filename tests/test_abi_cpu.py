@@ -154,3 +154,30 @@ def test_barrier_check_rejects_bad_arguments(lib):
     assert f(ctypes.c_void_p(0x20010), 1000, None) == SP_ERR_WORKSPACE
     assert f(FAKE_WS, 0, None) == SP_ERR_INVALID_ARG
     assert f(FAKE_WS, 2000000, None) == SP_ERR_INVALID_ARG
+
+
+def test_per_device_entry_points_reject_bad_arguments(lib):
+    """sp_ring_block_step / sp_query_block_attn_fwd: block indices outside
+    0 .. P-1, indivisible sizes and missing pointers fail on the host."""
+    f32 = ctypes.c_float
+    ring = lambda i, j, S=1024, P=4, q=FAKE: lib.sp_ring_block_step(
+        q, FAKE, FAKE, None, 1, S, 2, 1, 128, P, 0, i, j, f32(0.0), 0, FAKE, None, FAKE_WS,
+        ctypes.c_size_t(1 << 20), None)
+    for i, j in ((4, 0), (0, 4), (-1, 0), (0, -1)):
+        assert ring(i, j) == SP_ERR_INVALID_ARG
+    assert ring(0, 0, S=1023) == SP_ERR_INVALID_ARG     # S % P
+    assert ring(0, 0, P=0) == SP_ERR_INVALID_ARG
+    assert ring(0, 0, q=None) == SP_ERR_INVALID_ARG
+    qb = lambda i, P=4: lib.sp_query_block_attn_fwd(
+        FAKE, FAKE, FAKE, None, 1, 1024, 2, 1, 128, P, 0, i, f32(0.0), 0, FAKE, None, FAKE_WS,
+        ctypes.c_size_t(1 << 20), None)
+    assert qb(4) == SP_ERR_INVALID_ARG and qb(-1) == SP_ERR_INVALID_ARG and qb(0, P=0) == \
+        SP_ERR_INVALID_ARG
+    assert lib.sp_last_launch_count() == 0
+
+
+def test_permutation_threshold_setting_round_trips(lib):
+    lib.sp_permute_set_bulk_min_bytes.restype = ctypes.c_size_t
+    lib.sp_permute_set_bulk_min_bytes.argtypes = [ctypes.c_size_t]
+    prev = lib.sp_permute_set_bulk_min_bytes(12345)
+    assert lib.sp_permute_set_bulk_min_bytes(prev) == 12345
