@@ -51,6 +51,10 @@ def _fullsize_oracle_early(request):
         import torch
         if torch.cuda.is_available():
             pool = request.getfixturevalue("fullsize_oracle")
+            from fullsize_oracle import BACKWARD_REQUESTS
             for n in names:
-                pool.submit(n)
+                if n in BACKWARD_REQUESTS:
+                    pool.submit_backward(n)
+                else:
+                    pool.submit(n)
     yield

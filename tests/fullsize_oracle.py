@@ -64,6 +64,13 @@ def request_spec(name):
     raise KeyError(name)
 
 
+BACKWARD_REQUESTS = {  # name: (workload, order)
+    "bwd_llama8b_32k": ("llama8b_32k", "contiguous"),
+    "bwd_packed_128k_striped": ("packed_128k", "striped"),
+}
+BACKWARD_DQ_ROWS = 512
+
+
 def _doc_ranges(pos, S):
     """[start, end) of every document of batch row 0 (all rows of a workload
     share one position_ids row)."""
@@ -98,6 +105,70 @@ def _rows_piece(path, h, kvh, lo, hi, rows, causal):
     out, lse = oracle.attention_rows(q, k, v, np.asarray(rows) - lo, pos,
                                      max_chunk_elems=_CHUNK_ELEMS)
     return out[:, :, 0, :], lse[:, 0, :]
+
+
+def _load(path, name, h0, h1):
+    """float32 values of heads [h0, h1) of a stored tensor, token-major
+    ([B][S][h1-h0][d]) as the oracle takes them."""
+    a = np.load(os.path.join(path, name + ".npy"), mmap_mode="r")  # [B][H][S][d]
+    return np.ascontiguousarray(_values(a[:, h0:h1]).transpose(0, 2, 1, 3))
+
+
+def _dq_piece(path, h, kvh, rows, causal):
+    """dq of query head h on the given rows (oracle.attention_backward_rows)."""
+    import oracle
+    pos = np.load(os.path.join(path, "pos.npy")) if causal else None
+    dq = oracle.attention_backward_rows(_load(path, "q", h, h + 1), _load(path, "k", kvh, kvh + 1),
+                                        _load(path, "v", kvh, kvh + 1),
+                                        _load(path, "dout", h, h + 1), rows, pos)
+    return dq[:, :, 0, :]
+
+
+def _dkdv_piece(path, h, kvh, keys, causal):
+    """Query head h's share of dk, dv on the given key rows of its key/value
+    head (oracle.attention_backward_keys on that head pair)."""
+    import oracle
+    pos = np.load(os.path.join(path, "pos.npy")) if causal else None
+    dk, dv = oracle.attention_backward_keys(_load(path, "q", h, h + 1),
+                                            _load(path, "k", kvh, kvh + 1),
+                                            _load(path, "v", kvh, kvh + 1),
+                                            _load(path, "dout", h, h + 1), keys, pos)
+    return dk[:, :, 0, :], dv[:, :, 0, :]
+
+
+def backward_dout(cfg, device="cuda"):
+    """The upstream gradient of the full-size backward tests: N(0, 1) from a
+    seeded generator (seed + 7), rounded to bf16."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(cfg["seed"] + 7)
+    return torch.randn((cfg["B"], cfg["S"], cfg["Hq"], cfg["d"]), generator=g,
+                       device=device).to(torch.bfloat16)
+
+
+def backward_keys(pos, S, P, order):
+    """Key tokens whose observers are cheap to enumerate: the last 16 tokens
+    of every document, every token of documents up to 128 long, the first 16
+    of documents up to 5000 long; for a single document, 48 seeded keys of
+    the last block and the first 8 keys of that block."""
+    import oracle
+    seg_starts = np.nonzero(pos[0] == 0)[0]
+    ends = np.append(seg_starts[1:], S)
+    keys = set()
+    for a, e in zip(seg_starts, ends):
+        L = e - a
+        keys.update(range(max(a, e - 16), e))
+        if L <= 128:
+            keys.update(range(a, e))
+        elif L <= 5000:
+            keys.update(range(a, a + 16))
+    if len(seg_starts) == 1:
+        Lb = S // P
+        blk = oracle.block_tokens(S, P, P - 1, order)
+        rng = np.random.default_rng(S)
+        keys.update(int(t) for t in rng.choice(blk, 48, replace=False))
+        keys.update(range(S - Lb, S - Lb + 8))
+    return np.array(sorted(keys), dtype=np.int64)
 
 
 class FullSizeOracle:
@@ -165,6 +236,67 @@ class FullSizeOracle:
         cfg = workloads.CONFIGS[workload]
         self._queue(name, self._workload_dir(workload), workloads.position_ids(cfg), rows, heads,
                     tuple(cfg[x] for x in ("B", "S", "Hq", "Hkv", "d")))
+
+    def submit_backward(self, name):
+        """Queue a backward request: dq on BACKWARD_DQ_ROWS seeded rows of
+        every query head, dk and dv on backward_keys() of every key/value
+        head (one piece per query head, summed over its group)."""
+        if name in self.requests:
+            return
+        workload, order = BACKWARD_REQUESTS[name]
+        cfg = workloads.CONFIGS[workload]
+        B, S, Hq, Hkv, d, P = (cfg[x] for x in ("B", "S", "Hq", "Hkv", "d", "P"))
+        wdir = self._workload_dir(workload)
+        dpath = os.path.join(wdir, "dout.npy")
+        if not os.path.exists(dpath):
+            import torch
+            t = backward_dout(cfg)
+            np.save(dpath, t.permute(0, 2, 1, 3).contiguous().view(torch.int16).cpu().numpy()
+                    .view(np.uint16))
+            del t
+        pos = workloads.position_ids(cfg)
+        rows = workloads.sample_rows(S, P, BACKWARD_DQ_ROWS, cfg["seed"] + 3, order)
+        keys = backward_keys(pos, S, P, order)
+        self._queue_backward(name, wdir, pos, rows, keys, (B, Hq, Hkv, d))
+
+    def submit_backward_arrays(self, name, q, k, v, dout, pos, rows, keys):
+        """A backward request on given arrays (float32 numpy, [B][S][H][d])."""
+        wdir = self._write(name, q, k, v, pos)
+        np.save(os.path.join(wdir, "dout.npy"),
+                np.ascontiguousarray(dout.astype(np.float32).transpose(0, 2, 1, 3)))
+        self._queue_backward(name, wdir, pos, np.asarray(rows), np.asarray(keys),
+                             (q.shape[0], q.shape[2], k.shape[2], q.shape[3]))
+
+    def _queue_backward(self, name, wdir, pos, rows, keys, dims):
+        B, Hq, Hkv, d = dims
+        causal = pos is not None
+        g = Hq // Hkv
+        dq_jobs = [(h, self.pool.apply_async(_dq_piece, (wdir, h, h // g, rows, causal)))
+                   for h in range(Hq)]
+        kv_jobs = [(h, self.pool.apply_async(_dkdv_piece, (wdir, h, h // g, keys, causal)))
+                   for h in range(Hq)]
+        self.requests[name] = dict(kind="backward", rows=rows, keys=keys, dq_jobs=dq_jobs,
+                                   kv_jobs=kv_jobs, dims=(B, Hq, Hkv, d), result=None)
+
+    def backward_result(self, name, timeout=3600.0):
+        """(rows, dq [B][R][Hq][d], keys, dk [B][J][Hkv][d], dv), float64."""
+        self.submit_backward(name)
+        req = self.requests[name]
+        if req["result"] is None:
+            B, Hq, Hkv, d = req["dims"]
+            g = Hq // Hkv
+            dq = np.zeros((B, len(req["rows"]), Hq, d))
+            for h, res in req["dq_jobs"]:
+                dq[:, :, h, :] = res.get(timeout)
+            dk = np.zeros((B, len(req["keys"]), Hkv, d))
+            dv = np.zeros_like(dk)
+            for h, res in req["kv_jobs"]:
+                a, b = res.get(timeout)
+                dk[:, :, h // g, :] += a
+                dv[:, :, h // g, :] += b
+            req["result"] = (req["rows"], dq, req["keys"], dk, dv)
+            req["dq_jobs"], req["kv_jobs"] = [], []
+        return req["result"]
 
     def submit_arrays(self, name, q, k, v, pos, rows=None, heads=None):
         """Queue a request on given arrays (q [B][S][Hq][d], k/v

@@ -80,3 +80,24 @@ def test_bf16_inputs_travel_exactly(pool):
     ref_out, ref_lse = oracle.attention_rows(f(q), f(k), f(v), None, pos)
     np.testing.assert_allclose(out, ref_out, rtol=0, atol=1e-12)
     np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("n_docs", [1, 4])
+def test_backward_pieces_equal_whole_gqa_oracle(pool, n_docs):
+    """dq per query head, and dk/dv per query head summed over each GQA
+    group, equal the oracle's whole-tensor attention_backward_rows / _keys."""
+    S, Hq, Hkv, d = 160, 4, 2, 16
+    q, k, v, pos = _case(S, Hq, Hkv, d, 31 + n_docs, n_docs)
+    dout = np.random.default_rng(5).standard_normal(q.shape).astype(np.float32)
+    rows = workloads.sample_rows(S, 4, 24, 3, "contiguous")
+    keys = np.array([0, 5, 77, 100, 159])
+    name = f"cpu_bwd_{n_docs}"
+    pool.submit_backward_arrays(name, q, k, v, dout, pos, rows, keys)
+    got_rows, dq, got_keys, dk, dv = pool.backward_result(name, timeout=600)
+    ref_dq = oracle.attention_backward_rows(q, k, v, dout, rows, pos)
+    ref_dk, ref_dv = oracle.attention_backward_keys(q, k, v, dout, keys, pos)
+    np.testing.assert_array_equal(got_rows, rows)
+    np.testing.assert_array_equal(got_keys, keys)
+    np.testing.assert_allclose(dq, ref_dq, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, ref_dk, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, ref_dv, rtol=0, atol=1e-12)
