@@ -14,6 +14,11 @@ without the built library raises ImportError -- there is no CPU path.
     ulysses_ring_attention(q, k, v, P_u, P_r)  Ulysses + Ring hybrid (heads < devices)
     blockwise_attention_backward(...)          dq, dk, dv from out, dout and lse
     doc_starts(position_ids)                   O(n) causal-mask carrier
+    ring_block_step(q_blk, k_blk, v_blk, ...)  one device's ring step on block tensors
+    query_block_attention(q_blk, k, v, ...)    one device's query block against all K/V
+
+sequence_parallelism_gb300.dist runs the ring, all-gathered and Ulysses
+exchanges across the ranks of a torch.distributed group (one GPU per rank).
 """
 
 import torch
@@ -24,7 +29,7 @@ from ._lib import SPError  # noqa: F401
 __all__ = ["seq_to_head", "head_to_seq", "blockwise_attention", "ring_step", "merge_partials",
            "ulysses_attention", "ulysses_attention_backward", "ulysses_ring_attention",
            "blockwise_attention_backward",
-           "doc_starts", "attention_workspace",
+           "doc_starts", "attention_workspace", "ring_block_step", "query_block_attention",
            "SPError"]
 
 
@@ -78,6 +83,42 @@ def ring_step(q, k, v, P, step, order="contiguous", position_ids=None, scale=0.0
         workspace = attention_workspace(B, S, position_ids is not None, q.device)
     return _lib.sp_blockwise_attn_step(q, k, v, position_ids, P, order, step, scale, out, lse,
                                        workspace)
+
+
+def _block_outputs(q_blk, out, lse):
+    B, Lb, Hq, d = q_blk.shape
+    if out is None:
+        out = torch.empty_like(q_blk)
+    if lse is None:
+        lse = torch.empty((B, Hq, Lb), dtype=torch.float32, device=q_blk.device)
+    return out, lse
+
+
+def ring_block_step(q_blk, k_blk, v_blk, P, i, j, order="contiguous", position_ids=None,
+                    scale=0.0, out=None, lse=None, workspace=None):
+    """What device i of a ring computes at the step it holds key/value block
+    j: query block i ([B][S/P][Hq][d]) against block j ([B][S/P][Hkv][d]),
+    masks in global token indices (position_ids of the whole sequence, or
+    None for non-causal).  Returns the partial (out, lse [B][Hq][S/P])."""
+    B, Lb = q_blk.shape[:2]
+    S = Lb * P
+    out, lse = _block_outputs(q_blk, out, lse)
+    if workspace is None:
+        workspace = attention_workspace(B, S, position_ids is not None, q_blk.device)
+    return _lib.sp_ring_block_step(q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, scale,
+                                   out, lse, workspace)
+
+
+def query_block_attention(q_blk, k, v, P, i, order="contiguous", position_ids=None, scale=0.0,
+                          out=None, lse=None, workspace=None):
+    """Query block i ([B][S/P][Hq][d]) against the whole sequence's k, v
+    ([B][S][Hkv][d]) in ring order: block i's rows of blockwise_attention."""
+    B, S = k.shape[:2]
+    out, lse = _block_outputs(q_blk, out, lse)
+    if workspace is None:
+        workspace = attention_workspace(B, S, position_ids is not None, q_blk.device)
+    return _lib.sp_query_block_attn_fwd(q_blk, k, v, position_ids, P, order, i, scale, out, lse,
+                                        workspace)
 
 
 def blockwise_attention_backward(q, k, v, out, dout, lse, P, order="contiguous",

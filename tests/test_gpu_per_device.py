@@ -102,6 +102,28 @@ def test_query_block_against_whole_sequence(sp, case):
             assert torch.equal(out, ref_out[:, ti]) and torch.equal(lse, ref_lse[:, :, ti])
 
 
+def test_package_helpers_match_the_c_calls(sp):
+    """sp.ring_block_step / sp.query_block_attention allocate their outputs
+    and give the same bits as the C entry points."""
+    from sequence_parallelism_gb300 import _lib
+    B, S, Hq, Hkv, d, P = 1, 768, 2, 1, 128, 3
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 4400, "bf16")
+    pos = torch.from_numpy(_positions("packed", B, S, 80)).cuda()
+    blocks = [oracle.block_tokens(S, P, p, "striped") for p in range(P)]
+    o1, l1 = sp.ring_block_step(_block(q, blocks[2]), _block(k, blocks[0]), _block(v, blocks[0]),
+                                P, 2, 0, "striped", pos)
+    ws = sp.attention_workspace(B, S, True)
+    o2, l2 = torch.empty_like(o1), torch.empty_like(l1)
+    _lib.sp_ring_block_step(_block(q, blocks[2]), _block(k, blocks[0]), _block(v, blocks[0]), pos,
+                            S, P, "striped", 2, 0, 0.0, o2, l2, ws)
+    o3, l3 = sp.query_block_attention(_block(q, blocks[1]), k, v, P, 1, "striped", pos)
+    o4, l4 = sp.blockwise_attention(q, k, v, P, "striped", pos)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    t1 = torch.from_numpy(blocks[1]).cuda()
+    assert torch.equal(o3, o4[:, t1]) and torch.equal(l3, l4[:, :, t1])
+
+
 def test_per_device_argument_errors(sp):
     from sequence_parallelism_gb300 import _lib
     q, k, v = workloads.small_case(1, 512, 2, 1, 128, 5, "bf16")
