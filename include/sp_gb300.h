@@ -56,7 +56,7 @@ typedef struct CUstream_st* sp_stream_t;
 typedef enum sp_status {
   SP_OK = 0,
   SP_ERR_INVALID_ARG = 1,     /* bad pointer, size, divisibility or enum   */
-  SP_ERR_UNSUPPORTED = 2,     /* valid request this build cannot run        */
+  SP_ERR_UNSUPPORTED = 2,     /* valid request the library does not support */
   SP_ERR_WORKSPACE = 3,       /* workspace NULL/too small/misaligned        */
   SP_ERR_CUDA = 4,            /* CUDA runtime/driver error at launch        */
   SP_ERR_DEVICE_TIMEOUT = 5   /* a kernel gave up waiting on a barrier      */
