@@ -482,8 +482,11 @@ def causal_attention_measurement(name, order, peaks, peak_kind, flush, stream, r
         raise RuntimeError(f"device error word {code:#x} in {name} {order}")
     fl = attention_flops(cfg, pos_np)
     rl = _attn_roofline(fl, t, peaks, peak_kind, name)
+    sustained = peaks.get("bf16_tflops_sustained")
     return {"workload": name, "order": order, "P": P, "ms": round(t, 4),
-            "TFLOP/s": rl["achieved"], "frac_of_bf16_peak": rl["frac"], "roofline": rl,
+            "TFLOP/s": rl["achieved"], "frac_of_bf16_peak": rl["frac"],
+            "frac_of_sustained_bf16_peak": round(rl["achieved"] / sustained, 4) if sustained
+            else None, "roofline": rl,
             "flops": fl, "reps": reps, "clocks": clocks,
             "note": "doc_start scan + attention kernel, median of reps, L2 flushed"}
 
@@ -525,6 +528,15 @@ def ulysses_layer_measurement(peaks, peak_kind, flush, stream, reps=50):
     for _ in range(3):
         layer()
     torch.cuda.synchronize()
+    # the same layer captured once into a CUDA graph and replayed (the launch
+    # gaps between its kernels shrink; the kernels are the same)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        layer()
+    torch.cuda.synchronize()
+    graph_ms, _, _ = _timed(graph.replay, flush, stream, reps)
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     time.sleep(0.2)
@@ -541,6 +553,8 @@ def ulysses_layer_measurement(peaks, peak_kind, flush, stream, reps=50):
     perm_gbs = 2.0 * 3 * q.numel() * 2 / (perm * 1e-3) / 1e9
     inv_gbs = 2.0 * q.numel() * 2 / (inv * 1e-3) / 1e9
     return {"ms_per_step": round(step, 4), "TFLOP/s_step": round(fl / (step * 1e-3) / 1e12, 1),
+            "graph_ms_per_step": round(graph_ms, 4),
+            "graph_TFLOP/s_step": round(fl / (graph_ms * 1e-3) / 1e12, 1),
             "attention_ms": round(attn, 4), "frac_of_bf16_peak": rl["frac"], "roofline": rl,
             "permute": permute_summary(perm_gbs, inv_gbs, peaks), "reps": reps,
             "clocks": clocks, "note": "mean of reps, L2 flushed before each step"}
