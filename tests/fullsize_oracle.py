@@ -31,7 +31,7 @@ import workloads
 
 # one BLAS thread per worker process: the pool supplies the parallelism
 _WORKER_ENV = {"OPENBLAS_NUM_THREADS": "1", "OMP_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
-_CHUNK_ELEMS = 1 << 23  # scores per oracle chunk (64 MiB of float64)
+_CHUNK_ELEMS = 1 << 24  # scores per oracle chunk (128 MiB of float64)
 
 
 def rotating_heads(Hq, Hkv):
@@ -41,22 +41,14 @@ def rotating_heads(Hq, Hkv):
     return [kv * g + kv % g for kv in range(Hkv)]
 
 
-def _union_samples(cfg, n):
-    rows = [workloads.sample_rows(cfg["S"], cfg["P"], n, cfg["seed"], o) for o in cfg["orders"]]
-    return np.unique(np.concatenate(rows))
-
-
 def request_spec(name):
     """(workload, rows or None for every row, heads) of a named request."""
     if name == "ulysses_4k":
         return "ulysses_4k", None, None
     if name == "llama8b_32k":
         return "llama8b_32k", None, None
-    if name == "packed_128k_heads":  # every row of one head per key/value group
-        cfg = workloads.CONFIGS["packed_128k"]
-        return "packed_128k", None, rotating_heads(cfg["Hq"], cfg["Hkv"])
-    if name == "packed_128k_rows":   # sampled rows (both orders' block edges), every head
-        return "packed_128k", _union_samples(workloads.CONFIGS["packed_128k"], 256), None
+    if name == "packed_128k":
+        return "packed_128k", None, None
     if name == "halfmil_512k":       # the workload's 4096 seeded rows, every head
         cfg = workloads.CONFIGS["halfmil_512k"]
         return "halfmil_512k", workloads.sample_rows(cfg["S"], cfg["P"], cfg["sampled_rows"],
