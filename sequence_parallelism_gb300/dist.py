@@ -13,7 +13,9 @@ The pages describe three ways to spread one attention layer over P devices:
   funciona Ulysses Sequence Parallelism (SP)"; "DeepSpeed-Ulysses",
   "Method"): an all-to-all turns every device's sequence shard of all heads
   into the whole sequence of a head group, attention runs per head group, and
-  a second all-to-all turns the result back.  ulysses_attention() below.
+  a second all-to-all turns the result back.  ulysses_attention() below,
+  and its gradients (the same exchanges transposed around the per-group
+  backward) in ulysses_attention_backward().
 * All-gathered K/V ("Ulysses序列并行技术详解：ms-swift如何降低长序列显存占用"):
   K and V reach every rank through two all-gathers and each rank attends its
   own query block against the whole sequence.  allgather_kv_attention() below.
@@ -70,6 +72,15 @@ class LibraryKernels:
     def attention(self, q, k, v, position_ids, P, order, out, lse):
         ws = self.workspace(q.shape[0], q.shape[1], position_ids is not None, q.device)
         _lib.sp_blockwise_attn_fwd(q, k, v, position_ids, P, order, 0.0, out, lse, ws)
+
+    def attention_backward(self, q, k, v, out, dout, lse, position_ids, P, order, dq, dk, dv):
+        B, S, Hq, _ = q.shape
+        key = ("bwd", B, S, Hq, P, position_ids is not None, str(q.device))
+        if key not in self._ws:
+            n = _lib.sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, P, position_ids is not None)
+            self._ws[key] = torch.empty(n, dtype=torch.uint8, device=q.device)
+        _lib.sp_blockwise_attn_bwd(q, k, v, out, dout, lse, position_ids, P, order, 0.0, dq, dk,
+                                   dv, self._ws[key])
 
 
 _DEFAULT = None
@@ -169,12 +180,46 @@ def allgather_kv_attention(q_blk, k_blk, v_blk, position_ids, order="contiguous"
     return out, lse
 
 
+def _to_head_groups(t, P, kn, group):
+    """[B][S/P][H][d] sequence shard of every rank -> this rank's head group
+    for the whole sequence, [B][S][H/P][d]: local seq->head, then an
+    all-to-all (one batch row at a time; recv[p] = rank p's tokens)."""
+    B, Sl, H, d = t.shape
+    gh = H // P
+    y = torch.empty((P, B, Sl, gh, d), dtype=t.dtype, device=t.device)
+    kn.seq_to_head(t, y, P)
+    f = torch.empty((B, Sl * P, gh, d), dtype=t.dtype, device=t.device)
+    for b in range(B):
+        dist.all_to_all_single(f[b].view(P, Sl, gh, d), y[:, b].contiguous(), group=group)
+    return f
+
+
+def _to_seq_shards(f, P, kn, group):
+    """The inverse: this rank's head group for the whole sequence,
+    [B][S][G][d] -> its sequence shard of every head, [B][S/P][G*P][d]
+    (all-to-all sending shard p to rank p, then local head->seq)."""
+    B, S, G, d = f.shape
+    Sl = S // P
+    back = torch.empty((P, B, Sl, G, d), dtype=f.dtype, device=f.device)
+    for b in range(B):
+        if B == 1:  # back[:, 0] is contiguous: receive in place
+            dist.all_to_all_single(back[:, 0], f[0].view(P, Sl, G, d), group=group)
+        else:
+            recv = torch.empty((P, Sl, G, d), dtype=f.dtype, device=f.device)
+            dist.all_to_all_single(recv, f[b].view(P, Sl, G, d), group=group)
+            back[:, b] = recv
+    out = torch.empty((B, Sl, G * P, d), dtype=f.dtype, device=f.device)
+    kn.head_to_seq(back, out, P)
+    return out
+
+
 def ulysses_attention(q, k, v, position_ids=None, ring_blocks=1, order="contiguous", group=None,
-                      kernels=None):
+                      kernels=None, return_context=False):
     """One Ulysses attention layer across the group: this rank holds the
     sequence shard r (tokens [r*S/P, (r+1)*S/P)) of every head, q
     [B][S/P][Hq][d], k/v [B][S/P][Hkv][d]; returns its shard of the output
-    [B][S/P][Hq][d].
+    [B][S/P][Hq][d] (and, with return_context, what
+    ulysses_attention_backward needs).
 
     seq->head on the shard gives P head-group slices; the first all-to-all
     sends slice g to rank g, so this rank holds head group r for the whole
@@ -189,31 +234,29 @@ def ulysses_attention(q, k, v, position_ids=None, ring_blocks=1, order="contiguo
     if Hq % P or Hkv % P:
         raise ValueError("Ulysses needs the head counts divisible by the group size")
     S = Sl * P
-    G, Gk = Hq // P, Hkv // P
-    groups = []
-    for t, gh in ((q, G), (k, Gk), (v, Gk)):
-        y = torch.empty((P, B, Sl, gh, d), dtype=t.dtype, device=t.device)
-        kn.seq_to_head(t, y, P)
-        groups.append(y)
-    # first all-to-all, one batch row at a time: recv[p] = rank p's tokens
-    full = []
-    for y, gh in zip(groups, (G, Gk, Gk)):
-        f = torch.empty((B, S, gh, d), dtype=y.dtype, device=y.device)
-        for b in range(B):
-            dist.all_to_all_single(f[b].view(P, Sl, gh, d), y[:, b].contiguous(), group=group)
-        full.append(f)
-    out_g = torch.empty_like(full[0])
+    G = Hq // P
+    fq, fk, fv = (_to_head_groups(t, P, kn, group) for t in (q, k, v))
+    out_g = torch.empty_like(fq)
     lse_g = torch.empty((B, G, S), dtype=_lse_dtype(q), device=q.device)
-    kn.attention(full[0], full[1], full[2], position_ids, ring_blocks, order, out_g, lse_g)
-    # second all-to-all: sequence shard p of this head group goes to rank p
-    back = torch.empty((P, B, Sl, G, d), dtype=q.dtype, device=q.device)
-    for b in range(B):
-        if B == 1:  # back[:, 0] is contiguous: receive in place
-            dist.all_to_all_single(back[:, 0], out_g[0].view(P, Sl, G, d), group=group)
-        else:
-            recv = torch.empty((P, Sl, G, d), dtype=q.dtype, device=q.device)
-            dist.all_to_all_single(recv, out_g[b].view(P, Sl, G, d), group=group)
-            back[:, b] = recv
-    out = torch.empty_like(q)
-    kn.head_to_seq(back, out, P)
-    return out
+    kn.attention(fq, fk, fv, position_ids, ring_blocks, order, out_g, lse_g)
+    out = _to_seq_shards(out_g, P, kn, group)
+    if not return_context:
+        return out
+    return out, dict(q=fq, k=fk, v=fv, out=out_g, lse=lse_g, pos=position_ids, rb=ring_blocks,
+                     order=order)
+
+
+def ulysses_attention_backward(ctx, dout, group=None, kernels=None):
+    """Gradients of ulysses_attention across the group: dout, this rank's
+    sequence shard [B][S/P][Hq][d], goes to the head groups like q did (the
+    transpose of the second all-to-all), every rank runs the blockwise
+    attention backward on its head group for the whole sequence, and dq, dk,
+    dv come back to sequence shards (the transpose of the first all-to-all).
+    Returns (dq, dk, dv), this rank's shards."""
+    kn = _kernels(kernels)
+    P, _ = _world(group)
+    fdo = _to_head_groups(dout, P, kn, group)
+    dq_g, dk_g, dv_g = (torch.empty_like(ctx[n]) for n in ("q", "k", "v"))
+    kn.attention_backward(ctx["q"], ctx["k"], ctx["v"], ctx["out"], fdo, ctx["lse"], ctx["pos"],
+                          ctx["rb"], ctx["order"], dq_g, dk_g, dv_g)
+    return tuple(_to_seq_shards(g, P, kn, group) for g in (dq_g, dk_g, dv_g))

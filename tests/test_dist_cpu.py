@@ -83,6 +83,11 @@ class OracleKernels:
     def head_to_seq(self, y, x, P):
         x.copy_(torch.from_numpy(oracle.head_to_seq(y.numpy())))
 
+    def attention_backward(self, q, k, v, out, dout, lse, position_ids, P, order, dq, dk, dv):
+        g = oracle.attention_backward(q.numpy(), k.numpy(), v.numpy(), dout.numpy(), self.pos)
+        for dst, src in zip((dq, dk, dv), g):
+            dst.copy_(torch.from_numpy(src))
+
     def attention(self, q, k, v, position_ids, P, order, out, lse):
         o, l_ = oracle.blockwise_ring_attention(q.numpy(), k.numpy(), v.numpy(), P, order,
                                                 self.pos)
@@ -109,12 +114,17 @@ def _worker(rank, world, port, kind, params, results):
             out, lse = fn(blk(q), blk(k), blk(v), tpos, order, kernels=kn)
             err = max(np.abs(out.numpy() - ref_o[:, t]).max(),
                       np.abs(lse.numpy() - ref_l[:, :, t]).max())
-        else:  # ulysses: sequence shards, contiguous
+        else:  # ulysses: sequence shards, contiguous; forward and backward
             Sl = S // world
             sh = lambda a: torch.from_numpy(np.ascontiguousarray(a[:, rank * Sl:(rank + 1) * Sl]))
-            out = spd.ulysses_attention(sh(q), sh(k), sh(v), tpos, ring_blocks=2, order=order,
-                                        kernels=kn)
+            out, ctx = spd.ulysses_attention(sh(q), sh(k), sh(v), tpos, ring_blocks=2, order=order,
+                                             kernels=kn, return_context=True)
             err = np.abs(out.numpy() - ref_o[:, rank * Sl:(rank + 1) * Sl]).max()
+            dout = np.random.default_rng(seed + 1).standard_normal(q.shape)
+            grads = spd.ulysses_attention_backward(ctx, sh(dout), kernels=kn)
+            ref_g = oracle.attention_backward(q, k, v, dout, pos)
+            for g_, r_ in zip(grads, ref_g):
+                err = max(err, np.abs(g_.numpy() - r_[:, rank * Sl:(rank + 1) * Sl]).max())
         results[rank] = (float(err), log)
     finally:
         dist.destroy_process_group()
@@ -156,7 +166,7 @@ def test_allgather_kv(world, params):
     (2, (2, 40, 2, 2, 8, "none", "striped", 32)),
     (4, (1, 64, 8, 4, 8, "causal", "contiguous", 33)),
 ])
-def test_ulysses_all_to_all(world, params):
+def test_ulysses_all_to_all_forward_and_backward(world, params):
     res = _run(world, "ulysses", params)
     for rank in range(world):
         assert res[rank][0] < 1e-12

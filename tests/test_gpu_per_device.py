@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import check_attention, np32
+from helpers import check_attention, check_grad, np32
 import workloads
 from test_gpu_attention import _positions
 
@@ -164,9 +164,16 @@ def test_data_plane_on_one_rank_runs_the_library_kernels(sp):
             out, lse = fn(q, k, v, tpos, "contiguous")
             torch.cuda.synchronize()
             check_attention(np32(out), lse.cpu().numpy(), ref_o, ref_l, "bf16", fn.__name__)
-        out = spd.ulysses_attention(q, k, v, tpos, ring_blocks=2)
+        out, ctx = spd.ulysses_attention(q, k, v, tpos, ring_blocks=2, return_context=True)
         torch.cuda.synchronize()
         err = np.abs(np32(out).astype(np.float64) - ref_o)
         assert err.max() <= 2e-2 and err.mean() <= 2e-3
+        g = torch.Generator(device="cuda").manual_seed(4301)
+        dout = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
+        grads = spd.ulysses_attention_backward(ctx, dout)
+        torch.cuda.synchronize()
+        ref_g = oracle.attention_backward(np32(q), np32(k), np32(v), np32(dout), pos)
+        for name, got, ref in zip(("dq", "dk", "dv"), grads, ref_g):
+            check_grad(np32(got), ref, "bf16", f"one-rank Ulysses {name}")
     finally:
         dist.destroy_process_group()
