@@ -56,12 +56,26 @@ TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "dram_traffic.json")
 KERNEL_SOURCES = ("attn_bf16.cu", "attn_common.cuh", "ptx.cuh", "common.cuh")
 
 
-def kernel_sources_sha256():
+def _code_only(text):
+    """C++ source without comments and whitespace: what the compiler sees of
+    it (a comment edit leaves the recorded capture valid, a code edit does not)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return re.sub(r"\s+", "", text)
+
+
+def kernel_sources_sha256(read=None):
+    """SHA-256 of the attention kernel's sources (code only).  `read(name)`
+    returns a file's text (default: the working tree)."""
     import hashlib
+    if read is None:
+        def read(name):
+            with open(os.path.join(ROOT, "sequence_parallelism_gb300", "csrc", name)) as f:
+                return f.read()
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "sequence_parallelism_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        h.update(_code_only(read(name)).encode())
     return h.hexdigest()
 
 

@@ -26,6 +26,11 @@
 // runs.  O is rescaled in TMEM only when a row's max grows by more than
 // 2^8 (exact after the final division; bf16 P stays far from overflow).
 //
+// Per-device form (what one device of a real ring holds): a fixed query
+// block whose rows live in a block tensor, and optionally a single key/value
+// block tensor for one ring step; tensor maps over those block tensors, masks
+// and doc_start in global token indices (AttnArgs::q_block, ::kv_block).
+//
 // Operand layouts (all 128-byte swizzled, as TMA writes them):
 //   Q, K tile: [2 halves of d][128 rows][64 elements]  K-major for S = Q K^T
 //   V tile   : [2 halves of d][128 keys][64 elements]  MN-major B for O += P V
