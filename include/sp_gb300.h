@@ -328,9 +328,26 @@ sp_status sp_blockwise_attn_fwd_noalloc(const void* q, const void* k, const void
  * every tensor pointer 16-byte aligned, else SP_ERR_INVALID_ARG), SP_F32
  * with d <= 256 (CUDA cores, float32 throughout).  workspace:
  * sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, P, position_ids != NULL)
- * bytes, 256-byte aligned.  Errors as for sp_blockwise_attn_fwd.
+ * bytes, 256-byte aligned (it includes a float32 dQ accumulator of
+ * B * Hq * P * Lbp * 128 floats, Lbp = S/P rounded up to a multiple of 128,
+ * used by the bf16 path when dQ is accumulated by reductions, see
+ * sp_set_bwd_dq_reduction).  Errors as for sp_blockwise_attn_fwd.
  * ------------------------------------------------------------------------ */
 size_t sp_blockwise_attn_bwd_workspace_bytes(int B, int S, int Hq, int P, int causal);
+
+/* How the bf16 backward forms dQ, for the whole process; returns the
+ * previous setting.
+ *   on != 0 (default): one kernel per 128-key tile multiplies S^T and dP^T
+ *     once and forms dV, dK and each (query tile, key tile) piece of dQ; the
+ *     pieces are added into the workspace's float32 accumulator by vector
+ *     reductions in whatever order the tiles finish, then scaled and rounded
+ *     to bf16.  10 d FLOPs per allowed (query, key) pair; dq is reproducible
+ *     to float32 rounding of the sum, not bit for bit.
+ *   on == 0: two kernels (dQ query-stationary, dK/dV key-stationary) that
+ *     each multiply S and dP; 14 d FLOPs per pair; bit-reproducible.
+ * dk and dv are bit-reproducible in both forms.  No counterpart on
+ * the pages (an implementation choice). */
+int sp_set_bwd_dq_reduction(int on);
 sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const void* v, const void* out,
                                 const void* dout, const float* lse, const int32_t* position_ids,
                                 int B, int S, int Hq, int Hkv, int d, int P, sp_block_order order,

@@ -30,7 +30,7 @@ EXPORTS = (
     "sp_blockwise_attn_fwd", "sp_blockwise_attn_step", "sp_blockwise_attn_fwd_noalloc",
     "sp_ring_block_step", "sp_query_block_attn_fwd",
     "sp_ulysses_ring_attn_workspace_bytes", "sp_ulysses_ring_attn_fwd",
-    "sp_blockwise_attn_bwd_workspace_bytes", "sp_blockwise_attn_bwd",
+    "sp_blockwise_attn_bwd_workspace_bytes", "sp_blockwise_attn_bwd", "sp_set_bwd_dq_reduction",
     "sp_attn_merge_partials",
     "sp_get_device_error", "sp_get_permute_error", "sp_permute_set_bulk_min_bytes",
     "sp_check_barrier_timeout",
@@ -78,6 +78,7 @@ def _load():
         "sp_get_device_error": (i, [vp, ctypes.POINTER(ctypes.c_int), vp]),
         "sp_get_permute_error": (i, [ctypes.POINTER(ctypes.c_int)]),
         "sp_permute_set_bulk_min_bytes": (sz, [sz]),
+        "sp_set_bwd_dq_reduction": (i, [i]),
         "sp_check_barrier_timeout": (i, [vp, i, vp]),
         "sp_last_launch_count": (i, []),
     }
@@ -303,6 +304,10 @@ def sp_get_permute_error():
 
 def sp_permute_set_bulk_min_bytes(min_bytes):
     return int(_lib.sp_permute_set_bulk_min_bytes(int(min_bytes)))
+
+
+def sp_set_bwd_dq_reduction(on):
+    return int(_lib.sp_set_bwd_dq_reduction(1 if on else 0))
 
 
 def sp_check_barrier_timeout(workspace, timeout_us, stream=None):

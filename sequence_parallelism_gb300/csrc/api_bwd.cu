@@ -10,6 +10,9 @@
 //   lo                            [B][P][Lbp] doc_start in block order (causal)
 //   doc_start                     [B][S] (causal only)
 //   scan scratch                  doc_start scan (causal only)
+//   dQ accumulator                fp32, B * Hq * P * Lbp * 128 floats (bf16
+//                                 path with dQ by reductions)
+#include <atomic>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -17,10 +20,15 @@
 #include "common.cuh"
 
 namespace sp {
+
+int launch_attn_bwd_bf16_fused(const BwdArgs& a, float* dq_acc, cudaStream_t st);
+
 namespace {
 
+std::atomic<int> g_bwd_dq_reduction{1};
+
 struct BwdLayout {
-  size_t dsum, lse2, lo, doc, scan, total;
+  size_t dsum, lse2, lo, doc, scan, acc, total;
   int Lbp;
 };
 
@@ -34,12 +42,17 @@ BwdLayout bwd_layout(int B, int S, int Hq, int P, int causal) {
   L.lo = causal ? round_up(static_cast<size_t>(B) * P * L.Lbp * sizeof(int32_t), 256) : 0;
   L.doc = causal ? round_up(static_cast<size_t>(B) * S * sizeof(int32_t), 256) : 0;
   L.scan = causal ? segment_scratch_bytes(B, S) : 0;
-  L.total = kWsHeaderBytes + L.dsum + L.lse2 + L.lo + L.doc + L.scan;
+  L.acc = round_up(static_cast<size_t>(B) * Hq * P * L.Lbp * 128 * sizeof(float), 256);
+  L.total = kWsHeaderBytes + L.dsum + L.lse2 + L.lo + L.doc + L.scan + L.acc;
   return L;
 }
 
 }  // namespace
 }  // namespace sp
+
+extern "C" int sp_set_bwd_dq_reduction(int on) {
+  return sp::g_bwd_dq_reduction.exchange(on ? 1 : 0);
+}
 
 extern "C" size_t sp_blockwise_attn_bwd_workspace_bytes(int B, int S, int Hq, int P,
                                                         int causal) {
@@ -114,7 +127,11 @@ extern "C" sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const v
     launches += n;
     a.doc_start = doc;
   }
-  const int n = dtype == SP_BF16 ? sp::launch_attn_bwd_bf16(a, st) : sp::launch_attn_bwd_simt(a, st);
+  float* dq_acc = reinterpret_cast<float*>(ws + sp::kWsHeaderBytes + L.dsum + L.lse2 + L.lo +
+                                            L.doc + L.scan);
+  const int n = dtype != SP_BF16 ? sp::launch_attn_bwd_simt(a, st)
+                : sp::g_bwd_dq_reduction.load() ? sp::launch_attn_bwd_bf16_fused(a, dq_acc, st)
+                                                : sp::launch_attn_bwd_bf16(a, st);
   if (n < 0) return SP_ERR_CUDA;
   sp::g_last_launches = launches + n;
   return SP_OK;

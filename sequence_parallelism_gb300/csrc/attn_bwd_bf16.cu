@@ -525,7 +525,7 @@ struct alignas(16) ColData {
   int lo[kQT];      // doc_start of the column's query (causal); INT_MAX past the end
   int info;         // kInfoEnd, kInfoTile (masked per pair) or kInfoFull (every pair allowed)
   int i, u0;        // query block and first local row of the tile
-  int pad;
+  int h;            // query head
 };
 
 // One CTA per 128-key tile (K, V resident).  Per 128-query tile:
@@ -641,6 +641,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               cd.info = (fulls >> e) & 1u ? kInfoFull : kInfoTile;
               cd.i = i;
               cd.u0 = u0;
+              cd.h = h;
               const uint32_t bar = smem_u32(&q_full[slot]);
               const uint32_t dst = sslot + slot * 2 * kTileBytes;
               mbar_arrive_expect_tx(bar, 2 * kTileBytes + col_bytes);
@@ -877,16 +878,546 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   }
 }
 
-}  // namespace
 
-// prep, then dQ and dK/dV (independent of each other) on the tensor cores.
-int launch_attn_bwd_bf16(const BwdArgs& a, cudaStream_t st) {
-  BwdMaps tm;  // 128-row boxes for both kernels
+// ------------------------------------------------------ fused dK/dV + dQ
+// The dK/dV walk with dQ folded in, so that S^T and dP^T are multiplied once
+// per pair of tiles (10 d FLOPs per allowed pair instead of 14 d for the two
+// kernels above).  dS^T goes to shared memory instead of tensor memory: read
+// as a K-major operand it is the A of dK += dS^T Q, read MN-major it is the A
+// of dQ_tile = dS K.  dQ_tile (128 queries x 128 columns, fp32) lands in the
+// tensor-memory columns dP^T held; the elementwise warps read it and stage it
+// in shared memory, and the TMA adds it into an fp32 accumulator in global
+// memory (bulk reductions); bwd_dq_convert_kernel scales and rounds the sums
+// to bf16.  The reductions arrive in no fixed order, so dQ is reproducible to fp32 rounding, not bit
+// for bit (the two-kernel path is).
+constexpr int kFThreads = 224;  // warps 0-3 elementwise, 4 TMA, 5 MMA, 6 dQ reductions
+constexpr int kFProducer = 4;
+constexpr int kFMma = 5;
+constexpr int kFReducer = 6;
+constexpr int kFSmemBytes = 6 * kTileBytes;  // K, V, Q slots 0 and 1, dO, dS^T
+// A and B MN-major: dQ_tile = dS K reads dS from the key-row-major dS^T
+// buffer and K from its key-row-major tile.
+constexpr uint32_t kIdescAmnBmn = kIdescBmn | (1u << 15);
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
+                                       uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z),
+               "r"(w)
+               : "memory");
+}
+
+// dst[i] += src[i] for `bytes` / 4 floats, by the TMA unit (bulk group of the
+// issuing thread; both addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                   dst),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
+
+
+// One CTA per 128-key tile, walking the query tiles like bwd_dkdv_kernel.
+// Per 128-query tile t:
+//   S^T = K Q^T, dP^T = V dO^T                (SS, TMEM [0,128) / [128,256))
+//   two 64-column halves: P^T (bf16 pairs) over S^T columns [32h, 32h+32),
+//     dS^T (bf16) to the shared-memory buffer
+//   dV += P^T dO (TS), dK += dS^T Q (SS)        half 0 while half 1 is computed
+//   dQ_tile = dS K (SS, TMEM [128,256)) -> elementwise warps -> shared memory
+//     (Q_t's slot and the dS^T buffer, both free once dQ_tile is complete)
+//     -> two 32 KiB TMA bulk reductions into the global fp32 sums
+// dO has one slot (released after the last dV product, reloaded while dK,
+// dQ and the next S^T run); dP^T of the next tile waits until dQ_tile has
+// been read out of tensor memory.  The reducer warp issues the two bulk
+// reductions and, as the TMA finishes reading them, releases the dS^T buffer
+// (to the next tile's dS^T stores) and Q_t's slot (to the producer, for
+// Q_{t+2}), so the reductions drain while the next tile is computed.
+//
+// dQ accumulator layout: per (batch, query head, block, 128-row tile) a
+// 64 KiB block ordered [column quad 32][row 128][4]: staged in the same
+// order, its two halves are two contiguous bulk reductions, and a warp's
+// shared-memory stores cover 512 contiguous bytes.
+__global__ void __launch_bounds__(kFThreads, 1)
+    bwd_fused_kernel(const __grid_constant__ BwdMaps tm, BwdArgs a, int n_tiles_k,
+                     float* __restrict__ dq_acc) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t q_full[kQSlots], q_empty[kQSlots], do_full, do_empty, kv_full, s_full,
+      half_full[2], dq_full, dq_free, stage_full, stage_free, dkv_full, done;
+  __shared__ ColData cols[kQSlots];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sk = smem_u32(smem), sv = sk + kTileBytes, sq = sk + 2 * kTileBytes;
+  const uint32_t sdo = sk + 4 * kTileBytes, sds = sk + 5 * kTileBytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int BH = a.B * a.Hkv;
+  const int pos = blockIdx.x / BH, bh = blockIdx.x % BH;
+  const int b = bh / a.Hkv, hk = bh % a.Hkv;
+  const int j = pos / n_tiles_k, kt = pos % n_tiles_k;
+  const int Lb = a.S / a.P, w0 = kt * kT;
+  const int k_first = static_cast<int>(block_token(a.order, a.S, a.P, j, w0));
+  const int k_last = static_cast<int>(block_token(a.order, a.S, a.P, j, min(w0 + kT, Lb) - 1));
+  const int32_t* ds_row =
+      a.doc_start ? a.doc_start + static_cast<long long>(b % a.pos_rows) * a.S : nullptr;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQSlots; ++s) {
+      mbar_init(smem_u32(&q_full[s]), 1);
+      mbar_init(smem_u32(&q_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&do_full), 1);
+    mbar_init(smem_u32(&do_empty), 1);
+    mbar_init(smem_u32(&kv_full), 1);
+    mbar_init(smem_u32(&s_full), 1);
+    mbar_init(smem_u32(&half_full[0]), kT);
+    mbar_init(smem_u32(&half_full[1]), kT);
+    mbar_init(smem_u32(&dq_full), 1);
+    mbar_init(smem_u32(&dq_free), kT);
+    mbar_init(smem_u32(&stage_full), kT);
+    mbar_init(smem_u32(&stage_free), 1);
+    mbar_init(smem_u32(&dkv_full), 1);
+    mbar_init(smem_u32(&done), 1);
+    abort_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == kFMma) {
+    tmem_alloc(smem_u32(&tmem_base_s), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  volatile int* abort_flag = &abort_s;
+  // TMEM columns: S^T [0,128), dP^T then dQ_tile [128,256), dV [256,384), dK [384,512)
+  const uint32_t cdP = 128, cdQ = 128, cdV = 256, cdK = 384;
+
+  if (warp == kFProducer) {
+    // ------------------------------------------------------------ producer
+    const int G = a.Hq / a.Hkv;
+    if (lane == 0) {
+      prefetch_tmap(&tm.k);
+      prefetch_tmap(&tm.v);
+      prefetch_tmap(&tm.q);
+      prefetch_tmap(&tm.dout);
+      const uint32_t kf = smem_u32(&kv_full);
+      mbar_arrive_expect_tx(kf, 2 * kTileBytes);
+      row_tma(sk, &tm.k, kf, hk, a.order, j, w0, b);
+      row_tma(sv, &tm.v, kf, hk, a.order, j, w0, b);
+    }
+    const long long lo_row = static_cast<long long>(b % a.pos_rows);
+    const uint32_t col_bytes = (ds_row ? 3 : 2) * kQT * 4;
+    int n = 0, n_do = 0;  // Q tiles and dO tiles issued
+    bool ok = true, ended = false;
+    for (int g = 0; g < G && ok; ++g) {
+      const int h = hk * G + g;
+      const long long bhq = static_cast<long long>(b) * a.Hq + h;
+      for (int s = 0; s < a.P && ok; ++s) {
+        const int i = (j + s) % a.P;
+        int qt0, qt1;
+        block_tiles(a.order, a.S, a.P, i, ds_row ? k_first : 0, a.S - 1, kQT, qt0, qt1);
+        for (int base = qt0; base <= qt1 && ok; base += 32) {
+          const int qt = base + lane;
+          bool stop = false, full = true;
+          if (ds_row && qt <= qt1) {
+            const int u0 = qt * kQT;
+            const int tq_first = static_cast<int>(block_token(a.order, a.S, a.P, i, u0));
+            const int tq_last =
+                static_cast<int>(block_token(a.order, a.S, a.P, i, min(u0 + kQT, Lb) - 1));
+            stop = ds_row[tq_first] > k_last;
+            full = k_last <= tq_first && ds_row[tq_last] <= k_first;
+          }
+          const unsigned stops = __ballot_sync(0xffffffffu, stop);
+          const unsigned fulls = __ballot_sync(0xffffffffu, full);
+          int cnt = min(32, qt1 - base + 1);
+          if (stops) cnt = min(cnt, __ffs(static_cast<int>(stops)) - 1);
+          for (int e = 0; e < cnt; ++e) {
+            const int slot = n % kQSlots;
+            if (!wait_warp(smem_u32(&q_empty[slot]), ((n / kQSlots) & 1) ^ 1, abort_flag, a.err,
+                           kErrBwdKvEmpty)) {
+              ok = false;
+              break;
+            }
+            const int u0 = (base + e) * kQT;
+            if (lane == 0) {
+              ColData& cd = cols[slot];
+              cd.info = (fulls >> e) & 1u ? kInfoFull : kInfoTile;
+              cd.i = i;
+              cd.u0 = u0;
+              cd.h = h;
+              const uint32_t bar = smem_u32(&q_full[slot]);
+              mbar_arrive_expect_tx(bar, kTileBytes + col_bytes);
+              row_tma(sq + slot * kTileBytes, &tm.q, bar, h, a.order, i, u0, b);
+              const long long off = blk_index(bhq, a.P, a.Lbp, i, u0);
+              bulk_load(smem_u32(cd.lse2), a.lse2_blk + off, kQT * 4, bar);
+              bulk_load(smem_u32(cd.D), a.D_blk + off, kQT * 4, bar);
+              if (ds_row)
+                bulk_load(smem_u32(cd.lo), a.lo_blk + blk_index(lo_row, a.P, a.Lbp, i, u0),
+                          kQT * 4, bar);
+            }
+            ++n;
+            if (!wait_warp(smem_u32(&do_empty), (n_do & 1) ^ 1, abort_flag, a.err,
+                           kErrBwdKvEmpty)) {
+              ok = false;
+              break;
+            }
+            if (lane == 0) {
+              const uint32_t bar = smem_u32(&do_full);
+              mbar_arrive_expect_tx(bar, kTileBytes);
+              row_tma(sdo, &tm.dout, bar, h, a.order, i, u0, b);
+            }
+            ++n_do;
+          }
+          if (stops) break;
+        }
+      }
+    }
+    if (ok) {  // end of the list
+      const int slot = n % kQSlots;
+      if (wait_warp(smem_u32(&q_empty[slot]), ((n / kQSlots) & 1) ^ 1, abort_flag, a.err,
+                    kErrBwdKvEmpty)) {
+        ended = true;
+        if (lane == 0) {
+          cols[slot].info = kInfoEnd;
+          mbar_arrive(smem_u32(&q_full[slot]));
+        }
+      }
+    }
+    // copies still in flight land before the CTA can exit: K/V, the last dO,
+    // the last Q tile, and the one before it unless the end marker's wait
+    // for its slot already saw it consumed
+    if (lane == 0) {
+      mbar_wait(smem_u32(&kv_full), 0, abort_flag, a.err, kErrBwdDrain);
+      if (n_do > 0)
+        mbar_wait(smem_u32(&do_full), (n_do - 1) & 1, abort_flag, a.err, kErrBwdDrain);
+      for (int m = n - 1; m >= 0 && m > n - 1 - (ended ? 1 : kQSlots); --m)
+        mbar_wait(smem_u32(&q_full[m % kQSlots]), (m / kQSlots) & 1, abort_flag, a.err,
+                  kErrBwdDrain);
+    }
+    __syncwarp();
+  } else if (warp == kFMma) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint64_t dk0 = smem_desc_sw128(sk, 16, 1024), dv0 = smem_desc_sw128(sv, 16, 1024);
+      const uint64_t dkq = smem_desc_sw128(sq, 16, 1024);          // K-major Q views
+      const uint64_t dqmn = smem_desc_sw128(sq, kHalfBytes, 1024);  // MN-major Q views
+      const uint64_t ddo = smem_desc_sw128(sdo, 16, 1024);          // K-major dO
+      const uint64_t ddomn = smem_desc_sw128(sdo, kHalfBytes, 1024);
+      const uint64_t dds = smem_desc_sw128(sds, 16, 1024);            // dS^T, K-major
+      const uint64_t ddsmn = smem_desc_sw128(sds, kHalfBytes, 1024);  // dS, MN-major
+      const uint64_t dkmn = smem_desc_sw128(sk, kHalfBytes, 1024);    // K, MN-major
+      auto tile_info = [&](int t) -> int {
+        const int slot = t % kQSlots;
+        if (!wait_ready(smem_u32(&q_full[slot]), (t / kQSlots) & 1, abort_flag, a.err,
+                        kErrBwdQFull))
+          return -1;
+        return cols[slot].info;
+      };
+      // S^T = K Q^T for tile t
+      auto issue_s = [&](int t) {
+        tc_fence_after();
+        const uint64_t qb = dkq + (((t % kQSlots) * kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem, kmaj_desc(dk0, kk), kmaj_desc(qb, kk), kIdescKmaj, kk > 0 ? 1u : 0u);
+      };
+      // dP^T = V dO^T for tile t (its dO has landed), then publish S^T, dP^T
+      auto issue_dp = [&]() {
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + cdP, kmaj_desc(dv0, kk), kmaj_desc(ddo, kk), kIdescKmaj, kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&s_full));
+      };
+      auto issue_dv = [&](int t, int h) {
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = h * 4 + k4;  // 16-query step within the tile
+          mma_ts(tmem + cdV, tmem + kk * 8, ddomn + ((kk * 16 * 128) >> 4), kIdescBmn,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      auto issue_dk = [&](int t, int h) {
+        const uint64_t qb = dqmn + (((t % kQSlots) * kTileBytes) >> 4);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = h * 4 + k4;
+          mma_ss(tmem + cdK, kmaj_desc(dds, kk), qb + ((kk * 16 * 128) >> 4), kIdescBmn,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      // dQ_tile = dS K over the 128 keys (16 per step)
+      auto issue_dq = [&]() {
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_ss(tmem + cdQ, ddsmn + ((kk * 16 * 128) >> 4), dkmn + ((kk * 16 * 128) >> 4),
+                 kIdescAmnBmn, kk > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&dq_full));
+      };
+      bool ok = mbar_wait(smem_u32(&kv_full), 0, abort_flag, a.err, kErrBwdKvFull);
+      int cur = ok ? tile_info(0) : -1;
+      if (cur > 0) {
+        issue_s(0);
+        if (wait_ready(smem_u32(&do_full), 0, abort_flag, a.err, kErrBwdQFull))
+          issue_dp();
+        else
+          cur = -1;
+      }
+      for (int t = 0; cur > 0; ++t) {
+        if (!mbar_wait(smem_u32(&half_full[0]), t & 1, abort_flag, a.err, kErrBwdDsFull)) break;
+        tc_fence_after();
+        issue_dv(t, 0);
+        issue_dk(t, 0);
+        if (!mbar_wait(smem_u32(&half_full[1]), t & 1, abort_flag, a.err, kErrBwdDsFull)) break;
+        tc_fence_after();
+        issue_dv(t, 1);
+        mma_commit(smem_u32(&do_empty));  // dO_t consumed
+        issue_dk(t, 1);
+        issue_dq();  // Q_t's slot is released by the elementwise warps (dQ staging)
+        const int nxt = tile_info(t + 1);
+        if (nxt > 0) {
+          issue_s(t + 1);
+          if (!wait_ready(smem_u32(&dq_free), t & 1, abort_flag, a.err, kErrBwdSFree) ||
+              !wait_ready(smem_u32(&do_full), (t + 1) & 1, abort_flag, a.err, kErrBwdQFull))
+            break;
+          issue_dp();
+        }
+        cur = nxt;
+      }
+      mma_commit(smem_u32(&dkv_full));
+      mma_commit(smem_u32(&done));
+      mbar_wait(smem_u32(&done), 0, abort_flag, a.err, kErrBwdDrain);
+    }
+    __syncwarp();
+  } else if (warp == kFReducer) {
+    // ------------------------------------------------------ dQ reductions
+    if (lane == 0) {
+      for (int t = 0;; ++t) {
+        const int slot = t % kQSlots;
+        // Q_t's column data stays put until this thread releases the slot
+        if (!mbar_wait(smem_u32(&q_full[slot]), (t / kQSlots) & 1, abort_flag, a.err,
+                       kErrBwdQFull))
+          break;
+        const ColData& cd = cols[slot];
+        if (cd.info == kInfoEnd) break;
+        const long long bhq = static_cast<long long>(b) * a.Hq + cd.h;
+        float* blk = dq_acc + blk_index(bhq, a.P, a.Lbp, cd.i, cd.u0) * kD;
+        if (!mbar_wait(smem_u32(&stage_full), t & 1, abort_flag, a.err, kErrBwdOut)) break;
+        // the dS^T half first: the next tile's dS^T stores need that buffer
+        // soonest; Q_t's slot is needed again only for Q_{t+2}
+        bulk_reduce_add_f32(blk + kTileBytes / 4, sds, kTileBytes);
+        bulk_commit_group();
+        bulk_reduce_add_f32(blk, sq + slot * kTileBytes, kTileBytes);
+        bulk_commit_group();
+        bulk_wait_group_read<1>();
+        mbar_arrive(smem_u32(&stage_free));
+        bulk_wait_group_read0();
+        mbar_arrive(smem_u32(&q_empty[slot]));
+      }
+      bulk_wait_group0();  // the last reductions are complete
+    }
+    __syncwarp();
+  } else {
+    // --------------------------------------------------- elementwise warps
+    const int r = threadIdx.x;  // TMEM lane: key row of S^T / dP^T, query row of dQ_tile
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int w = w0 + r;
+    const bool key_live = w < Lb;
+    const int ktok = key_live ? static_cast<int>(block_token(a.order, a.S, a.P, j, w)) : -1;
+    const float sl2 = a.scale * kLog2e;
+    const uint32_t ds_row_addr = sds + r * 128;
+    const uint32_t swz = static_cast<uint32_t>(r & 7);
+    int t = 0;
+    bool ok = true;
+    for (;; ++t) {
+      const int slot = t % kQSlots;
+      if (!wait_warp(smem_u32(&q_full[slot]), (t / kQSlots) & 1, abort_flag, a.err,
+                     kErrBwdQFull)) {
+        ok = false;
+        break;
+      }
+      const ColData& cd = cols[slot];
+      const int info = cd.info;
+      if (info == kInfoEnd) break;
+      const int ti = cd.i, tu0 = cd.u0;
+      if (!wait_warp(smem_u32(&s_full), t & 1, abort_flag, a.err, kErrBwdSFull)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool full = info == kInfoFull;
+      int c_min = 0;
+      if (!full) {
+        c_min = a.order == SP_ORDER_STRIPED ? -floor_div_i(-(ktok - ti), a.P) - tu0
+                                            : ktok - (ti * Lb + tu0);
+      }
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sx[64], px[64];
+        tmem_ld32_at(tmem + lane_base + h * 64, sx, 0);
+        tmem_ld32_at(tmem + lane_base + h * 64 + 32, sx, 32);
+        tmem_ld32_at(tmem + lane_base + cdP + h * 64, px, 0);
+        tmem_ld32_at(tmem + lane_base + cdP + h * 64 + 32, px, 32);
+        tmem_wait_ld();
+        if (!full) {
+#pragma unroll
+          for (int c4 = 0; c4 < 64; c4 += 4) {
+            const int c = h * 64 + c4;
+            const int4 lo = *reinterpret_cast<const int4*>(&cd.lo[c]);
+            if (c < c_min || lo.x > ktok) sx[c4] = 0xff800000u;
+            if (c + 1 < c_min || lo.y > ktok) sx[c4 + 1] = 0xff800000u;
+            if (c + 2 < c_min || lo.z > ktok) sx[c4 + 2] = 0xff800000u;
+            if (c + 3 < c_min || lo.w > ktok) sx[c4 + 3] = 0xff800000u;
+          }
+        }
+        uint32_t pk[32], dk[32];
+#pragma unroll
+        for (int c4 = 0; c4 < 64; c4 += 4) {
+          const int c = h * 64 + c4;
+          const float4 l2 = *reinterpret_cast<const float4*>(&cd.lse2[c]);
+          const float4 D = *reinterpret_cast<const float4*>(&cd.D[c]);
+          float x0, x1, x2, x3;
+          ffma2(x0, x1, __uint_as_float(sx[c4]), __uint_as_float(sx[c4 + 1]), sl2, sl2, -l2.x,
+                -l2.y);
+          ffma2(x2, x3, __uint_as_float(sx[c4 + 2]), __uint_as_float(sx[c4 + 3]), sl2, sl2, -l2.z,
+                -l2.w);
+          const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+          float d0, d1, d2, d3;
+          fadd2(d0, d1, __uint_as_float(px[c4]), __uint_as_float(px[c4 + 1]), -D.x, -D.y);
+          fadd2(d2, d3, __uint_as_float(px[c4 + 2]), __uint_as_float(px[c4 + 3]), -D.z, -D.w);
+          fmul2(d0, d1, d0, d1, p0, p1);
+          fmul2(d2, d3, d2, d3, p2, p3);
+          pk[c4 >> 1] = pack_bf16(p0, p1);
+          pk[(c4 >> 1) + 1] = pack_bf16(p2, p3);
+          dk[c4 >> 1] = pack_bf16(d0, d1);
+          dk[(c4 >> 1) + 1] = pack_bf16(d2, d3);
+        }
+        // P^T of half h as 32 bf16-pair columns (S^T columns [32h, 32h + 32)
+        // were read in half 0); dS^T row r, queries [64h, 64h + 64): one
+        // 128-byte row of the half's swizzled 16 KiB block
+        tmem_st32(tmem + lane_base + h * 32, pk);
+        if (h == 0 && t > 0) {
+          // the dS^T buffer held half of dQ_{t-1} until the TMA read it
+          if (!wait_warp(smem_u32(&stage_free), (t - 1) & 1, abort_flag, a.err, kErrBwdOut)) {
+            ok = false;
+            break;
+          }
+        }
+        const uint32_t row = ds_row_addr + h * kHalfBytes;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          sts128(row + ((static_cast<uint32_t>(c) ^ swz) << 4), dk[4 * c], dk[4 * c + 1],
+                 dk[4 * c + 2], dk[4 * c + 3]);
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&half_full[h]));
+      }
+      if (!ok) break;
+      // dQ_tile: this thread's query row, 128 fp32 columns
+      if (!wait_warp(smem_u32(&dq_full), t & 1, abort_flag, a.err, kErrBwdOut)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t x[128];
+      tmem_ld32_at(tmem + lane_base + cdQ, x, 0);
+      tmem_ld32_at(tmem + lane_base + cdQ + 32, x, 32);
+      tmem_ld32_at(tmem + lane_base + cdQ + 64, x, 64);
+      tmem_ld32_at(tmem + lane_base + cdQ + 96, x, 96);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&dq_free));
+      // stage: column quads 0..15 in Q_t's slot, 16..31 in the dS^T buffer
+      // (free: every product that read them is complete)
+      const uint32_t stage0 = sq + slot * kTileBytes + r * 16, stage1 = sds + r * 16;
+#pragma unroll
+      for (int q4 = 0; q4 < 32; ++q4)
+        sts128((q4 < 16 ? stage0 : stage1) + (q4 & 15) * (kQT * 16), x[4 * q4], x[4 * q4 + 1],
+               x[4 * q4 + 2], x[4 * q4 + 3]);
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&stage_full));
+    }
+    // epilogue: dK * scale and dV, rows of key token ktok
+    const bool have = t > 0 && ok;
+    if (have && !wait_warp(smem_u32(&dkv_full), 0, abort_flag, a.err, kErrBwdOut)) ok = false;
+    tc_fence_after();
+    const long long orow =
+        ((static_cast<long long>(b) * a.S + (key_live ? ktok : 0)) * a.Hkv + hk) * kD;
+    uint4* dk_row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk) + orow);
+    uint4* dv_row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dv) + orow);
+#pragma unroll 1
+    for (int m = 0; m < 2; ++m) {
+      const float mul = m == 0 ? a.scale : 1.f;
+      uint4* dst = m == 0 ? dk_row : dv_row;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t x[32];
+        if (have && ok) {
+          tmem_ld32(tmem + lane_base + (m == 0 ? cdK : cdV) + c * 32, x);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16(__uint_as_float(x[2 * e]) * mul, __uint_as_float(x[2 * e + 1]) * mul);
+        if (key_live) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[c * 4 + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kFMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// dq = scale * (the fp32 sums), bf16, in [B][S][Hq][d].  One CTA per 64 KiB
+// accumulator block (128 rows of one block and head): thread (row r, half
+// g0) writes 16-byte pieces of row r's 256 output bytes; the reads of a warp
+// cover 512 contiguous bytes.
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __restrict__ acc,
+                                                             __nv_bfloat16* dq, int S, int Hq,
+                                                             int P, int Lbp, int order,
+                                                             float scale) {
+  const int tiles = Lbp / kQT;
+  const long long blk = blockIdx.x;  // ((b * Hq + h) * P + i) * tiles + tile
+  const int tile = static_cast<int>(blk % tiles);
+  const long long bhp = blk / tiles;
+  const int i = static_cast<int>(bhp % P);
+  const long long bh = bhp / P;
+  const int h = static_cast<int>(bh % Hq);
+  const long long b = bh / Hq;
+  const int r = threadIdx.x & (kQT - 1), g0 = threadIdx.x >> 7;
+  const int u = tile * kQT + r;
+  if (u >= S / P) return;
+  const long long t = block_token(order, S, P, i, u);
+  const float4* src = acc + blk * (kQT * kD / 4) + r;
+  uint4* dst = reinterpret_cast<uint4*>(dq + ((b * S + t) * Hq + h) * kD);
+#pragma unroll 4
+  for (int g = g0; g < kD / 8; g += 2) {  // 8 columns: quads 2g and 2g + 1
+    const float4 lo = src[(2 * g) * kQT], hi = src[(2 * g + 1) * kQT];
+    dst[g] = make_uint4(pack_bf16(lo.x * scale, lo.y * scale), pack_bf16(lo.z * scale, lo.w * scale),
+                        pack_bf16(hi.x * scale, hi.y * scale), pack_bf16(hi.z * scale, hi.w * scale));
+  }
+}
+
+// Tensor maps and the prep kernel, shared by both backward forms.
+bool launch_prep(const BwdArgs& a, BwdMaps& tm, cudaStream_t st) {
   if (!tmap::make_map(&tm.q, a.q, a.B, a.S, a.Hq, a.P, a.order) ||
       !tmap::make_map(&tm.dout, a.dout, a.B, a.S, a.Hq, a.P, a.order) ||
       !tmap::make_map(&tm.k, a.k, a.B, a.S, a.Hkv, a.P, a.order) ||
       !tmap::make_map(&tm.v, a.v, a.B, a.S, a.Hkv, a.P, a.order))
-    return -1;
+    return false;
   const int Lb = a.S / a.P;
   PrepArgs pa;
   pa.out = static_cast<const uint4*>(a.out);
@@ -907,7 +1438,16 @@ int launch_attn_bwd_bf16(const BwdArgs& a, cudaStream_t st) {
   pa.order = a.order;
   const long long n_prep = pa.nA + pa.nB + pa.nC;
   bwd_prep_kernel<<<static_cast<unsigned>((n_prep + 255) / 256), 256, 0, st>>>(pa);
-  const int n_tiles = (Lb + kT - 1) / kT;
+  return true;
+}
+
+}  // namespace
+
+// prep, then dQ and dK/dV (independent of each other) on the tensor cores.
+int launch_attn_bwd_bf16(const BwdArgs& a, cudaStream_t st) {
+  BwdMaps tm;  // 128-row boxes for both kernels
+  if (!launch_prep(a, tm, st)) return -1;
+  const int n_tiles = (a.S / a.P + kT - 1) / kT;
   const int dq_smem = kQSmemBytes + 1024, kv_smem = kKvSmemBytes + 1024;
   if (cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem) !=
           cudaSuccess ||
@@ -918,6 +1458,29 @@ int launch_attn_bwd_bf16(const BwdArgs& a, cudaStream_t st) {
   bwd_dq_kernel<<<n_q, kQThreads, dq_smem, st>>>(tm, a, n_tiles);
   const unsigned n_kv = static_cast<unsigned>(a.P) * n_tiles * a.B * a.Hkv;
   bwd_dkdv_kernel<<<n_kv, kKvThreads, kv_smem, st>>>(tm, a, n_tiles);
+  return cudaGetLastError() == cudaSuccess ? 3 : -1;
+}
+
+// prep, the fused kernel into a zeroed fp32 dQ accumulator
+// (B * Hq * P * Lbp * 128 floats), then dq from the accumulator.
+int launch_attn_bwd_bf16_fused(const BwdArgs& a, float* dq_acc, cudaStream_t st) {
+  BwdMaps tm;
+  const size_t acc_bytes =
+      static_cast<size_t>(a.B) * a.Hq * a.P * a.Lbp * kD * sizeof(float);
+  if (cudaMemsetAsync(dq_acc, 0, acc_bytes, st) != cudaSuccess) return -1;
+  if (!launch_prep(a, tm, st)) return -1;
+  const int n_tiles = (a.S / a.P + kT - 1) / kT;
+  const int f_smem = kFSmemBytes + 1024;
+  if (cudaFuncSetAttribute(bwd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           f_smem) != cudaSuccess)
+    return -1;
+  const unsigned n_kv = static_cast<unsigned>(a.P) * n_tiles * a.B * a.Hkv;
+  bwd_fused_kernel<<<n_kv, kFThreads, f_smem, st>>>(tm, a, n_tiles, dq_acc);
+  const unsigned n_blk = static_cast<unsigned>(static_cast<long long>(a.B) * a.Hq * a.P *
+                                               (a.Lbp / kQT));
+  bwd_dq_convert_kernel<<<n_blk, 256, 0, st>>>(reinterpret_cast<const float4*>(dq_acc),
+                                                static_cast<__nv_bfloat16*>(a.dq), a.S, a.Hq,
+                                                a.P, a.Lbp, a.order, a.scale);
   return cudaGetLastError() == cudaSuccess ? 3 : -1;
 }
 

@@ -181,3 +181,24 @@ def test_permutation_threshold_setting_round_trips(lib):
     lib.sp_permute_set_bulk_min_bytes.argtypes = [ctypes.c_size_t]
     prev = lib.sp_permute_set_bulk_min_bytes(12345)
     assert lib.sp_permute_set_bulk_min_bytes(prev) == 12345
+
+
+def test_backward_dq_form_setting_round_trips(lib):
+    lib.sp_set_bwd_dq_reduction.restype = ctypes.c_int
+    lib.sp_set_bwd_dq_reduction.argtypes = [ctypes.c_int]
+    prev = lib.sp_set_bwd_dq_reduction(0)
+    assert prev == 1                              # dQ by reductions is the default
+    assert lib.sp_set_bwd_dq_reduction(7) == 0    # any non-zero value means on
+    assert lib.sp_set_bwd_dq_reduction(prev) == 1
+
+
+def test_backward_workspace_holds_the_dq_accumulator(lib):
+    """The backward workspace includes the float32 dQ accumulator: B * Hq * P
+    * Lbp * 128 floats, Lbp = S/P rounded up to a multiple of 128."""
+    lib.sp_blockwise_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.sp_blockwise_attn_bwd_workspace_bytes.argtypes = [ctypes.c_int] * 5
+    for B, S, Hq, P, causal in [(1, 32768, 32, 8, 1), (2, 1000, 4, 2, 0), (1, 1416, 4, 3, 1)]:
+        Lbp = -(-(S // P) // 128) * 128
+        acc = B * Hq * P * Lbp * 128 * 4
+        assert lib.sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, P, causal) >= acc
+    assert lib.sp_blockwise_attn_bwd_workspace_bytes(1, 1000, 4, 3, 0) == 0   # S % P != 0

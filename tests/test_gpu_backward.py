@@ -20,6 +20,16 @@ def sp():
     return m
 
 
+@pytest.fixture(params=["dq_reduction", "dq_recompute"])
+def dq_form(request):
+    """Both forms of the bf16 backward: dQ summed by reductions in the fused
+    kernel (the default) and dQ recomputed by its own kernel."""
+    from sequence_parallelism_gb300 import _lib
+    prev = _lib.sp_set_bwd_dq_reduction(request.param == "dq_reduction")
+    yield request.param
+    _lib.sp_set_bwd_dq_reduction(prev)
+
+
 def _run_bwd(sp, dtype, B, S, Hq, Hkv, d, P, order, pos_kind, seed):
     q, k, v = workloads.small_case(B, S, Hq, Hkv, d, seed, dtype)
     g = torch.Generator(device="cuda")
@@ -55,7 +65,7 @@ def test_backward_f32(sp, B, S, Hq, Hkv, d, P, order, pos):
     (1, 2048, 8, 2, 4, "contiguous", "packed"),     # GQA group of 4, documents across blocks
     (1, 1416, 4, 4, 3, "striped", "causal"),        # ragged tiles: blocks of 472 rows
 ])
-def test_backward_bf16(sp, B, S, Hq, Hkv, P, order, pos):
+def test_backward_bf16(sp, dq_form, B, S, Hq, Hkv, P, order, pos):
     _run_bwd(sp, "bf16", B, S, Hq, Hkv, 128, P, order, pos, 850 + S)
 
 
@@ -65,7 +75,7 @@ def test_backward_bf16(sp, B, S, Hq, Hkv, P, order, pos):
     ("f32", 1, 1, 1, 1, 1, "contiguous", "none"),
     ("f32", 1, 64, 2, 1, 64, "striped", "packed"),
 ])
-def test_backward_degenerate_shapes(sp, dtype, B, S, Hq, Hkv, P, order, pos):
+def test_backward_degenerate_shapes(sp, dq_form, dtype, B, S, Hq, Hkv, P, order, pos):
     _run_bwd(sp, dtype, B, S, Hq, Hkv, 128 if dtype == "bf16" else 16, P, order, pos,
              950 + S + P)
 

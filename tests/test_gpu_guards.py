@@ -178,7 +178,8 @@ def test_doc_starts_writes_stay_inside():
     ("bf16", "striped", "packed"),
     ("f32", "contiguous", "none"),
 ])
-def test_backward_writes_stay_inside(sp, dtype, order, pos_kind):
+@pytest.mark.parametrize("dq_reduction", [True, False])
+def test_backward_writes_stay_inside(sp, dq_reduction, dtype, order, pos_kind):
     B, S, Hq, Hkv, P = 1, 640 if dtype == "bf16" else 96, 4, 2, 2
     d = 128 if dtype == "bf16" else 32
     q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 760, dtype)
@@ -190,9 +191,13 @@ def test_backward_writes_stay_inside(sp, dtype, order, pos_kind):
     out, lse = sp.blockwise_attention(q, k, v, P, order, tpos)
     dq, dk, dv = (Guarded(t.shape, t.dtype) for t in (q, k, v))
     ws = _workspace(_lib.sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, P, tpos is not None))
-    _lib.sp_blockwise_attn_bwd(q, k, v, out, dout, lse, tpos, P, order, 0.0, dq.t, dk.t, dv.t,
-                               ws.t)
-    what = f"backward {dtype} {order} {pos_kind}"
+    prev = _lib.sp_set_bwd_dq_reduction(dq_reduction)
+    try:
+        _lib.sp_blockwise_attn_bwd(q, k, v, out, dout, lse, tpos, P, order, 0.0, dq.t, dk.t, dv.t,
+                                   ws.t)
+    finally:
+        _lib.sp_set_bwd_dq_reduction(prev)
+    what = f"backward {dtype} {order} {pos_kind} dq_reduction={dq_reduction}"
     _assert_guarded(what, ("dq", dq), ("dk", dk), ("dv", dv), ("workspace", ws))
     _no_nan(what, dq=dq.t, dk=dk.t, dv=dv.t)
     rq, rk, rv = oracle.attention_backward(np32(q), np32(k), np32(v), np32(dout), pos)
