@@ -664,9 +664,13 @@ def next_row_measurements(peaks, flush, stream):
 
 
 def backward_measurement(peaks, flush, stream, reps=20):
-    """Attention backward (dq, dk, dv) on llama8b_32k: prep + dQ + dK/dV
-    kernels, L2 flushed between reps.  Algorithmic FLOPs = 2.5 x the
-    forward's (five d-long products per allowed pair: S, dP, dV, dQ, dK)."""
+    """Attention backward (dq, dk, dv) on llama8b_32k, L2 flushed between
+    reps, in both forms: the default (doc_start scan, prep, the fused
+    kernel -- S^T and dP^T once per pair of tiles, dQ pieces summed by TMA
+    bulk reductions -- and the dq conversion) and the bit-reproducible
+    two-kernel form (dQ recomputed by its own kernel).  Algorithmic FLOPs =
+    2.5 x the forward's (five d-long products per allowed pair: S, dP, dV,
+    dQ, dK)."""
     import torch
 
     import sequence_parallelism_gb300 as sp
@@ -687,15 +691,30 @@ def backward_measurement(peaks, flush, stream, reps=20):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     call = lambda: _lib.sp_blockwise_attn_bwd(q, k, v, out, dout, lse, pos, P, "contiguous", 0.0,
                                               dq, dk, dv, ws)
-    t, _, clocks = _timed(call, flush, stream, reps)
-    launches = _lib.sp_last_launch_count()
     fl = 2.5 * attention_flops(cfg, pos_np)
-    tf = fl / (t * 1e-3) / 1e12
-    return {"ms": round(t, 4), "TFLOP/s": round(tf, 1),
-            "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4), "flops": fl,
-            "reps": reps, "launches_per_call": launches, "clocks": clocks,
-            "note": "doc_start scan + prep + dQ + dK/dV kernels, median of reps; "
-                    "flops = 2.5 x forward (S, dP, dV, dQ, dK)"}
+
+    def one(form_reduction):
+        prev = _lib.sp_set_bwd_dq_reduction(form_reduction)
+        try:
+            t, _, clocks = _timed(call, flush, stream, reps)
+            launches = _lib.sp_last_launch_count()
+        finally:
+            _lib.sp_set_bwd_dq_reduction(prev)
+        tf = fl / (t * 1e-3) / 1e12
+        return {"ms": round(t, 4), "TFLOP/s": round(tf, 1),
+                "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+                "frac_of_sustained_bf16_peak": (round(tf / peaks["bf16_tflops_sustained"], 4)
+                                                if peaks.get("bf16_tflops_sustained") else None),
+                "launches_per_call": launches, "clocks": clocks}
+
+    res = one(True)
+    res.update({"flops": fl, "reps": reps,
+                "note": "doc_start scan + prep + fused dK/dV/dQ kernel (dQ pieces summed "
+                        "by TMA bulk reductions into float32) + dq conversion, median of "
+                        "reps; flops = 2.5 x forward (S, dP, dV, dQ, dK)",
+                "two_kernel_form": dict(one(False), note="doc_start scan + prep + dQ + dK/dV "
+                                        "kernels (dQ recomputed; bit-reproducible)")})
+    return res
 
 
 # ------------------------------------------------------- CPU oracle leg
