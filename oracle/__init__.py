@@ -62,6 +62,7 @@ from .attention import (  # noqa: F401
     full_attention,
     merge_partials,
     ring_partial,
+    ring_partial_backward,
     ring_unstabilised_f32,
     segment_ids,
 )

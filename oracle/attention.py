@@ -366,6 +366,54 @@ def attention_backward(q, k, v, dout, position_ids=None, scale=None):
     return dq, dk, dv
 
 
+def ring_partial_backward(q_blk, k_blk, v_blk, out_blk, dout_blk, lse_blk, S, P, i, j,
+                          order="contiguous", position_ids=None, scale=None):
+    """The gradient parts of one ring step on one device: the device holding
+    query block i ("Ring Attention", "Cómo funciona la atención en anillo")
+    after receiving key/value block j.  Block tensors in local row order
+    (q_blk, out_blk, dout_blk [B][S/P][Hq][d]; k_blk, v_blk [B][S/P][Hkv][d];
+    lse_blk [B][Hq][S/P], the forward's lse of block i's rows over the whole
+    sequence); position_ids of the whole sequence.  The derivatives of the
+    definition (as in attention_backward), restricted to the pair:
+        P_ij  = exp(scale * Q_i K_j^T - lse_i)   on the allowed pairs
+        D_i   = sum_c dO_i[:, c] * O_i[:, c]
+        dS_ij = P_ij * (dO_i V_j^T - D_i)
+        dq part = scale * dS_ij K_j,  dk part = scale * dS_ij^T Q_i,
+        dv part = P_ij^T dO_i
+    Summed over j (dq) and over i (dk, dv) these give attention_backward.
+    Returns the three parts in float64, block-shaped.
+    """
+    B, Lb, Hq, d = q_blk.shape
+    Hkv = k_blk.shape[2]
+    g = Hq // Hkv
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    ti = block_tokens(S, P, i, order)
+    tj = block_tokens(S, P, j, order)
+    seg = None if position_ids is None else segment_ids(position_ids)
+    dq = np.zeros((B, Lb, Hq, d))
+    dk = np.zeros((B, Lb, Hkv, d))
+    dv = np.zeros((B, Lb, Hkv, v_blk.shape[3]))
+    for b in range(B):
+        allowed = _allowed_between(None if seg is None else seg[b], ti, tj)
+        for h in range(Hq):
+            kvh = h // g
+            qh = np.asarray(q_blk[b, :, h, :], dtype=np.float64)
+            kh = np.asarray(k_blk[b, :, kvh, :], dtype=np.float64)
+            vh = np.asarray(v_blk[b, :, kvh, :], dtype=np.float64)
+            oh = np.asarray(out_blk[b, :, h, :], dtype=np.float64)
+            doh = np.asarray(dout_blk[b, :, h, :], dtype=np.float64)
+            lse = np.asarray(lse_blk[b, h, :], dtype=np.float64)
+            live = allowed & np.isfinite(lse)[:, None]
+            s = scale * (qh @ kh.T)
+            p = np.where(live, np.exp(np.where(live, s - lse[:, None], 0.0)), 0.0)
+            D = (doh * oh).sum(axis=1)
+            ds = p * (doh @ vh.T - D[:, None])
+            dq[b, :, h, :] += scale * (ds @ kh)
+            dk[b, :, kvh, :] += scale * (ds.T @ qh)
+            dv[b, :, kvh, :] += p.T @ doh
+    return dq, dk, dv
+
+
 def attention_backward_rows(q, k, v, dout, rows, position_ids=None, scale=None,
                             max_chunk_elems=1 << 24):
     """dq for the given query tokens only, every query head.

@@ -158,3 +158,59 @@ def test_sampled_rows_and_keys_match_autograd(case):
     dk1, dv1 = oracle.attention_backward_keys(q, k, v, do, keys, pos, scale, kv_heads=[1])
     assert np.abs(dk1[:, :, 1] - tk[:, keys, 1]).max() < 1e-12
     assert not dk1[:, :, 0].any() and not dv1[:, :, 0].any()
+
+
+def _blocks(x, S, P, p, order, axis=1):
+    return np.take(x, oracle.block_tokens(S, P, p, order), axis=axis)
+
+
+@pytest.mark.parametrize("case,order,P", [("noncausal", "contiguous", 3), ("causal", "striped", 4),
+                                          ("packed", "contiguous", 4), ("packed", "striped", 3)])
+def test_ring_partial_backward_sums_to_autograd(case, order, P):
+    """The per-device ring-step gradient parts, scattered back to token order
+    and summed over every (query block i, key/value block j) pair, equal
+    float64 autograd on the whole problem (GQA group of 3); using each
+    block pair's own log-sum-exp instead of the whole row's -- a plausible
+    slip -- does not."""
+    B, S, Hq, Hkv, d = 2, 36, 6, 2, 8
+    q, k, v, do = (_rand((B, S, h, d), s) for s, h in ((31, Hq), (32, Hkv), (33, Hkv), (34, Hq)))
+    if case == "noncausal":
+        pos, mask = None, None
+    elif case == "causal":
+        pos = np.tile(np.arange(S)[None, :], (B, 1))
+        mask = np.tril(np.ones((S, S), dtype=bool))
+    else:
+        pos = np.tile(_packed([10, 1, 14, 11]), (B, 1))
+        mask = oracle.allowed_mask(pos, 1, S)[0]
+    scale = 0.3
+    tq, tk, tv = _torch_grads(q, k, v, do, mask, scale)
+    out, lse = oracle.full_attention(q, k, v, pos, scale)
+    dq, dk, dv = np.zeros(q.shape), np.zeros(k.shape), np.zeros(v.shape)
+    for i in range(P):
+        ti = oracle.block_tokens(S, P, i, order)
+        for j in range(P):
+            tj = oracle.block_tokens(S, P, j, order)
+            pq, pk, pv = oracle.ring_partial_backward(
+                _blocks(q, S, P, i, order), _blocks(k, S, P, j, order), _blocks(v, S, P, j, order),
+                _blocks(out, S, P, i, order), _blocks(do, S, P, i, order),
+                _blocks(lse, S, P, i, order, axis=2), S, P, i, j, order, pos, scale)
+            dq[:, ti] += pq
+            dk[:, tj] += pk
+            dv[:, tj] += pv
+    assert np.abs(dq - tq).max() < 1e-10
+    assert np.abs(dk - tk).max() < 1e-10
+    assert np.abs(dv - tv).max() < 1e-10
+    # planted slip: the pair's own lse (softmax over block j only)
+    i, j = P - 1, 0
+    _, lse_pair = oracle.ring_partial(q, k, v, P, (i - j) % P, order, pos, scale)
+    ti = oracle.block_tokens(S, P, i, order)
+    pq_wrong, _, _ = oracle.ring_partial_backward(
+        _blocks(q, S, P, i, order), _blocks(k, S, P, j, order), _blocks(v, S, P, j, order),
+        _blocks(out, S, P, i, order), _blocks(do, S, P, i, order),
+        _blocks(lse_pair, S, P, i, order, axis=2), S, P, i, j, order, pos, scale)
+    pq_right, _, _ = oracle.ring_partial_backward(
+        _blocks(q, S, P, i, order), _blocks(k, S, P, j, order), _blocks(v, S, P, j, order),
+        _blocks(out, S, P, i, order), _blocks(do, S, P, i, order),
+        _blocks(lse, S, P, i, order, axis=2), S, P, i, j, order, pos, scale)
+    if np.abs(pq_right).max() > 0:
+        assert np.abs(pq_wrong - pq_right).max() > 1e-3
