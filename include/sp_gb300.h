@@ -355,6 +355,45 @@ sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const void* v, con
                                 void* workspace, size_t workspace_bytes, sp_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Backward of one ring step on one device (the device that holds query
+ * block i, with key/value block j received from its ring neighbour; "Ring
+ * Attention", "Cómo funciona la atención en anillo" -- the pages train with
+ * it, "Ulysses SP: entrenar modelos con millones de tokens").  Adds block
+ * pair (i, j)'s part of the gradients of the whole-sequence attention:
+ *
+ *   P   = exp(scale * Q_i K_j^T - lse_i)  on the allowed pairs (lse_i: the
+ *         forward's log-sum-exp of block i's rows over ALL key blocks)
+ *   D_i = rowsum(dout_i * out_i)           (out_i: the forward's output)
+ *   dS  = P * (dout_i V_j^T - D_i)
+ *   dq_acc += scale * dS K_j,  dk_acc += scale * dS^T Q_i,  dv_acc += P^T dout_i
+ *   (GQA: the query heads of a group add into their key/value head)
+ *
+ * Summed over j (for dq_acc) or over i (for dk_acc, dv_acc) these are the
+ * whole-sequence gradients, so a ring that passes K_j, V_j together with
+ * their dk/dv accumulators visits every pair once.
+ *
+ * q_blk, out_blk, dout_blk [B][S/P][Hq][d] (block i's rows in local order:
+ * local row u holds token u*P + i striped, i*S/P + u contiguous); k_blk,
+ * v_blk [B][S/P][Hkv][d] (block j); lse_blk [B][Hq][S/P] float32;
+ * position_ids [B][S] of the whole sequence or NULL (non-causal).
+ * dq_acc [B][S/P][Hq][d], dk_acc, dv_acc [B][S/P][Hkv][d]: float32
+ * accumulators, read and written (the caller zeroes them before the first
+ * step).  Supported: SP_BF16 with d == 128 (tensor cores; P and dS rounded
+ * to bf16 before the products, float32 accumulation), else
+ * SP_ERR_UNSUPPORTED; tensor pointers 16-byte aligned.  workspace:
+ * sp_ring_block_step_bwd_workspace_bytes(B, S, Hq, P, position_ids != NULL)
+ * bytes, 256-byte aligned.  Errors as for sp_blockwise_attn_bwd, and
+ * SP_ERR_INVALID_ARG for i or j outside [0, P).
+ * ------------------------------------------------------------------------ */
+size_t sp_ring_block_step_bwd_workspace_bytes(int B, int S, int Hq, int P, int causal);
+sp_status sp_ring_block_step_bwd(const void* q_blk, const void* k_blk, const void* v_blk,
+                                 const void* out_blk, const void* dout_blk, const float* lse_blk,
+                                 const int32_t* position_ids, int B, int S, int Hq, int Hkv,
+                                 int d, int P, sp_block_order order, int i, int j, float scale,
+                                 sp_dtype dtype, float* dq_acc, float* dk_acc, float* dv_acc,
+                                 void* workspace, size_t workspace_bytes, sp_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Merge of per-block partial results (the cross-device combine of ring
  * attention, "Ring Attention", "Cómo funciona la atención en anillo").
  *

@@ -15,6 +15,7 @@ without the built library raises ImportError -- there is no CPU path.
     blockwise_attention_backward(...)          dq, dk, dv from out, dout and lse
     doc_starts(position_ids)                   O(n) causal-mask carrier
     ring_block_step(q_blk, k_blk, v_blk, ...)  one device's ring step on block tensors
+    ring_block_step_backward(...)              its gradient parts, into float32 accumulators
     query_block_attention(q_blk, k, v, ...)    one device's query block against all K/V
 
 sequence_parallelism_gb300.dist runs the ring, all-gathered and Ulysses
@@ -29,7 +30,8 @@ from ._lib import SPError  # noqa: F401
 __all__ = ["seq_to_head", "head_to_seq", "blockwise_attention", "ring_step", "merge_partials",
            "ulysses_attention", "ulysses_attention_backward", "ulysses_ring_attention",
            "blockwise_attention_backward",
-           "doc_starts", "attention_workspace", "ring_block_step", "query_block_attention",
+           "doc_starts", "attention_workspace", "ring_block_step", "ring_block_step_backward",
+           "query_block_attention",
            "SPError"]
 
 
@@ -107,6 +109,28 @@ def ring_block_step(q_blk, k_blk, v_blk, P, i, j, order="contiguous", position_i
         workspace = attention_workspace(B, S, position_ids is not None, q_blk.device)
     return _lib.sp_ring_block_step(q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, scale,
                                    out, lse, workspace)
+
+
+def ring_block_step_backward(q_blk, k_blk, v_blk, out_blk, dout_blk, lse_blk, P, i, j,
+                             order="contiguous", position_ids=None, scale=0.0, dq_acc=None,
+                             dk_acc=None, dv_acc=None, workspace=None):
+    """The backward of one device's ring step: adds block pair (i, j)'s
+    gradient parts into float32 accumulators (created zeroed when not
+    given): dq_acc [B][S/P][Hq][d], dk_acc and dv_acc [B][S/P][Hkv][d].
+    lse_blk is block i's forward lse over the whole sequence.  Returns the
+    three accumulators."""
+    B, Lb = q_blk.shape[:2]
+    S = Lb * P
+    f32 = lambda like, acc: acc if acc is not None else torch.zeros(
+        like.shape, dtype=torch.float32, device=like.device)
+    dq_acc, dk_acc, dv_acc = f32(q_blk, dq_acc), f32(k_blk, dk_acc), f32(v_blk, dv_acc)
+    if workspace is None:
+        n = _lib.sp_ring_block_step_bwd_workspace_bytes(B, S, q_blk.shape[2], P,
+                                                        position_ids is not None)
+        workspace = torch.empty(n, dtype=torch.uint8, device=q_blk.device)
+    return _lib.sp_ring_block_step_bwd(q_blk, k_blk, v_blk, out_blk, dout_blk, lse_blk,
+                                       position_ids, S, P, order, i, j, scale, dq_acc, dk_acc,
+                                       dv_acc, workspace)
 
 
 def query_block_attention(q_blk, k, v, P, i, order="contiguous", position_ids=None, scale=0.0,

@@ -29,6 +29,7 @@ EXPORTS = (
     "sp_blockwise_attn_split_workspace_bytes",
     "sp_blockwise_attn_fwd", "sp_blockwise_attn_step", "sp_blockwise_attn_fwd_noalloc",
     "sp_ring_block_step", "sp_query_block_attn_fwd",
+    "sp_ring_block_step_bwd_workspace_bytes", "sp_ring_block_step_bwd",
     "sp_ulysses_ring_attn_workspace_bytes", "sp_ulysses_ring_attn_fwd",
     "sp_blockwise_attn_bwd_workspace_bytes", "sp_blockwise_attn_bwd", "sp_set_bwd_dq_reduction",
     "sp_attn_merge_partials",
@@ -64,6 +65,9 @@ def _load():
                                        sz, vp]),
         "sp_blockwise_attn_fwd_noalloc": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp, vp,
                                               vp]),
+        "sp_ring_block_step_bwd_workspace_bytes": (sz, [i, i, i, i, i]),
+        "sp_ring_block_step_bwd": (i, [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f,
+                                       i, vp, vp, vp, vp, sz, vp]),
         "sp_ring_block_step": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, vp, vp, vp,
                                    sz, vp]),
         "sp_query_block_attn_fwd": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp,
@@ -228,6 +232,31 @@ def sp_ring_block_step(q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, sca
         _ORDERS[order], i, j, float(scale), _dtype(q_blk), _ptr(out_blk), _ptr(lse_blk),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
     return out_blk, lse_blk
+
+
+def sp_ring_block_step_bwd_workspace_bytes(B, S, Hq, P, causal):
+    return int(_lib.sp_ring_block_step_bwd_workspace_bytes(B, S, Hq, P, 1 if causal else 0))
+
+
+def sp_ring_block_step_bwd(q_blk, k_blk, v_blk, out_blk, dout_blk, lse_blk, position_ids, S, P,
+                           order, i, j, scale, dq_acc, dk_acc, dv_acc, workspace, stream=None):
+    """Backward of one device's ring step: adds block pair (i, j)'s part of
+    the gradients into the float32 accumulators dq_acc ([B][S/P][Hq][d]),
+    dk_acc, dv_acc ([B][S/P][Hkv][d]); lse_blk is block i's forward lse."""
+    _dense(q_blk, k_blk, v_blk, out_blk, dout_blk, lse_blk, position_ids, dq_acc, dk_acc, dv_acc,
+           workspace)
+    B, Lb, Hq, d = q_blk.shape
+    Hkv = k_blk.shape[2]
+    if Lb * P != S or k_blk.shape[1] != Lb:
+        raise ValueError("block tensors must hold S/P rows")
+    if any(t.dtype != torch.float32 for t in (dq_acc, dk_acc, dv_acc)):
+        raise ValueError("the gradient accumulators are float32")
+    _check("sp_ring_block_step_bwd", _lib.sp_ring_block_step_bwd(
+        _ptr(q_blk), _ptr(k_blk), _ptr(v_blk), _ptr(out_blk), _ptr(dout_blk), _ptr(lse_blk),
+        _ptr(position_ids), B, S, Hq, Hkv, d, P, _ORDERS[order], i, j, float(scale),
+        _dtype(q_blk), _ptr(dq_acc), _ptr(dk_acc), _ptr(dv_acc), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dq_acc, dk_acc, dv_acc
 
 
 def sp_query_block_attn_fwd(q_blk, k, v, position_ids, P, order, i, scale, out_blk, lse_blk,

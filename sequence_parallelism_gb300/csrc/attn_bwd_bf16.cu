@@ -163,6 +163,9 @@ struct PrepArgs {
   int32_t* lo_blk;
   long long rows, nA, nB, nC;
   int S, H, P, Lbp, order;
+  // geometry of the doc_start lookups (the whole sequence); lo_block >= 0:
+  // the rows are those of that one block (per-device form)
+  int lo_S, lo_P, lo_order, lo_block;
 };
 
 __global__ void __launch_bounds__(256) bwd_prep_kernel(PrepArgs pa) {
@@ -212,9 +215,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(PrepArgs pa) {
   if (g < pa.nC) {
     const int u = static_cast<int>(g % pa.Lbp);
     const long long rp = g / pa.Lbp;
-    const int p = static_cast<int>(rp % pa.P);
-    const long long r = rp / pa.P;
-    pa.lo_blk[g] = u < Lb ? pa.doc_start[r * pa.S + block_token(pa.order, pa.S, pa.P, p, u)]
+    const int p = pa.lo_block >= 0 ? pa.lo_block : static_cast<int>(rp % pa.P);
+    const long long r = pa.lo_block >= 0 ? rp : rp / pa.P;
+    pa.lo_blk[g] = u < Lb ? pa.doc_start[r * pa.lo_S +
+                                         block_token(pa.lo_order, pa.lo_S, pa.lo_P, p, u)]
                           : INT_MAX;
   }
 }
@@ -916,6 +920,16 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* dst, uint32_t src, ui
 }
 
 
+// Per-device form of the fused kernel: query block i against key/value block
+// j, the block tensors [B][S/P][H][d] in local row order (their tensor maps
+// hold one block); masks use the global tokens of both blocks.  q_block < 0:
+// the whole sequence.
+struct BwdBlock {
+  int q_block, kv_block;
+  float* dk_acc;  // [B][S/P][Hkv][d] float32: += scale * dS^T Q
+  float* dv_acc;  // [B][S/P][Hkv][d] float32: += P^T dO
+};
+
 // One CTA per 128-key tile, walking the query tiles like bwd_dkdv_kernel.
 // Per 128-query tile t:
 //   S^T = K Q^T, dP^T = V dO^T                (SS, TMEM [0,128) / [128,256))
@@ -938,7 +952,7 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* dst, uint32_t src, ui
 // shared-memory stores cover 512 contiguous bytes.
 __global__ void __launch_bounds__(kFThreads, 1)
     bwd_fused_kernel(const __grid_constant__ BwdMaps tm, BwdArgs a, int n_tiles_k,
-                     float* __restrict__ dq_acc) {
+                     float* __restrict__ dq_acc, BwdBlock bb) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t q_full[kQSlots], q_empty[kQSlots], do_full, do_empty, kv_full, s_full,
       half_full[2], dq_full, dq_free, stage_full, stage_free, dkv_full, done;
@@ -951,10 +965,15 @@ __global__ void __launch_bounds__(kFThreads, 1)
   const uint32_t sdo = sk + 4 * kTileBytes, sds = sk + 5 * kTileBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // per-device form: one block in the tensor maps, the per-query arrays and
+  // the dQ accumulator
+  const bool per_dev = bb.q_block >= 0;
+  const int P_arr = per_dev ? 1 : a.P;
+  const int map_order = per_dev ? static_cast<int>(SP_ORDER_CONTIGUOUS) : a.order;
   const int BH = a.B * a.Hkv;
   const int pos = blockIdx.x / BH, bh = blockIdx.x % BH;
   const int b = bh / a.Hkv, hk = bh % a.Hkv;
-  const int j = pos / n_tiles_k, kt = pos % n_tiles_k;
+  const int j = per_dev ? bb.kv_block : pos / n_tiles_k, kt = per_dev ? pos : pos % n_tiles_k;
   const int Lb = a.S / a.P, w0 = kt * kT;
   const int k_first = static_cast<int>(block_token(a.order, a.S, a.P, j, w0));
   const int k_last = static_cast<int>(block_token(a.order, a.S, a.P, j, min(w0 + kT, Lb) - 1));
@@ -1003,8 +1022,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
       prefetch_tmap(&tm.dout);
       const uint32_t kf = smem_u32(&kv_full);
       mbar_arrive_expect_tx(kf, 2 * kTileBytes);
-      row_tma(sk, &tm.k, kf, hk, a.order, j, w0, b);
-      row_tma(sv, &tm.v, kf, hk, a.order, j, w0, b);
+      row_tma(sk, &tm.k, kf, hk, map_order, per_dev ? 0 : j, w0, b);
+      row_tma(sv, &tm.v, kf, hk, map_order, per_dev ? 0 : j, w0, b);
     }
     const long long lo_row = static_cast<long long>(b % a.pos_rows);
     const uint32_t col_bytes = (ds_row ? 3 : 2) * kQT * 4;
@@ -1015,6 +1034,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
       const long long bhq = static_cast<long long>(b) * a.Hq + h;
       for (int s = 0; s < a.P && ok; ++s) {
         const int i = (j + s) % a.P;
+        if (per_dev && i != bb.q_block) continue;
         int qt0, qt1;
         block_tiles(a.order, a.S, a.P, i, ds_row ? k_first : 0, a.S - 1, kQT, qt0, qt1);
         for (int base = qt0; base <= qt1 && ok; base += 32) {
@@ -1048,12 +1068,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
               cd.h = h;
               const uint32_t bar = smem_u32(&q_full[slot]);
               mbar_arrive_expect_tx(bar, kTileBytes + col_bytes);
-              row_tma(sq + slot * kTileBytes, &tm.q, bar, h, a.order, i, u0, b);
-              const long long off = blk_index(bhq, a.P, a.Lbp, i, u0);
+              row_tma(sq + slot * kTileBytes, &tm.q, bar, h, map_order, per_dev ? 0 : i, u0, b);
+              const long long off = blk_index(bhq, P_arr, a.Lbp, per_dev ? 0 : i, u0);
               bulk_load(smem_u32(cd.lse2), a.lse2_blk + off, kQT * 4, bar);
               bulk_load(smem_u32(cd.D), a.D_blk + off, kQT * 4, bar);
               if (ds_row)
-                bulk_load(smem_u32(cd.lo), a.lo_blk + blk_index(lo_row, a.P, a.Lbp, i, u0),
+                bulk_load(smem_u32(cd.lo),
+                          a.lo_blk + blk_index(lo_row, P_arr, a.Lbp, per_dev ? 0 : i, u0),
                           kQT * 4, bar);
             }
             ++n;
@@ -1065,7 +1086,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             if (lane == 0) {
               const uint32_t bar = smem_u32(&do_full);
               mbar_arrive_expect_tx(bar, kTileBytes);
-              row_tma(sdo, &tm.dout, bar, h, a.order, i, u0, b);
+              row_tma(sdo, &tm.dout, bar, h, map_order, per_dev ? 0 : i, u0, b);
             }
             ++n_do;
           }
@@ -1202,7 +1223,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         const ColData& cd = cols[slot];
         if (cd.info == kInfoEnd) break;
         const long long bhq = static_cast<long long>(b) * a.Hq + cd.h;
-        float* blk = dq_acc + blk_index(bhq, a.P, a.Lbp, cd.i, cd.u0) * kD;
+        float* blk = dq_acc + blk_index(bhq, P_arr, a.Lbp, per_dev ? 0 : cd.i, cd.u0) * kD;
         if (!mbar_wait(smem_u32(&stage_full), t & 1, abort_flag, a.err, kErrBwdOut)) break;
         // the dS^T half first: the next tile's dS^T stores need that buffer
         // soonest; Q_t's slot is needed again only for Q_{t+2}
@@ -1339,18 +1360,18 @@ __global__ void __launch_bounds__(kFThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&stage_full));
     }
-    // epilogue: dK * scale and dV, rows of key token ktok
+    // epilogue: dK * scale and dV, rows of key token ktok (bf16), or in the
+    // per-device form added to the float32 accumulators at local row w
     const bool have = t > 0 && ok;
     if (have && !wait_warp(smem_u32(&dkv_full), 0, abort_flag, a.err, kErrBwdOut)) ok = false;
     tc_fence_after();
     const long long orow =
         ((static_cast<long long>(b) * a.S + (key_live ? ktok : 0)) * a.Hkv + hk) * kD;
-    uint4* dk_row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dk) + orow);
-    uint4* dv_row = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.dv) + orow);
+    const long long lrow =
+        ((static_cast<long long>(b) * Lb + (key_live ? w : 0)) * a.Hkv + hk) * kD;
 #pragma unroll 1
     for (int m = 0; m < 2; ++m) {
       const float mul = m == 0 ? a.scale : 1.f;
-      uint4* dst = m == 0 ? dk_row : dv_row;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t x[32];
@@ -1361,11 +1382,28 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[e] = 0u;
         }
+        if (per_dev) {
+          if (key_live && have && ok) {
+            float4* acc = reinterpret_cast<float4*>((m == 0 ? bb.dk_acc : bb.dv_acc) + lrow);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              float4 v4 = acc[c * 8 + e];
+              v4.x += __uint_as_float(x[4 * e]) * mul;
+              v4.y += __uint_as_float(x[4 * e + 1]) * mul;
+              v4.z += __uint_as_float(x[4 * e + 2]) * mul;
+              v4.w += __uint_as_float(x[4 * e + 3]) * mul;
+              acc[c * 8 + e] = v4;
+            }
+          }
+          continue;
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           pk[e] = pack_bf16(__uint_as_float(x[2 * e]) * mul, __uint_as_float(x[2 * e + 1]) * mul);
         if (key_live) {
+          uint4* dst = reinterpret_cast<uint4*>(
+              static_cast<__nv_bfloat16*>(m == 0 ? a.dk : a.dv) + orow);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             dst[c * 4 + e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
@@ -1411,6 +1449,34 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __res
   }
 }
 
+// Per-device form: dq_acc[b][u][h][:] += scale * (the fp32 sums of block i),
+// float32, [B][S/P][Hq][d]; the blocked accumulator holds one block.
+__global__ void __launch_bounds__(256) bwd_dq_add_kernel(const float4* __restrict__ acc,
+                                                         float4* dq_acc, int Lb, int Hq, int Lbp,
+                                                         float scale) {
+  const int tiles = Lbp / kQT;
+  const long long blk = blockIdx.x;  // (b * Hq + h) * tiles + tile
+  const int tile = static_cast<int>(blk % tiles);
+  const long long bh = blk / tiles;
+  const int h = static_cast<int>(bh % Hq);
+  const long long b = bh / Hq;
+  const int r = threadIdx.x & (kQT - 1), g0 = threadIdx.x >> 7;
+  const int u = tile * kQT + r;
+  if (u >= Lb) return;
+  const float4* src = acc + blk * (kQT * kD / 4) + r;
+  float4* dst = dq_acc + ((b * Lb + u) * Hq + h) * (kD / 4);
+#pragma unroll 4
+  for (int q = g0; q < kD / 4; q += 2) {
+    const float4 x = src[q * kQT];
+    float4 y = dst[q];
+    y.x += x.x * scale;
+    y.y += x.y * scale;
+    y.z += x.z * scale;
+    y.w += x.w * scale;
+    dst[q] = y;
+  }
+}
+
 // Tensor maps and the prep kernel, shared by both backward forms.
 bool launch_prep(const BwdArgs& a, BwdMaps& tm, cudaStream_t st) {
   if (!tmap::make_map(&tm.q, a.q, a.B, a.S, a.Hq, a.P, a.order) ||
@@ -1436,6 +1502,10 @@ bool launch_prep(const BwdArgs& a, BwdMaps& tm, cudaStream_t st) {
   pa.P = a.P;
   pa.Lbp = a.Lbp;
   pa.order = a.order;
+  pa.lo_S = a.S;
+  pa.lo_P = a.P;
+  pa.lo_order = a.order;
+  pa.lo_block = -1;
   const long long n_prep = pa.nA + pa.nB + pa.nC;
   bwd_prep_kernel<<<static_cast<unsigned>((n_prep + 255) / 256), 256, 0, st>>>(pa);
   return true;
@@ -1475,12 +1545,68 @@ int launch_attn_bwd_bf16_fused(const BwdArgs& a, float* dq_acc, cudaStream_t st)
                            f_smem) != cudaSuccess)
     return -1;
   const unsigned n_kv = static_cast<unsigned>(a.P) * n_tiles * a.B * a.Hkv;
-  bwd_fused_kernel<<<n_kv, kFThreads, f_smem, st>>>(tm, a, n_tiles, dq_acc);
+  bwd_fused_kernel<<<n_kv, kFThreads, f_smem, st>>>(tm, a, n_tiles, dq_acc,
+                                                     BwdBlock{-1, -1, nullptr, nullptr});
   const unsigned n_blk = static_cast<unsigned>(static_cast<long long>(a.B) * a.Hq * a.P *
                                                (a.Lbp / kQT));
   bwd_dq_convert_kernel<<<n_blk, 256, 0, st>>>(reinterpret_cast<const float4*>(dq_acc),
                                                 static_cast<__nv_bfloat16*>(a.dq), a.S, a.Hq,
                                                 a.P, a.Lbp, a.order, a.scale);
+  return cudaGetLastError() == cudaSuccess ? 3 : -1;
+}
+
+// Per-device form: prep of block i's rows, the fused kernel over key/value
+// block j's key tiles walking block i's query tiles, then dq_acc += the
+// block's dQ sums.  a.q, a.out, a.dout, a.lse hold block i ([B][S/P][Hq][d],
+// lse [B][Hq][S/P]); a.k, a.v block j; a.S, a.P, a.order the whole sequence;
+// dq_blocked: B * Hq * Lbp * 128 floats of scratch.
+int launch_attn_bwd_bf16_block(const BwdArgs& a, int qb, int kb, float* dq_blocked,
+                               float* dq_acc, float* dk_acc, float* dv_acc, cudaStream_t st) {
+  const int Lb = a.S / a.P;
+  BwdMaps tm;  // one block of Lb rows in each map
+  if (!tmap::make_map(&tm.q, a.q, a.B, Lb, a.Hq, 1, SP_ORDER_CONTIGUOUS) ||
+      !tmap::make_map(&tm.dout, a.dout, a.B, Lb, a.Hq, 1, SP_ORDER_CONTIGUOUS) ||
+      !tmap::make_map(&tm.k, a.k, a.B, Lb, a.Hkv, 1, SP_ORDER_CONTIGUOUS) ||
+      !tmap::make_map(&tm.v, a.v, a.B, Lb, a.Hkv, 1, SP_ORDER_CONTIGUOUS))
+    return -1;
+  PrepArgs pa;
+  pa.out = static_cast<const uint4*>(a.out);
+  pa.dout = static_cast<const uint4*>(a.dout);
+  pa.lse = a.lse;
+  pa.doc_start = a.doc_start;
+  pa.D_blk = a.D_blk;
+  pa.lse2_blk = a.lse2_blk;
+  pa.lo_blk = a.lo_blk;
+  pa.rows = static_cast<long long>(a.B) * Lb * a.Hq;
+  pa.nA = (pa.rows * 16 + 31) / 32 * 32;
+  pa.nB = static_cast<long long>(a.B) * a.Hq * (a.Lbp - Lb);
+  pa.nC = a.doc_start ? static_cast<long long>(a.pos_rows) * a.Lbp : 0;
+  pa.S = Lb;  // the rows of one block, in local order
+  pa.H = a.Hq;
+  pa.P = 1;
+  pa.Lbp = a.Lbp;
+  pa.order = SP_ORDER_CONTIGUOUS;
+  pa.lo_S = a.S;
+  pa.lo_P = a.P;
+  pa.lo_order = a.order;
+  pa.lo_block = qb;
+  const long long n_prep = pa.nA + pa.nB + pa.nC;
+  bwd_prep_kernel<<<static_cast<unsigned>((n_prep + 255) / 256), 256, 0, st>>>(pa);
+  const size_t acc_bytes = static_cast<size_t>(a.B) * a.Hq * a.Lbp * kD * sizeof(float);
+  if (cudaMemsetAsync(dq_blocked, 0, acc_bytes, st) != cudaSuccess) return -1;
+  const int n_tiles = (Lb + kT - 1) / kT;
+  const int f_smem = kFSmemBytes + 1024;
+  if (cudaFuncSetAttribute(bwd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           f_smem) != cudaSuccess)
+    return -1;
+  const unsigned n_kv = static_cast<unsigned>(n_tiles) * a.B * a.Hkv;
+  bwd_fused_kernel<<<n_kv, kFThreads, f_smem, st>>>(tm, a, n_tiles, dq_blocked,
+                                                     BwdBlock{qb, kb, dk_acc, dv_acc});
+  const unsigned n_blk =
+      static_cast<unsigned>(static_cast<long long>(a.B) * a.Hq * (a.Lbp / kQT));
+  bwd_dq_add_kernel<<<n_blk, 256, 0, st>>>(reinterpret_cast<const float4*>(dq_blocked),
+                                            reinterpret_cast<float4*>(dq_acc), Lb, a.Hq, a.Lbp,
+                                            a.scale);
   return cudaGetLastError() == cudaSuccess ? 3 : -1;
 }
 

@@ -8,7 +8,9 @@ The pages describe three ways to spread one attention layer over P devices:
   device i + 1 and receives one from device i - 1, so at step s it holds block
   j = (i - s) mod P; the partial results are combined by the cumulative
   softmax.  ring_attention() below: P - 1 point-to-point exchanges, the next
-  block in flight while the current one is multiplied.
+  block in flight while the current one is multiplied; its gradients in
+  ring_attention_backward(), where each key/value block travels with its
+  dK/dV accumulators.
 * Ulysses ("Ulysses SP: entrenar modelos con millones de tokens", "Cómo
   funciona Ulysses Sequence Parallelism (SP)"; "DeepSpeed-Ulysses",
   "Method"): an all-to-all turns every device's sequence shard of all heads
@@ -55,6 +57,17 @@ class LibraryKernels:
         ws = self.workspace(q_blk.shape[0], S, position_ids is not None, q_blk.device)
         _lib.sp_ring_block_step(q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, 0.0, out,
                                 lse, ws)
+
+    def ring_step_backward(self, q_blk, k_blk, v_blk, out_blk, dout_blk, lse_blk, position_ids,
+                           S, P, order, i, j, dq_acc, dk_acc, dv_acc):
+        B, _, Hq, _ = q_blk.shape
+        causal = position_ids is not None
+        key = ("ring_bwd", B, S, Hq, P, causal, str(q_blk.device))
+        if key not in self._ws:
+            n = _lib.sp_ring_block_step_bwd_workspace_bytes(B, S, Hq, P, causal)
+            self._ws[key] = torch.empty(n, dtype=torch.uint8, device=q_blk.device)
+        _lib.sp_ring_block_step_bwd(q_blk, k_blk, v_blk, out_blk, dout_blk, lse_blk, position_ids,
+                                    S, P, order, i, j, 0.0, dq_acc, dk_acc, dv_acc, self._ws[key])
 
     def merge(self, outs, lses, out, lse):
         _lib.sp_attn_merge_partials(outs, lses, out, lse)
@@ -155,6 +168,60 @@ def ring_attention(q_blk, k_blk, v_blk, position_ids, order="contiguous", group=
         for r in reqs:
             r.wait()
     return outs[cur][0], lses[cur][0]
+
+
+def ring_attention_backward(q_blk, k_blk, v_blk, out_blk, dout_blk, lse_blk, position_ids,
+                            order="contiguous", group=None, kernels=None):
+    """Gradients of ring_attention across the group.  This rank (i of P)
+    holds block i of q, k, v, of the forward's out and lse, and of dout;
+    returns (dq, dk, dv) for its blocks in the inputs' dtypes.
+
+    Step s: with key/value block j = (i - s) mod P and that block's dK/dV
+    accumulators (float32; float64 for float64 data), add pair (i, j)'s
+    gradient parts -- dq locally, dk and dv into the travelling
+    accumulators -- then pass K_j, V_j and the accumulators to rank i + 1.
+    K/V of the next step are in flight while the step is computed; the
+    accumulators can leave only after it, and make one last hop after step
+    P - 1, which brings every block's accumulators back to the rank that
+    holds it.
+    """
+    kn = _kernels(kernels)
+    P, i = _world(group)
+    B, Lb, Hq, d = q_blk.shape
+    S = Lb * P
+    nxt_rank, prv_rank = _peer(group, (i + 1) % P), _peer(group, (i - 1) % P)
+    acc_dtype = torch.float64 if q_blk.dtype == torch.float64 else torch.float32
+    dev = q_blk.device
+    dq = torch.zeros((B, Lb, Hq, d), dtype=acc_dtype, device=dev)
+    kv = [(k_blk, v_blk), (torch.empty_like(k_blk), torch.empty_like(v_blk))]
+    acc = [(torch.zeros(k_blk.shape, dtype=acc_dtype, device=dev),
+            torch.zeros(v_blk.shape, dtype=acc_dtype, device=dev)),
+           (torch.empty(k_blk.shape, dtype=acc_dtype, device=dev),
+            torch.empty(v_blk.shape, dtype=acc_dtype, device=dev))]
+    for s in range(P):
+        j = (i - s) % P
+        reqs = []
+        if s + 1 < P:
+            (ck, cv), (nk, nv) = kv[s % 2], kv[(s + 1) % 2]
+            reqs = dist.batch_isend_irecv([
+                dist.P2POp(dist.isend, ck, nxt_rank, group),
+                dist.P2POp(dist.isend, cv, nxt_rank, group),
+                dist.P2POp(dist.irecv, nk, prv_rank, group),
+                dist.P2POp(dist.irecv, nv, prv_rank, group)])
+        hk, hv = kv[s % 2]
+        ak, av = acc[s % 2]
+        kn.ring_step_backward(q_blk, hk, hv, out_blk, dout_blk, lse_blk, position_ids, S, P,
+                              order, i, j, dq, ak, av)
+        (nak, nav) = acc[(s + 1) % 2]
+        reqs += dist.batch_isend_irecv([
+            dist.P2POp(dist.isend, ak, nxt_rank, group),
+            dist.P2POp(dist.isend, av, nxt_rank, group),
+            dist.P2POp(dist.irecv, nak, prv_rank, group),
+            dist.P2POp(dist.irecv, nav, prv_rank, group)])
+        for r in reqs:
+            r.wait()
+    dk, dv = acc[P % 2]
+    return dq.to(q_blk.dtype), dk.to(k_blk.dtype), dv.to(v_blk.dtype)
 
 
 def allgather_kv_attention(q_blk, k_blk, v_blk, position_ids, order="contiguous", group=None,

@@ -9,7 +9,9 @@ GPU tests check the kernels against the same oracle), and every supplied
 step first checks that the block it was handed is the one the ring schedule
 names ("Ring Attention", "Cómo funciona la atención en anillo": at step s
 device i holds key/value block j = (i - s) mod P).  Each rank's result must
-equal its rows of full attention."""
+equal its rows of full attention, or of its gradients; in the ring backward
+every step also checks that the dK/dV accumulators it is handed hold exactly
+the parts of the ranks the block has visited so far."""
 
 import os
 import socket
@@ -62,6 +64,35 @@ class OracleKernels:
         out.copy_(torch.from_numpy(o[:, ti]))
         lse.copy_(torch.from_numpy(l_[:, :, ti]))
 
+    def _pair_parts(self, S, P, order, i, j):
+        ti, tj = oracle.block_tokens(S, P, i, order), oracle.block_tokens(S, P, j, order)
+        return oracle.ring_partial_backward(
+            self.q[:, ti], self.k[:, tj], self.v[:, tj], self.out[:, ti], self.dout[:, ti],
+            self.lse[:, :, ti], S, P, i, j, order, self.pos)
+
+    def ring_step_backward(self, q_blk, k_blk, v_blk, out_blk, dout_blk, lse_blk, position_ids,
+                           S, P, order, i, j, dq_acc, dk_acc, dv_acc):
+        ti, tj = oracle.block_tokens(S, P, i, order), oracle.block_tokens(S, P, j, order)
+        assert np.array_equal(q_blk.numpy(), self.q[:, ti])
+        assert np.array_equal(out_blk.numpy(), self.out[:, ti])
+        assert np.array_equal(dout_blk.numpy(), self.dout[:, ti])
+        assert np.array_equal(lse_blk.numpy(), self.lse[:, :, ti])
+        assert np.array_equal(k_blk.numpy(), self.k[:, tj]), f"device {i} holds the wrong block"
+        assert np.array_equal(v_blk.numpy(), self.v[:, tj])
+        # block j started at rank j and has visited ranks j, ..., i - 1
+        seen_k, seen_v = np.zeros(k_blk.shape), np.zeros(v_blk.shape)
+        for r in range(j, j + (i - j) % P):
+            _, pk, pv = self._pair_parts(S, P, order, r % P, j)
+            seen_k += pk
+            seen_v += pv
+        assert np.abs(dk_acc.numpy() - seen_k).max() < 1e-12, "dK accumulator out of step"
+        assert np.abs(dv_acc.numpy() - seen_v).max() < 1e-12, "dV accumulator out of step"
+        self.log.append((i, j))
+        pq, pk, pv = self._pair_parts(S, P, order, i, j)
+        dq_acc += torch.from_numpy(pq)
+        dk_acc += torch.from_numpy(pk)
+        dv_acc += torch.from_numpy(pv)
+
     def merge(self, outs, lses, out, lse):
         o, l_ = oracle.merge_partials(outs.numpy(), lses.numpy())
         out.copy_(torch.from_numpy(o))
@@ -107,7 +138,16 @@ def _worker(rank, world, port, kind, params, results):
         kn = OracleKernels(q, k, v, pos, order, log)
         tpos = None if pos is None else torch.from_numpy(pos)
         ref_o, ref_l = oracle.full_attention(q, k, v, pos)
-        if kind in ("ring", "allgather"):
+        if kind == "ring_bwd":
+            t = oracle.block_tokens(S, world, rank, order)
+            blk = lambda a, ax=1: torch.from_numpy(np.ascontiguousarray(np.take(a, t, axis=ax)))
+            dout = np.random.default_rng(seed + 1).standard_normal(q.shape)
+            kn.out, kn.lse, kn.dout = ref_o, ref_l, dout
+            grads = spd.ring_attention_backward(blk(q), blk(k), blk(v), blk(ref_o), blk(dout),
+                                                blk(ref_l, 2), tpos, order, kernels=kn)
+            ref_g = oracle.attention_backward(q, k, v, dout, pos)
+            err = max(np.abs(g_.numpy() - r_[:, t]).max() for g_, r_ in zip(grads, ref_g))
+        elif kind in ("ring", "allgather"):
             t = oracle.block_tokens(S, world, rank, order)
             blk = lambda a: torch.from_numpy(np.ascontiguousarray(a[:, t]))
             fn = spd.ring_attention if kind == "ring" else spd.allgather_kv_attention
@@ -170,3 +210,20 @@ def test_ulysses_all_to_all_forward_and_backward(world, params):
     res = _run(world, "ulysses", params)
     for rank in range(world):
         assert res[rank][0] < 1e-12
+
+
+@pytest.mark.parametrize("world,params", [
+    (2, (1, 48, 2, 1, 8, "causal", "contiguous", 41)),
+    (3, (2, 60, 4, 2, 8, "packed", "striped", 42)),
+    (4, (1, 64, 2, 2, 8, "none", "striped", 43)),
+])
+def test_ring_backward_exchange(world, params):
+    """The ring backward: every rank sees key/value block j = (i - s) mod P at
+    step s together with accumulators that hold the parts of exactly the
+    ranks that block has visited, and ends with its own blocks' gradients
+    (dq from its steps, dk/dv brought home by the last hop)."""
+    res = _run(world, "ring_bwd", params)
+    for rank in range(world):
+        err, log = res[rank]
+        assert err < 1e-10, f"rank {rank}: {err}"
+        assert log == [(rank, (rank - s) % world) for s in range(world)]

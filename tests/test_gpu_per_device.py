@@ -7,8 +7,10 @@ mask in global token indices.  Every (i, j) pair must equal block i's rows of
 the oracle's ring partial at step (i - j) mod P, merging device i's P steps
 must give block i's rows of full attention, and sp_query_block_attn_fwd (the
 all-gathered variant: query block i against the whole K, V) must give those
-rows directly.  Shapes span ragged 128-row tiles, GQA, packed documents and
-both block orders."""
+rows directly.  The backward of a ring step (sp_ring_block_step_bwd) must
+give every pair's gradient parts, and their sums the whole gradients.
+Shapes span ragged 128-row tiles, GQA, packed documents and both block
+orders."""
 
 import numpy as np
 import pytest
@@ -102,6 +104,89 @@ def test_query_block_against_whole_sequence(sp, case):
             assert torch.equal(out, ref_out[:, ti]) and torch.equal(lse, ref_lse[:, :, ti])
 
 
+@pytest.mark.parametrize("case", [c for c in CASES if c[0] == "bf16"])
+def test_ring_block_step_backward_every_pair(sp, case):
+    """Every (query block i, key/value block j) pair's gradient parts against
+    oracle.ring_partial_backward on the same inputs (our forward's out and
+    lse, as a training step would use), then the sums -- dq over j, dk and
+    dv over i -- against the whole gradients of the oracle and against the
+    whole-sequence backward on the GPU."""
+    from sequence_parallelism_gb300 import _lib
+    dtype, B, S, Hq, Hkv, d, P, order, pos_kind = case
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 4500 + S, dtype)
+    g = torch.Generator(device="cuda").manual_seed(4501 + S)
+    dout = torch.randn(q.shape, generator=g, device="cuda").to(q.dtype)
+    pos = _positions(pos_kind, B, S, 81)
+    tpos = None if pos is None else torch.from_numpy(pos).cuda()
+    out, lse = sp.blockwise_attention(q, k, v, P, order, tpos)
+    Lb = S // P
+    blocks = [oracle.block_tokens(S, P, p, order) for p in range(P)]
+    ws = torch.empty(_lib.sp_ring_block_step_bwd_workspace_bytes(B, S, Hq, P, pos is not None),
+                     dtype=torch.uint8, device="cuda")
+    tl = lambda t, p: t[:, :, torch.from_numpy(blocks[p]).cuda()].contiguous()
+    dq = torch.zeros((B, S, Hq, d), dtype=torch.float64)
+    dk = torch.zeros((B, S, Hkv, d), dtype=torch.float64)
+    dv = torch.zeros((B, S, Hkv, d), dtype=torch.float64)
+    for i in range(P):
+        for j in range(P):
+            acc = [torch.zeros((B, Lb, h, d), dtype=torch.float32, device="cuda")
+                   for h in (Hq, Hkv, Hkv)]
+            args = (_block(q, blocks[i]), _block(k, blocks[j]), _block(v, blocks[j]),
+                    _block(out, blocks[i]), _block(dout, blocks[i]), tl(lse, i))
+            _lib.sp_ring_block_step_bwd(*args, tpos, S, P, order, i, j, 0.0, *acc, ws)
+            torch.cuda.synchronize()
+            ref = oracle.ring_partial_backward(*(np32(a) for a in args[:5]),
+                                               args[5].cpu().numpy(), S, P, i, j, order, pos)
+            for name, got, r in zip(("dq", "dk", "dv"), acc, ref):
+                check_grad(got.cpu().numpy(), r, "bf16", f"{case} pair ({i}, {j}) {name}")
+            dq[:, blocks[i]] += acc[0].cpu().double()
+            dk[:, blocks[j]] += acc[1].cpu().double()
+            dv[:, blocks[j]] += acc[2].cpu().double()
+    assert _lib.sp_get_device_error(ws) == (0, 0)
+    ref_g = oracle.attention_backward(np32(q), np32(k), np32(v), np32(dout), pos)
+    whole = sp.blockwise_attention_backward(q, k, v, out, dout, lse, P, order, tpos)
+    torch.cuda.synchronize()
+    for name, got, r, w in zip(("dq", "dk", "dv"), (dq, dk, dv), ref_g, whole):
+        check_grad(got.numpy(), r, "bf16", f"{case} summed {name}")
+        # the same products summed in another order: within bf16 rounding of the whole call
+        check_grad(got.numpy(), np32(w).astype(np.float64), "bf16", f"{case} vs whole {name}")
+
+
+def test_ring_block_step_backward_helper_and_errors(sp):
+    """sp.ring_block_step_backward gives the C call's bits; bad block indices,
+    float32 tensors, float32-less accumulators and a short workspace are
+    refused before any launch."""
+    from sequence_parallelism_gb300 import _lib
+    B, S, Hq, Hkv, d, P = 1, 512, 2, 1, 128, 4
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 4600, "bf16")
+    dout = torch.randn_like(q)
+    tpos = torch.from_numpy(_positions("causal", B, S, 82)).cuda()
+    out, lse = sp.blockwise_attention(q, k, v, P, "contiguous", tpos)
+    blk = lambda t: t[:, 256:384].contiguous()
+    lse_b = lse[:, :, 256:384].contiguous()
+    args = (blk(q), blk(k), blk(v), blk(out), blk(dout), lse_b)
+    h = sp.ring_block_step_backward(*args, P, 2, 2, "contiguous", tpos)
+    ws = torch.empty(_lib.sp_ring_block_step_bwd_workspace_bytes(B, S, Hq, P, True),
+                     dtype=torch.uint8, device="cuda")
+    acc = [torch.zeros_like(t, dtype=torch.float32) for t in (blk(q), blk(k), blk(v))]
+    _lib.sp_ring_block_step_bwd(*args, tpos, S, P, "contiguous", 2, 2, 0.0, *acc, ws)
+    torch.cuda.synchronize()
+    for a_, b_ in zip(h, acc):
+        assert torch.equal(a_, b_)
+    for i, j in ((4, 0), (0, 4), (-1, 0)):
+        with pytest.raises(_lib.SPError):
+            _lib.sp_ring_block_step_bwd(*args, tpos, S, P, "contiguous", i, j, 0.0, *acc, ws)
+    f32 = [t.float() for t in args[:5]]
+    with pytest.raises(_lib.SPError, match="not supported|unsupported"):
+        _lib.sp_ring_block_step_bwd(*f32, lse_b, tpos, S, P, "contiguous", 0, 0, 0.0, *acc, ws)
+    with pytest.raises(ValueError):
+        _lib.sp_ring_block_step_bwd(*args, tpos, S, P, "contiguous", 0, 0, 0.0, acc[0].double(),
+                                    acc[1], acc[2], ws)
+    with pytest.raises(_lib.SPError):
+        _lib.sp_ring_block_step_bwd(*args, tpos, S, P, "contiguous", 0, 0, 0.0, *acc, ws[:256])
+    assert _lib.sp_last_launch_count() == 0
+
+
 def test_package_helpers_match_the_c_calls(sp):
     """sp.ring_block_step / sp.query_block_attention allocate their outputs
     and give the same bits as the C entry points."""
@@ -175,5 +260,10 @@ def test_data_plane_on_one_rank_runs_the_library_kernels(sp):
         ref_g = oracle.attention_backward(np32(q), np32(k), np32(v), np32(dout), pos)
         for name, got, ref in zip(("dq", "dk", "dv"), grads, ref_g):
             check_grad(np32(got), ref, "bf16", f"one-rank Ulysses {name}")
+        out, lse = spd.ring_attention(q, k, v, tpos, "contiguous")
+        grads = spd.ring_attention_backward(q, k, v, out, dout, lse, tpos, "contiguous")
+        torch.cuda.synchronize()
+        for name, got, ref in zip(("dq", "dk", "dv"), grads, ref_g):
+            check_grad(np32(got), ref, "bf16", f"one-rank ring backward {name}")
     finally:
         dist.destroy_process_group()
