@@ -8,26 +8,29 @@
 //   dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO,
 // D_t = sum_c dO[t, c] O[t, c].
 //
-// Three kernels, no atomics:
+// Two forms, sharing the prep kernel:
 //  * prep: D per query row, and lse * log2(e), D and the document starts
-//    rewritten in block order (each block padded to a multiple of 64 rows), so
-//    that the dK/dV kernel fetches a query tile's per-column data with three
-//    contiguous bulk copies.
-//  * dQ: query-stationary.  One CTA keeps a 128-row Q tile and its dO tile in
-//    shared memory and walks the key/value blocks in ring order
-//    j = (i - s) mod P ("Ring Attention", "Cómo funciona la atención en
-//    anillo").  Per key tile: S = Q K^T and dP = dO V^T (SS MMAs); two
-//    elementwise warpgroups, one per 64 columns, read S and dP at once (so the
-//    next tile's MMAs start), form dS = P * (dP - D) and store it to TMEM as
-//    bf16; dQ += dS K reads dS from TMEM.
-//  * dK/dV: key-stationary.  One CTA keeps a 128-key K tile and V tile and
-//    walks, for every query head of the GQA group, the query blocks in the
-//    order its key block meets them on the ring, i = (j + s) mod P, in tiles
-//    of 64 queries.  Per tile: S^T = K Q^T and dP^T = V dO^T into one of two
-//    TMEM buffers, P^T and dS^T written back over them as bf16, then
-//    dV += P^T dO and dK += dS^T Q read them from TMEM.
+//    rewritten in block order (each block padded to a multiple of 128 rows),
+//    so that the key-stationary kernels fetch a query tile's per-column data
+//    with three contiguous bulk copies.
+//  * fused (default): key-stationary.  One CTA keeps a 128-key K tile and V
+//    tile and walks, for every query head of the GQA group, the query
+//    blocks in the order its key block meets them on the ring,
+//    i = (j + s) mod P, in tiles of 128 queries; per tile S^T and dP^T are
+//    multiplied once and give dV, dK and the tile's piece of dQ, which the
+//    TMA adds into a float32 accumulator (bulk reductions); a last kernel
+//    scales and rounds dq.  Per-device mode: one query block against one
+//    key/value block from block tensors, dK/dV added into float32
+//    accumulators (the backward of one ring step on one device).
+//  * two kernels, no atomics (bit-reproducible): dQ query-stationary -- one
+//    CTA keeps a 128-row Q tile and its dO tile and walks the key/value
+//    blocks in ring order j = (i - s) mod P ("Ring Attention", "Cómo
+//    funciona la atención en anillo"), S = Q K^T and dP = dO V^T (SS MMAs),
+//    two elementwise warpgroups form dS into TMEM, dQ += dS K -- and dK/dV
+//    key-stationary, like the fused kernel without dQ.
 // Warp roles: elementwise warps (one thread per TMEM lane = tile row), a TMA
-// producer warp and an MMA warp (TMEM owner).  Every barrier wait is bounded.
+// producer warp, an MMA warp (TMEM owner) and, in the fused kernel, a warp
+// that issues the dQ bulk reductions.  Every barrier wait is bounded.
 #include <climits>
 #include <cuda.h>
 #include <cuda_bf16.h>

@@ -140,3 +140,46 @@ def test_random_ring_block_pairs(sp, case):
         ro, rl = oracle.ring_partial(qn, kn, vn, P, (i - j) % P, order, pos)
         check_attention(np32(out), lse.cpu().numpy(), ro[:, ti], rl[:, :, ti], "bf16",
                         f"{_id(case)} i={i} j={j}")
+
+
+@pytest.mark.parametrize("case", _cases(2030, "bf16", 10, 700), ids=_id)
+def test_random_ring_block_pairs_backward(sp, case):
+    """Seeded shapes through sp_ring_block_step_bwd for two random (i, j)
+    block pairs each, accumulated twice into the same accumulators (the
+    second call adds the first call's parts again: exactly for dk and dv,
+    to float32 rounding for dq, whose per-key-tile pieces are summed in no
+    fixed order), against the oracle's ring step backward on our forward's
+    out and lse."""
+    import torch
+    import oracle
+    import workloads
+    from helpers import check_grad, np32
+    from test_gpu_attention import _positions
+    B, S, Hq, Hkv, d, P, order, pos_kind = case
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 1800 + S, "bf16")
+    g = torch.Generator(device="cuda").manual_seed(1801 + S)
+    dout = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
+    pos = _positions(pos_kind, B, S, 95 + S)
+    tpos = None if pos is None else torch.from_numpy(pos).cuda()
+    out, lse = sp.blockwise_attention(q, k, v, P, order, tpos)
+    rng = np.random.default_rng(S + 1)
+    for _ in range(2):
+        i, j = int(rng.integers(P)), int(rng.integers(P))
+        ti, tj = oracle.block_tokens(S, P, i, order), oracle.block_tokens(S, P, j, order)
+        blk = lambda t, tok: t[:, torch.from_numpy(tok).cuda()].contiguous()
+        lse_i = lse[:, :, torch.from_numpy(ti).cuda()].contiguous()
+        args = (blk(q, ti), blk(k, tj), blk(v, tj), blk(out, ti), blk(dout, ti), lse_i)
+        acc = sp.ring_block_step_backward(*args, P, i, j, order, tpos)
+        once = [a.clone() for a in acc]
+        sp.ring_block_step_backward(*args, P, i, j, order, tpos, dq_acc=acc[0], dk_acc=acc[1],
+                                    dv_acc=acc[2])
+        torch.cuda.synchronize()
+        ref = oracle.ring_partial_backward(*(np32(a) for a in args[:5]), lse_i.cpu().numpy(), S,
+                                           P, i, j, order, pos)
+        for name, got, first, r in zip(("dq", "dk", "dv"), acc, once, ref):
+            if name == "dq":
+                tol = 1e-5 * float(first.abs().max()) + 1e-30
+                assert float((got - 2 * first).abs().max()) <= tol, f"{_id(case)} dq not additive"
+            else:
+                assert torch.equal(got, first + first), f"{_id(case)} {name} not additive"
+            check_grad(first.cpu().numpy(), r, "bf16", f"{_id(case)} i={i} j={j} {name}")
