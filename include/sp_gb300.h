@@ -378,8 +378,11 @@ sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const void* v, con
  * position_ids [B][S] of the whole sequence or NULL (non-causal).
  * dq_acc [B][S/P][Hq][d], dk_acc, dv_acc [B][S/P][Hkv][d]: float32
  * accumulators, read and written (the caller zeroes them before the first
- * step).  Supported: SP_BF16 with d == 128 (tensor cores; P and dS rounded
- * to bf16 before the products, float32 accumulation), else
+ * step); the pieces of one call (dq: one per key tile; dk, dv: one per
+ * query head of the group) are added in no fixed order, so results are
+ * reproducible to float32 rounding.  Supported: SP_BF16 with d == 128
+ * (tensor cores; P and dS rounded to bf16 before the products, float32
+ * accumulation), else
  * SP_ERR_UNSUPPORTED; tensor pointers 16-byte aligned.  workspace:
  * sp_ring_block_step_bwd_workspace_bytes(B, S, Hq, P, position_ids != NULL)
  * bytes, 256-byte aligned.  Errors as for sp_blockwise_attn_bwd, and

@@ -20,8 +20,9 @@
 //    multiplied once and give dV, dK and the tile's piece of dQ, which the
 //    TMA adds into a float32 accumulator (bulk reductions); a last kernel
 //    scales and rounds dq.  Per-device mode: one query block against one
-//    key/value block from block tensors, dK/dV added into float32
-//    accumulators (the backward of one ring step on one device).
+//    key/value block from block tensors, one CTA per key tile and query
+//    head, dK/dV added into float32 accumulators by reductions (the
+//    backward of one ring step on one device).
 //  * two kernels, no atomics (bit-reproducible): dQ query-stationary -- one
 //    CTA keeps a 128-row Q tile and its dO tile and walks the key/value
 //    blocks in ring order j = (i - s) mod P ("Ring Attention", "Cómo
@@ -913,6 +914,12 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t x, uint32_t y, ui
                : "memory");
 }
 
+__device__ __forceinline__ void red_add_v4(float* addr, float x, float y, float z, float w) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(x),
+               "f"(y), "f"(z), "f"(w)
+               : "memory");
+}
+
 // dst[i] += src[i] for `bytes` / 4 floats, by the TMA unit (bulk group of the
 // issuing thread; both addresses 16-byte aligned, bytes a multiple of 16).
 __device__ __forceinline__ void bulk_reduce_add_f32(float* dst, uint32_t src, uint32_t bytes) {
@@ -970,12 +977,19 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
   // per-device form: one block in the tensor maps, the per-query arrays and
   // the dQ accumulator
+  // (in the per-device form every query head has its CTAs -- one block
+  // pair alone gives too few CTAs per key/value head to fill the GPU -- and
+  // the heads of a GQA group add into the accumulators by reductions)
   const bool per_dev = bb.q_block >= 0;
   const int P_arr = per_dev ? 1 : a.P;
   const int map_order = per_dev ? static_cast<int>(SP_ORDER_CONTIGUOUS) : a.order;
-  const int BH = a.B * a.Hkv;
+  const int G = a.Hq / a.Hkv;
+  const int n_heads = per_dev ? a.Hq : a.Hkv;
+  const int BH = a.B * n_heads;
   const int pos = blockIdx.x / BH, bh = blockIdx.x % BH;
-  const int b = bh / a.Hkv, hk = bh % a.Hkv;
+  const int b = bh / n_heads;
+  const int hk = per_dev ? (bh % n_heads) / G : bh % n_heads;
+  const int g_begin = per_dev ? (bh % n_heads) % G : 0, g_end = per_dev ? g_begin + 1 : G;
   const int j = per_dev ? bb.kv_block : pos / n_tiles_k, kt = per_dev ? pos : pos % n_tiles_k;
   const int Lb = a.S / a.P, w0 = kt * kT;
   const int k_first = static_cast<int>(block_token(a.order, a.S, a.P, j, w0));
@@ -1017,7 +1031,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
   if (warp == kFProducer) {
     // ------------------------------------------------------------ producer
-    const int G = a.Hq / a.Hkv;
     if (lane == 0) {
       prefetch_tmap(&tm.k);
       prefetch_tmap(&tm.v);
@@ -1032,7 +1045,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const uint32_t col_bytes = (ds_row ? 3 : 2) * kQT * 4;
     int n = 0, n_do = 0;  // Q tiles and dO tiles issued
     bool ok = true, ended = false;
-    for (int g = 0; g < G && ok; ++g) {
+    for (int g = g_begin; g < g_end && ok; ++g) {
       const int h = hk * G + g;
       const long long bhq = static_cast<long long>(b) * a.Hq + h;
       for (int s = 0; s < a.P && ok; ++s) {
@@ -1040,10 +1053,47 @@ __global__ void __launch_bounds__(kFThreads, 1)
         if (per_dev && i != bb.q_block) continue;
         int qt0, qt1;
         block_tiles(a.order, a.S, a.P, i, ds_row ? k_first : 0, a.S - 1, kQT, qt0, qt1);
-        for (int base = qt0; base <= qt1 && ok; base += 32) {
-          const int qt = base + lane;
-          bool stop = false, full = true;
-          if (ds_row && qt <= qt1) {
+        // Q, dO and the column data of query tile qt into the next slots
+        auto issue_tile = [&](int qt, bool full) -> bool {
+          const int slot = n % kQSlots;
+          if (!wait_warp(smem_u32(&q_empty[slot]), ((n / kQSlots) & 1) ^ 1, abort_flag, a.err,
+                         kErrBwdKvEmpty))
+            return false;
+          const int u0 = qt * kQT;
+          if (lane == 0) {
+            ColData& cd = cols[slot];
+            cd.info = full ? kInfoFull : kInfoTile;
+            cd.i = i;
+            cd.u0 = u0;
+            cd.h = h;
+            const uint32_t bar = smem_u32(&q_full[slot]);
+            mbar_arrive_expect_tx(bar, kTileBytes + col_bytes);
+            row_tma(sq + slot * kTileBytes, &tm.q, bar, h, map_order, per_dev ? 0 : i, u0, b);
+            const long long off = blk_index(bhq, P_arr, a.Lbp, per_dev ? 0 : i, u0);
+            bulk_load(smem_u32(cd.lse2), a.lse2_blk + off, kQT * 4, bar);
+            bulk_load(smem_u32(cd.D), a.D_blk + off, kQT * 4, bar);
+            if (ds_row)
+              bulk_load(smem_u32(cd.lo),
+                        a.lo_blk + blk_index(lo_row, P_arr, a.Lbp, per_dev ? 0 : i, u0),
+                        kQT * 4, bar);
+          }
+          ++n;
+          if (!wait_warp(smem_u32(&do_empty), (n_do & 1) ^ 1, abort_flag, a.err,
+                         kErrBwdKvEmpty))
+            return false;
+          if (lane == 0) {
+            const uint32_t bar = smem_u32(&do_full);
+            mbar_arrive_expect_tx(bar, kTileBytes);
+            row_tma(sdo, &tm.dout, bar, h, map_order, per_dev ? 0 : i, u0, b);
+          }
+          ++n_do;
+          return true;
+        };
+        // skip/full flags of query tile qt (lane-parallel, 32 tiles at a time)
+        auto flags = [&](int qt, bool& stop, bool& full) {
+          stop = false;
+          full = true;
+          if (ds_row) {
             const int u0 = qt * kQT;
             const int tq_first = static_cast<int>(block_token(a.order, a.S, a.P, i, u0));
             const int tq_last =
@@ -1051,49 +1101,43 @@ __global__ void __launch_bounds__(kFThreads, 1)
             stop = ds_row[tq_first] > k_last;
             full = k_last <= tq_first && ds_row[tq_last] <= k_first;
           }
-          const unsigned stops = __ballot_sync(0xffffffffu, stop);
-          const unsigned fulls = __ballot_sync(0xffffffffu, full);
-          int cnt = min(32, qt1 - base + 1);
-          if (stops) cnt = min(cnt, __ffs(static_cast<int>(stops)) - 1);
-          for (int e = 0; e < cnt; ++e) {
-            const int slot = n % kQSlots;
-            if (!wait_warp(smem_u32(&q_empty[slot]), ((n / kQSlots) & 1) ^ 1, abort_flag, a.err,
-                           kErrBwdKvEmpty)) {
-              ok = false;
-              break;
-            }
-            const int u0 = (base + e) * kQT;
-            if (lane == 0) {
-              ColData& cd = cols[slot];
-              cd.info = (fulls >> e) & 1u ? kInfoFull : kInfoTile;
-              cd.i = i;
-              cd.u0 = u0;
-              cd.h = h;
-              const uint32_t bar = smem_u32(&q_full[slot]);
-              mbar_arrive_expect_tx(bar, kTileBytes + col_bytes);
-              row_tma(sq + slot * kTileBytes, &tm.q, bar, h, map_order, per_dev ? 0 : i, u0, b);
-              const long long off = blk_index(bhq, P_arr, a.Lbp, per_dev ? 0 : i, u0);
-              bulk_load(smem_u32(cd.lse2), a.lse2_blk + off, kQT * 4, bar);
-              bulk_load(smem_u32(cd.D), a.D_blk + off, kQT * 4, bar);
-              if (ds_row)
-                bulk_load(smem_u32(cd.lo),
-                          a.lo_blk + blk_index(lo_row, P_arr, a.Lbp, per_dev ? 0 : i, u0),
-                          kQT * 4, bar);
-            }
-            ++n;
-            if (!wait_warp(smem_u32(&do_empty), (n_do & 1) ^ 1, abort_flag, a.err,
-                           kErrBwdKvEmpty)) {
-              ok = false;
-              break;
-            }
-            if (lane == 0) {
-              const uint32_t bar = smem_u32(&do_full);
-              mbar_arrive_expect_tx(bar, kTileBytes);
-              row_tma(sdo, &tm.dout, bar, h, map_order, per_dev ? 0 : i, u0, b);
-            }
-            ++n_do;
+        };
+        if (!per_dev) {
+          for (int base = qt0; base <= qt1 && ok; base += 32) {
+            bool stop = false, full = true;
+            if (base + lane <= qt1) flags(base + lane, stop, full);
+            const unsigned stops = __ballot_sync(0xffffffffu, stop);
+            const unsigned fulls = __ballot_sync(0xffffffffu, full);
+            int cnt = min(32, qt1 - base + 1);
+            if (stops) cnt = min(cnt, __ffs(static_cast<int>(stops)) - 1);
+            for (int e = 0; e < cnt && ok; ++e) ok = issue_tile(base + e, (fulls >> e) & 1u);
+            if (stops) break;
           }
-          if (stops) break;
+          continue;
+        }
+        // Per-device form: the walk is trimmed at its first tile past the
+        // keys' documents and starts at a tile that depends on the key tile
+        // -- otherwise the key tiles of a head walk the same query tiles in
+        // step and reduce into the same dQ tile at once.
+        int n_walk = qt1 - qt0 + 1;
+        for (int base = qt0; base <= qt1; base += 32) {
+          bool stop = false, full = true;
+          if (base + lane <= qt1) flags(base + lane, stop, full);
+          const unsigned stops = __ballot_sync(0xffffffffu, stop);
+          if (stops) {
+            n_walk = base + __ffs(static_cast<int>(stops)) - 1 - qt0;
+            break;
+          }
+        }
+        const int rot = n_walk > 0 ? kt % n_walk : 0;
+        for (int base = 0; base < n_walk && ok; base += 32) {
+          const int idx = base + lane;
+          bool stop = false, full = true;
+          if (idx < n_walk) flags(qt0 + (idx + rot) % n_walk, stop, full);
+          const unsigned fulls = __ballot_sync(0xffffffffu, full);
+          const int cnt = min(32, n_walk - base);
+          for (int e = 0; e < cnt && ok; ++e)
+            ok = issue_tile(qt0 + (base + e + rot) % n_walk, (fulls >> e) & 1u);
         }
       }
     }
@@ -1387,16 +1431,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
         if (per_dev) {
           if (key_live && have && ok) {
-            float4* acc = reinterpret_cast<float4*>((m == 0 ? bb.dk_acc : bb.dv_acc) + lrow);
+            float* acc = (m == 0 ? bb.dk_acc : bb.dv_acc) + lrow + c * 32;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              float4 v4 = acc[c * 8 + e];
-              v4.x += __uint_as_float(x[4 * e]) * mul;
-              v4.y += __uint_as_float(x[4 * e + 1]) * mul;
-              v4.z += __uint_as_float(x[4 * e + 2]) * mul;
-              v4.w += __uint_as_float(x[4 * e + 3]) * mul;
-              acc[c * 8 + e] = v4;
-            }
+            for (int e = 0; e < 8; ++e)
+              red_add_v4(acc + 4 * e, __uint_as_float(x[4 * e]) * mul,
+                         __uint_as_float(x[4 * e + 1]) * mul, __uint_as_float(x[4 * e + 2]) * mul,
+                         __uint_as_float(x[4 * e + 3]) * mul);
           }
           continue;
         }
@@ -1422,14 +1462,32 @@ __global__ void __launch_bounds__(kFThreads, 1)
   }
 }
 
-// dq = scale * (the fp32 sums), bf16, in [B][S][Hq][d].  One CTA per 64 KiB
-// accumulator block (128 rows of one block and head): thread (row r, half
-// g0) writes 16-byte pieces of row r's 256 output bytes; the reads of a warp
-// cover 512 contiguous bytes.
+// One 64 KiB accumulator block ([column quad 32][row 128][4] floats: rows
+// u0 .. u0 + 127 of one block and head) read into shared memory half a block
+// (16 quads) at a time, so that both sides are contiguous: the reads in the
+// block's own order, the writes along each row.  Padded to 129 rows per quad
+// so that the 16 lanes reading one row from 16 quads hit distinct banks.
+constexpr int kQuadsPerPass = 16;
+struct AccHalf {
+  float4 v[kQuadsPerPass][kQT + 1];
+};
+
+__device__ __forceinline__ void load_acc_half(AccHalf& sm, const float4* __restrict__ blk,
+                                              int pass) {
+  const float4* src = blk + pass * kQuadsPerPass * kQT;
+#pragma unroll 4
+  for (int e = threadIdx.x; e < kQuadsPerPass * kQT; e += 256)
+    sm.v[e / kQT][e % kQT] = src[e];
+}
+
+// dq = scale * (the fp32 sums), bf16, in [B][S][Hq][d].  One CTA per
+// accumulator block; per pass a half-warp writes 64 columns (128 bytes) of
+// one row.
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __restrict__ acc,
                                                              __nv_bfloat16* dq, int S, int Hq,
                                                              int P, int Lbp, int order,
                                                              float scale) {
+  __shared__ AccHalf sm;
   const int tiles = Lbp / kQT;
   const long long blk = blockIdx.x;  // ((b * Hq + h) * P + i) * tiles + tile
   const int tile = static_cast<int>(blk % tiles);
@@ -1438,45 +1496,59 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __res
   const long long bh = bhp / P;
   const int h = static_cast<int>(bh % Hq);
   const long long b = bh / Hq;
-  const int r = threadIdx.x & (kQT - 1), g0 = threadIdx.x >> 7;
-  const int u = tile * kQT + r;
-  if (u >= S / P) return;
-  const long long t = block_token(order, S, P, i, u);
-  const float4* src = acc + blk * (kQT * kD / 4) + r;
-  uint4* dst = reinterpret_cast<uint4*>(dq + ((b * S + t) * Hq + h) * kD);
-#pragma unroll 4
-  for (int g = g0; g < kD / 8; g += 2) {  // 8 columns: quads 2g and 2g + 1
-    const float4 lo = src[(2 * g) * kQT], hi = src[(2 * g + 1) * kQT];
-    dst[g] = make_uint4(pack_bf16(lo.x * scale, lo.y * scale), pack_bf16(lo.z * scale, lo.w * scale),
-                        pack_bf16(hi.x * scale, hi.y * scale), pack_bf16(hi.z * scale, hi.w * scale));
+  const int Lb = S / P;
+  const int l16 = threadIdx.x & 15, row0 = threadIdx.x >> 4;  // 16 rows per sweep
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    if (pass) __syncthreads();
+    load_acc_half(sm, acc + blk * (kQT * kD / 4), pass);
+    __syncthreads();
+#pragma unroll 1
+    for (int r = row0; r < kQT; r += 16) {
+      const int u = tile * kQT + r;
+      if (u >= Lb) break;
+      const long long t = block_token(order, S, P, i, u);
+      const float4 x = sm.v[l16][r];
+      uint2* dst = reinterpret_cast<uint2*>(dq + ((b * S + t) * Hq + h) * kD +
+                                            (pass * kQuadsPerPass + l16) * 4);
+      *dst = make_uint2(pack_bf16(x.x * scale, x.y * scale), pack_bf16(x.z * scale, x.w * scale));
+    }
   }
 }
 
 // Per-device form: dq_acc[b][u][h][:] += scale * (the fp32 sums of block i),
-// float32, [B][S/P][Hq][d]; the blocked accumulator holds one block.
+// float32, [B][S/P][Hq][d]; the blocked accumulator holds one block.  Same
+// staging as bwd_dq_convert_kernel; a half-warp updates 64 columns (256
+// bytes) of one row.
 __global__ void __launch_bounds__(256) bwd_dq_add_kernel(const float4* __restrict__ acc,
                                                          float4* dq_acc, int Lb, int Hq, int Lbp,
                                                          float scale) {
+  __shared__ AccHalf sm;
   const int tiles = Lbp / kQT;
   const long long blk = blockIdx.x;  // (b * Hq + h) * tiles + tile
   const int tile = static_cast<int>(blk % tiles);
   const long long bh = blk / tiles;
   const int h = static_cast<int>(bh % Hq);
   const long long b = bh / Hq;
-  const int r = threadIdx.x & (kQT - 1), g0 = threadIdx.x >> 7;
-  const int u = tile * kQT + r;
-  if (u >= Lb) return;
-  const float4* src = acc + blk * (kQT * kD / 4) + r;
-  float4* dst = dq_acc + ((b * Lb + u) * Hq + h) * (kD / 4);
-#pragma unroll 4
-  for (int q = g0; q < kD / 4; q += 2) {
-    const float4 x = src[q * kQT];
-    float4 y = dst[q];
-    y.x += x.x * scale;
-    y.y += x.y * scale;
-    y.z += x.z * scale;
-    y.w += x.w * scale;
-    dst[q] = y;
+  const int l16 = threadIdx.x & 15, row0 = threadIdx.x >> 4;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    if (pass) __syncthreads();
+    load_acc_half(sm, acc + blk * (kQT * kD / 4), pass);
+    __syncthreads();
+#pragma unroll 1
+    for (int r = row0; r < kQT; r += 16) {
+      const int u = tile * kQT + r;
+      if (u >= Lb) break;
+      const float4 x = sm.v[l16][r];
+      float4* dst = dq_acc + ((b * Lb + u) * Hq + h) * (kD / 4) + pass * kQuadsPerPass + l16;
+      float4 y = *dst;
+      y.x += x.x * scale;
+      y.y += x.y * scale;
+      y.z += x.z * scale;
+      y.w += x.w * scale;
+      *dst = y;
+    }
   }
 }
 
@@ -1602,9 +1674,9 @@ int launch_attn_bwd_bf16_block(const BwdArgs& a, int qb, int kb, float* dq_block
   if (cudaFuncSetAttribute(bwd_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            f_smem) != cudaSuccess)
     return -1;
-  const unsigned n_kv = static_cast<unsigned>(n_tiles) * a.B * a.Hkv;
-  bwd_fused_kernel<<<n_kv, kFThreads, f_smem, st>>>(tm, a, n_tiles, dq_blocked,
-                                                     BwdBlock{qb, kb, dk_acc, dv_acc});
+  const unsigned n_cta = static_cast<unsigned>(n_tiles) * a.B * a.Hq;  // one per query head
+  bwd_fused_kernel<<<n_cta, kFThreads, f_smem, st>>>(tm, a, n_tiles, dq_blocked,
+                                                      BwdBlock{qb, kb, dk_acc, dv_acc});
   const unsigned n_blk =
       static_cast<unsigned>(static_cast<long long>(a.B) * a.Hq * (a.Lbp / kQT));
   bwd_dq_add_kernel<<<n_blk, 256, 0, st>>>(reinterpret_cast<const float4*>(dq_blocked),
