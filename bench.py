@@ -24,8 +24,9 @@ during the timed region; under "extra", each other timed workload with its
 own roofline fraction and clock record: the Ulysses layer of ulysses_4k
 (with the permutation's bandwidth in both directions, also reported under
 "permute"), packed_128k in both block orders, halfmil_512k striped, the
-llama8b_32k backward, the fused Ulysses path, the Ulysses + Ring hybrid and
-two large permutations.
+llama8b_32k backward in both dQ forms and the packed_128k striped backward,
+the backward of an 8-device ring simulated through the per-device calls, the
+fused Ulysses path, the Ulysses + Ring hybrid and two large permutations.
 
 Multi-GPU: every rank runs its own independent replica of the step (the
 head groups / batches of the path are independent; no collective on the data
@@ -597,6 +598,9 @@ def extra_measurements(args, peaks, peak_kind, flush):
         res[f"{name}_{order}"] = causal_attention_measurement(name, order, peaks, peak_kind, flush,
                                                               stream, reps)
     res["llama8b_32k_causal_backward"] = backward_measurement(peaks, flush, stream)
+    res["packed_128k_striped_backward"] = backward_measurement(
+        peaks, flush, stream, "packed_128k", "striped", reps=10, two_forms=False)
+    res["llama8b_32k_ring_backward_per_device"] = ring_backward_measurement(peaks, flush, stream)
     res.update(next_row_measurements(peaks, flush, stream))
     # the q shapes of llama8b_32k (256 MiB) and packed_128k (1 GiB)
     for S_, label in ((32768, "permute_256MiB"), (131072, "permute_1GiB")):
@@ -667,21 +671,21 @@ def next_row_measurements(peaks, flush, stream):
     return res
 
 
-def backward_measurement(peaks, flush, stream, reps=20):
-    """Attention backward (dq, dk, dv) on llama8b_32k, L2 flushed between
-    reps, in both forms: the default (doc_start scan, prep, the fused
-    kernel -- S^T and dP^T once per pair of tiles, dQ pieces summed by TMA
-    bulk reductions -- and the dq conversion) and the bit-reproducible
-    two-kernel form (dQ recomputed by its own kernel).  Algorithmic FLOPs =
-    2.5 x the forward's (five d-long products per allowed pair: S, dP, dV,
-    dQ, dK)."""
+def backward_measurement(peaks, flush, stream, name="llama8b_32k", order="contiguous", reps=20,
+                         two_forms=True):
+    """Attention backward (dq, dk, dv), L2 flushed between reps, in the
+    default form (doc_start scan, prep, the fused kernel -- S^T and dP^T
+    once per pair of tiles, dQ pieces summed by TMA bulk reductions -- and
+    the dq conversion) and, with two_forms, the bit-reproducible two-kernel
+    form (dQ recomputed by its own kernel).  Algorithmic FLOPs = 2.5 x the
+    forward's (five d-long products per allowed pair: S, dP, dV, dQ, dK)."""
     import torch
 
     import sequence_parallelism_gb300 as sp
     import workloads
     from sequence_parallelism_gb300 import _lib
 
-    cfg = workloads.CONFIGS["llama8b_32k"]
+    cfg = workloads.CONFIGS[name]
     B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
     q, k, v = workloads.qkv_torch(B, S, Hq, Hkv, d, cfg["seed"], torch.bfloat16, "cuda")
     g = torch.Generator(device="cuda")
@@ -689,11 +693,11 @@ def backward_measurement(peaks, flush, stream, reps=20):
     dout = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
     pos_np = workloads.position_ids(cfg)
     pos = torch.from_numpy(pos_np).cuda()
-    out, lse = sp.blockwise_attention(q, k, v, P, "contiguous", pos)
+    out, lse = sp.blockwise_attention(q, k, v, P, order, pos)
     ws = torch.empty(_lib.sp_blockwise_attn_bwd_workspace_bytes(B, S, Hq, P, True),
                      dtype=torch.uint8, device="cuda")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    call = lambda: _lib.sp_blockwise_attn_bwd(q, k, v, out, dout, lse, pos, P, "contiguous", 0.0,
+    call = lambda: _lib.sp_blockwise_attn_bwd(q, k, v, out, dout, lse, pos, P, order, 0.0,
                                               dq, dk, dv, ws)
     fl = 2.5 * attention_flops(cfg, pos_np)
 
@@ -712,13 +716,67 @@ def backward_measurement(peaks, flush, stream, reps=20):
                 "launches_per_call": launches, "clocks": clocks}
 
     res = one(True)
-    res.update({"flops": fl, "reps": reps,
+    res.update({"workload": name, "order": order, "flops": fl, "reps": reps,
                 "note": "doc_start scan + prep + fused dK/dV/dQ kernel (dQ pieces summed "
                         "by TMA bulk reductions into float32) + dq conversion, median of "
-                        "reps; flops = 2.5 x forward (S, dP, dV, dQ, dK)",
-                "two_kernel_form": dict(one(False), note="doc_start scan + prep + dQ + dK/dV "
-                                        "kernels (dQ recomputed; bit-reproducible)")})
+                        "reps; flops = 2.5 x forward (S, dP, dV, dQ, dK)"})
+    if two_forms:
+        res["two_kernel_form"] = dict(one(False), note="doc_start scan + prep + dQ + dK/dV "
+                                      "kernels (dQ recomputed; bit-reproducible)")
     return res
+
+
+def ring_backward_measurement(peaks, flush, stream, reps=5):
+    """The backward of an 8-device ring simulated on one GPU (llama8b_32k,
+    contiguous blocks): every device's P steps as sp_ring_block_step_bwd
+    calls on block tensors, P^2 = 64 calls per rep, float32 accumulators;
+    what one device of a real ring computes is 1/P of it.  Same FLOP rule
+    as the whole-sequence backward."""
+    import torch
+
+    import sequence_parallelism_gb300 as sp
+    import workloads
+    from sequence_parallelism_gb300 import _lib
+
+    cfg = workloads.CONFIGS["llama8b_32k"]
+    B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
+    q, k, v = workloads.qkv_torch(B, S, Hq, Hkv, d, cfg["seed"], torch.bfloat16, "cuda")
+    g = torch.Generator(device="cuda")
+    g.manual_seed(cfg["seed"] + 7)
+    dout = torch.randn(q.shape, generator=g, device="cuda").to(torch.bfloat16)
+    pos_np = workloads.position_ids(cfg)
+    pos = torch.from_numpy(pos_np).cuda()
+    out, lse = sp.blockwise_attention(q, k, v, P, "contiguous", pos)
+    Lb = S // P
+    rows = [torch.arange(p * Lb, (p + 1) * Lb, device="cuda") for p in range(P)]
+    blk = lambda t, p, ax=1: t.index_select(ax, rows[p]).contiguous()
+    qb, kb, vb = [blk(q, p) for p in range(P)], [blk(k, p) for p in range(P)], [blk(v, p) for p in range(P)]
+    ob, db, lb = [blk(out, p) for p in range(P)], [blk(dout, p) for p in range(P)], [blk(lse, p, 2) for p in range(P)]
+    del q, k, v, out, dout, lse
+    acc = [(torch.zeros((B, Lb, Hq, d), device="cuda"), torch.zeros((B, Lb, Hkv, d), device="cuda"),
+            torch.zeros((B, Lb, Hkv, d), device="cuda")) for _ in range(P)]
+    ws = torch.empty(_lib.sp_ring_block_step_bwd_workspace_bytes(B, S, Hq, P, True),
+                     dtype=torch.uint8, device="cuda")
+
+    def ring():
+        for i in range(P):
+            for s_ in range(P):
+                j = (i - s_) % P
+                _lib.sp_ring_block_step_bwd(qb[i], kb[j], vb[j], ob[i], db[i], lb[i], pos, S, P,
+                                            "contiguous", i, j, 0.0, acc[i][0], acc[j][1],
+                                            acc[j][2], ws)
+
+    t, _, clocks = _timed(ring, flush, stream, reps)
+    st_, code = _lib.sp_get_device_error(ws)
+    if st_ != 0:
+        raise RuntimeError(f"device error word {code:#x} in the ring backward")
+    fl = 2.5 * attention_flops(cfg, pos_np)
+    tf = fl / (t * 1e-3) / 1e12
+    return {"ms": round(t, 4), "TFLOP/s": round(tf, 1),
+            "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+            "calls_per_rep": P * P, "reps": reps, "clocks": clocks,
+            "note": "64 sp_ring_block_step_bwd calls (8 simulated devices x 8 ring steps; "
+                    "causal pairs with j > i find no allowed tile), median of reps"}
 
 
 # ------------------------------------------------------- CPU oracle leg
