@@ -59,7 +59,13 @@ def request_spec(name):
 BACKWARD_REQUESTS = {  # name: (workload, order)
     "bwd_llama8b_32k": ("llama8b_32k", "contiguous"),
     "bwd_packed_128k_striped": ("packed_128k", "striped"),
+    "bwd_halfmil_512k_striped": ("halfmil_512k", "striped"),
 }
+# Above this many tokens in one document, the sampled keys are only the
+# sequence's last BACKWARD_TAIL_KEYS (their observers are few); a key
+# further in is seen by up to S queries, whose statistics the oracle needs.
+BACKWARD_TAIL_ONLY = 1 << 18
+BACKWARD_TAIL_KEYS = 64
 BACKWARD_DQ_ROWS = 512
 
 
@@ -142,9 +148,13 @@ def backward_keys(pos, S, P, order):
     """Key tokens whose observers are cheap to enumerate: the last 16 tokens
     of every document, every token of documents up to 128 long, the first 16
     of documents up to 5000 long; for a single document, 48 seeded keys of
-    the last block and the first 8 keys of that block."""
+    the last block and the first 8 keys of that block -- or, for a single
+    document longer than BACKWARD_TAIL_ONLY, its last BACKWARD_TAIL_KEYS
+    tokens only."""
     import oracle
     seg_starts = np.nonzero(pos[0] == 0)[0]
+    if len(seg_starts) == 1 and S > BACKWARD_TAIL_ONLY:
+        return np.arange(S - BACKWARD_TAIL_KEYS, S, dtype=np.int64)
     ends = np.append(seg_starts[1:], S)
     keys = set()
     for a, e in zip(seg_starts, ends):

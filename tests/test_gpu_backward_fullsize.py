@@ -6,7 +6,9 @@ start (tests/fullsize_oracle.py):
   (oracle.attention_backward_rows);
 * dk, dv on sampled key rows of every key/value head: every query that sees
   them enters with its full softmax statistics, summed over the query heads
-  of the group (oracle.attention_backward_keys);
+  of the group (oracle.attention_backward_keys); at halfmil_512k (one
+  document of 524288 tokens in 16 striped blocks) the sampled keys are the
+  last 64 tokens, the only ones whose observers the oracle can afford;
 * sum rules that hold at any size, on the whole tensors: the rows of dS sum
   to zero, so sum_j dk_j = 0; the rows of P sum to one, so sum_j dv_j equals
   the sum of dout over the group's query heads.
@@ -36,6 +38,8 @@ def sp():
                  marks=pytest.mark.fullsize_oracle("bwd_llama8b_32k")),
     pytest.param("bwd_packed_128k_striped", "packed_128k", "striped",
                  marks=pytest.mark.fullsize_oracle("bwd_packed_128k_striped")),
+    pytest.param("bwd_halfmil_512k_striped", "halfmil_512k", "striped",
+                 marks=pytest.mark.fullsize_oracle("bwd_halfmil_512k_striped")),
 ])
 def test_backward_full_size(sp, fullsize_oracle, name, workload, order):
     cfg = workloads.CONFIGS[workload]
@@ -71,14 +75,18 @@ def test_backward_full_size(sp, fullsize_oracle, name, workload, order):
 
 
 @pytest.mark.parametrize("workload,order", [("llama8b_32k", "contiguous"),
-                                            ("packed_128k", "striped")])
+                                            ("packed_128k", "striped"),
+                                            ("halfmil_512k", "striped")])
 def test_backward_forms_agree_everywhere(sp, workload, order):
     """Every element of both forms of the bf16 backward at full size: dk and
-    dv bit-identical (the same products in the same order), dq within one
-    bf16 step of the two-kernel form (the fused form adds dQ's per-tile
-    pieces in float32 in no fixed order).  The default (fused) form is the
-    one compared with the oracle above on sampled rows and keys; this
-    extends the check to every row."""
+    dv bit-identical (the same products in the same order); dq within one
+    bf16 step of the two-kernel form plus 1e-4 of the tensor's largest
+    magnitude -- the fused form adds dQ's per-key-tile pieces (up to 4096
+    at halfmil_512k) in float32 in no fixed order, and where those pieces
+    cancel, the reassociation error of the float32 sum can exceed one bf16
+    step of a small result.  The default (fused) form is the one compared
+    with the oracle above on sampled rows and keys; this extends the check
+    to every row."""
     from sequence_parallelism_gb300 import _lib
     cfg = workloads.CONFIGS[workload]
     B, S, Hq, Hkv, d, P = (cfg[x] for x in ("B", "S", "Hq", "Hkv", "d", "P"))
@@ -98,9 +106,12 @@ def test_backward_forms_agree_everywhere(sp, workload, order):
     assert torch.equal(dk_f, dk_r), f"{workload}: dk differs between the forms"
     assert torch.equal(dv_f, dv_r), f"{workload}: dv differs between the forms"
     a, b = dq_f.float(), dq_r.float()
-    step = torch.maximum(a.abs(), b.abs()) * 2.0 ** -7 + float(b.abs().max()) * 1e-6
-    bad = int(((a - b).abs() > step).sum())
+    scale = float(b.abs().max())
+    step = torch.maximum(a.abs(), b.abs()) * 2.0 ** -7
+    excess = ((a - b).abs() - step).clamp(min=0.0)
+    beyond = int((excess > 1e-6 * scale).sum())
     diff = int((a != b).sum())
+    worst = float(excess.max()) / scale
     print(f"PARITY-FORMS {workload} {order}: dq elements differing {diff} of {a.numel()}, "
-          f"beyond one bf16 step {bad}")
-    assert bad == 0, f"{workload}: {bad} dq elements differ by more than one bf16 step"
+          f"beyond one bf16 step + 1e-6 of max |dq| {beyond} (largest excess {worst:.2e})")
+    assert worst <= 1e-4, f"{workload}: dq differs beyond one bf16 step by {worst:.2e} of max |dq|"
