@@ -24,7 +24,8 @@ during the timed region; under "extra", each other timed workload with its
 own roofline fraction and clock record: the Ulysses layer of ulysses_4k
 (with the permutation's bandwidth in both directions, also reported under
 "permute"), packed_128k in both block orders, halfmil_512k striped, the
-llama8b_32k backward in both dQ forms and the packed_128k striped backward,
+llama8b_32k backward in both dQ forms, the packed_128k and halfmil_512k
+striped backwards,
 the backward of an 8-device ring simulated through the per-device calls, the
 fused Ulysses path, the Ulysses + Ring hybrid and two large permutations.
 
@@ -600,6 +601,8 @@ def extra_measurements(args, peaks, peak_kind, flush):
     res["llama8b_32k_causal_backward"] = backward_measurement(peaks, flush, stream)
     res["packed_128k_striped_backward"] = backward_measurement(
         peaks, flush, stream, "packed_128k", "striped", reps=10, two_forms=False)
+    res["halfmil_512k_striped_backward"] = backward_measurement(
+        peaks, flush, stream, "halfmil_512k", "striped", reps=3, two_forms=False)
     res["llama8b_32k_ring_backward_per_device"] = ring_backward_measurement(peaks, flush, stream)
     res.update(next_row_measurements(peaks, flush, stream))
     # the q shapes of llama8b_32k (256 MiB) and packed_128k (1 GiB)
