@@ -26,7 +26,8 @@ own roofline fraction and clock record: the Ulysses layer of ulysses_4k
 "permute"), packed_128k in both block orders, halfmil_512k striped, the
 llama8b_32k backward in both dQ forms, the packed_128k and halfmil_512k
 striped backwards,
-the backward of an 8-device ring simulated through the per-device calls, the
+the forward and backward of an 8-device ring simulated through the per-device
+calls, the
 fused Ulysses path, the Ulysses + Ring hybrid and two large permutations.
 
 Multi-GPU: every rank runs its own independent replica of the step (the
@@ -603,6 +604,7 @@ def extra_measurements(args, peaks, peak_kind, flush):
         peaks, flush, stream, "packed_128k", "striped", reps=10, two_forms=False)
     res["halfmil_512k_striped_backward"] = backward_measurement(
         peaks, flush, stream, "halfmil_512k", "striped", reps=3, two_forms=False)
+    res["llama8b_32k_ring_forward_per_device"] = ring_forward_measurement(peaks, flush, stream)
     res["llama8b_32k_ring_backward_per_device"] = ring_backward_measurement(peaks, flush, stream)
     res.update(next_row_measurements(peaks, flush, stream))
     # the q shapes of llama8b_32k (256 MiB) and packed_128k (1 GiB)
@@ -727,6 +729,60 @@ def backward_measurement(peaks, flush, stream, name="llama8b_32k", order="contig
         res["two_kernel_form"] = dict(one(False), note="doc_start scan + prep + dQ + dK/dV "
                                       "kernels (dQ recomputed; bit-reproducible)")
     return res
+
+
+def ring_forward_measurement(peaks, flush, stream, reps=10):
+    """The forward of an 8-device ring simulated on one GPU (llama8b_32k,
+    contiguous blocks), as dist.ring_attention runs it on each device: P
+    sp_ring_block_step calls per device, each partial folded into the
+    running result by sp_attn_merge_partials (P^2 = 64 steps, 56 merges per
+    rep).  FLOPs: the attention's algorithmic count."""
+    import torch
+
+    import sequence_parallelism_gb300 as sp
+    import workloads
+    from sequence_parallelism_gb300 import _lib
+
+    cfg = workloads.CONFIGS["llama8b_32k"]
+    B, S, Hq, Hkv, d, P = (cfg[k] for k in ("B", "S", "Hq", "Hkv", "d", "P"))
+    q, k, v = workloads.qkv_torch(B, S, Hq, Hkv, d, cfg["seed"], torch.bfloat16, "cuda")
+    pos_np = workloads.position_ids(cfg)
+    pos = torch.from_numpy(pos_np).cuda()
+    Lb = S // P
+    rows = [torch.arange(p * Lb, (p + 1) * Lb, device="cuda") for p in range(P)]
+    qb = [q.index_select(1, r).contiguous() for r in rows]
+    kb = [k.index_select(1, r).contiguous() for r in rows]
+    vb = [v.index_select(1, r).contiguous() for r in rows]
+    del q, k, v
+    outs = [torch.empty((2, B, Lb, Hq, d), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    lses = [torch.empty((2, B, Hq, Lb), dtype=torch.float32, device="cuda") for _ in range(2)]
+    ws = sp.attention_workspace(B, S, True)
+
+    def ring():
+        for i in range(P):
+            cur = 0
+            for s_ in range(P):
+                j = (i - s_) % P
+                slot = 0 if s_ == 0 else 1
+                _lib.sp_ring_block_step(qb[i], kb[j], vb[j], pos, S, P, "contiguous", i, j, 0.0,
+                                        outs[cur][slot], lses[cur][slot], ws)
+                if s_ > 0:
+                    _lib.sp_attn_merge_partials(outs[cur], lses[cur], outs[1 - cur][0],
+                                                lses[1 - cur][0])
+                    cur = 1 - cur
+
+    t, _, clocks = _timed(ring, flush, stream, reps)
+    st_, code = _lib.sp_get_device_error(ws)
+    if st_ != 0:
+        raise RuntimeError(f"device error word {code:#x} in the ring forward")
+    fl = attention_flops(cfg, pos_np)
+    tf = fl / (t * 1e-3) / 1e12
+    return {"ms": round(t, 4), "TFLOP/s": round(tf, 1),
+            "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+            "calls_per_rep": P * P, "merges_per_rep": P * (P - 1), "reps": reps,
+            "clocks": clocks,
+            "note": "64 sp_ring_block_step calls and 56 two-way merges (8 simulated devices x "
+                    "8 ring steps; causal pairs with j > i find no allowed tile), median of reps"}
 
 
 def ring_backward_measurement(peaks, flush, stream, reps=5):

@@ -5,8 +5,12 @@
 //
 //   lse = log sum_p exp(lse_p),  out = sum_p exp(lse_p - lse) * out_p
 //
-// One warp per (b, t, h) row; float32 arithmetic; memory-bound (it reads P
-// partial rows and writes one).
+// Memory-bound (it reads P partial rows and writes one); float32
+// arithmetic.  merge_vec_kernel: every lane owns one 16-byte piece of a row
+// (8 bf16 or 4 float32 values; a row of d = 128 bf16 is 16 lanes, so a warp
+// merges two rows with 16-byte loads), and computes the row's weights from
+// the P log-sum-exps itself; merge_kernel (one warp per row, element loads)
+// takes the head sizes that do not split into 16-byte pieces.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -87,6 +91,121 @@ __global__ void __launch_bounds__(256) merge_kernel(const T* __restrict__ outs,
   }
 }
 
+template <typename T>
+struct Vec;
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int kN = 8;
+  __device__ static void load(const uint4& u, float (&f)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+      f[2 * e] = x.x;
+      f[2 * e + 1] = x.y;
+    }
+  }
+  __device__ static uint4 store(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 x = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
+      w[e] = *reinterpret_cast<const uint32_t*>(&x);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+template <>
+struct Vec<float> {
+  static constexpr int kN = 4;
+  __device__ static void load(const uint4& u, float (&f)[4]) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+  }
+  __device__ static uint4 store(const float (&f)[4]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                      __float_as_uint(f[3]));
+  }
+};
+
+// lanes_per_row = d / Vec<T>::kN divides 32; the output and every partial
+// row are 16-byte aligned; P <= kMaxP.  Rows are visited token-fastest
+// within a (batch, head), so that neighbouring rows' log-sum-exps are
+// neighbours in memory, and every lane issues all loads of kRows rows (its
+// log-sum-exps and 16-byte pieces of every partial) before any arithmetic:
+// a merge moves little data per row, so loads in flight set its speed.
+template <typename T, int kMaxP, int kRows>
+__global__ void __launch_bounds__(256) merge_vec_kernel(const uint4* __restrict__ outs,
+                                                        const float* __restrict__ lses, int P,
+                                                        int B, int S, int H, int lanes_per_row,
+                                                        uint4* __restrict__ out,
+                                                        float* __restrict__ lse) {
+  constexpr int kN = Vec<T>::kN;
+  const int lane = threadIdx.x & 31;
+  const int rows_per_warp = 32 / lanes_per_row;
+  const int sub = lane / lanes_per_row, piece = lane % lanes_per_row;
+  const long long nrows = static_cast<long long>(B) * S * H;
+  const long long warp = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  const long long lse_pstride = static_cast<long long>(B) * H * S;
+  const long long out_pstride = nrows * lanes_per_row;  // in 16-byte pieces
+  const long long step = nwarps * rows_per_warp;        // rows per sweep of all warps
+  for (long long r0 = warp * rows_per_warp + sub; r0 < nrows; r0 += step * kRows) {
+    float l[kRows][kMaxP];
+    uint4 xv[kRows][kMaxP];
+    long long src[kRows];
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      const long long r = r0 + u * step;  // (b, h, t), t fastest: the lse index
+      const bool live = r < nrows;
+      const int t = static_cast<int>(r % S);
+      const long long bh = r / S;
+      const int h = static_cast<int>(bh % H);
+      const long long b = bh / H;
+      src[u] = ((b * S + t) * H + h) * lanes_per_row + piece;  // (b, t, h): the out index
+#pragma unroll
+      for (int p = 0; p < kMaxP; ++p) {
+        const bool on = live && p < P;
+        l[u][p] = on ? lses[p * lse_pstride + r] : -INFINITY;
+        if (on) xv[u][p] = outs[p * out_pstride + src[u]];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRows; ++u) {
+      const long long r = r0 + u * step;
+      if (r >= nrows) break;
+      float m = -INFINITY, w = 0.f;
+#pragma unroll
+      for (int p = 0; p < kMaxP; ++p) m = fmaxf(m, l[u][p]);
+      if (m == -INFINITY) {  // every partial empty
+        out[src[u]] = make_uint4(0u, 0u, 0u, 0u);
+        if (lse && piece == 0) lse[r] = -INFINITY;
+        continue;
+      }
+#pragma unroll
+      for (int p = 0; p < kMaxP; ++p)
+        if (p < P) w += expf(l[u][p] - m);
+      const float inv_w = 1.f / w;
+      float acc[kN];
+#pragma unroll
+      for (int e = 0; e < kN; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int p = 0; p < kMaxP; ++p) {
+        if (p >= P) break;
+        const float coef = (l[u][p] == -INFINITY) ? 0.f : expf(l[u][p] - m) * inv_w;
+        float x[kN];
+        Vec<T>::load(xv[u][p], x);
+#pragma unroll
+        for (int e = 0; e < kN; ++e) acc[e] = fmaf(coef, x[e], acc[e]);
+      }
+      out[src[u]] = Vec<T>::store(acc);
+      if (lse && piece == 0) lse[r] = m + logf(w);
+    }
+  }
+}
+
 }  // namespace
 }  // namespace sp
 
@@ -100,6 +219,39 @@ extern "C" sp_status sp_attn_merge_partials(const void* outs, const float* lses,
   if (dtype != SP_BF16 && dtype != SP_F32) return SP_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const long long nrows = static_cast<long long>(B) * S * H;
+  {
+    const int vec = dtype == SP_BF16 ? 8 : 4;
+    const int lanes = d / vec;
+    if (P <= 8 && d % vec == 0 && lanes <= 32 && 32 % lanes == 0 && sp::aligned(outs, 16) &&
+        sp::aligned(out, 16)) {
+      // enough warps to keep every SM's loads in flight
+      const long long warps = (nrows * lanes + 31) / 32;
+      long long blocks = (warps + 7) / 8;
+      const long long cap = static_cast<long long>(sp::device_sm_count()) * 32;
+      if (blocks > cap) blocks = cap;
+      const uint4* in = static_cast<const uint4*>(outs);
+      uint4* o = static_cast<uint4*>(out);
+      const unsigned g = static_cast<unsigned>(blocks);
+      if (dtype == SP_BF16) {
+        if (P <= 2)
+          sp::merge_vec_kernel<__nv_bfloat16, 2, 2><<<g, 256, 0, st>>>(in, lses, P, B, S, H,
+                                                                      lanes, o, lse);
+        else
+          sp::merge_vec_kernel<__nv_bfloat16, 8, 1><<<g, 256, 0, st>>>(in, lses, P, B, S, H,
+                                                                      lanes, o, lse);
+      } else {
+        if (P <= 2)
+          sp::merge_vec_kernel<float, 2, 2><<<g, 256, 0, st>>>(in, lses, P, B, S, H, lanes, o,
+                                                              lse);
+        else
+          sp::merge_vec_kernel<float, 8, 1><<<g, 256, 0, st>>>(in, lses, P, B, S, H, lanes, o,
+                                                              lse);
+      }
+      if (cudaGetLastError() != cudaSuccess) return SP_ERR_CUDA;
+      sp::g_last_launches = 1;
+      return SP_OK;
+    }
+  }
   long long blocks = (nrows + 7) / 8;
   const long long cap = static_cast<long long>(sp::device_sm_count()) * 8;
   if (blocks > cap) blocks = cap;
