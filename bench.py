@@ -28,7 +28,8 @@ llama8b_32k backward in both dQ forms, the packed_128k and halfmil_512k
 striped backwards,
 the forward and backward of an 8-device ring simulated through the per-device
 calls, the
-fused Ulysses path, the Ulysses + Ring hybrid and two large permutations.
+fused Ulysses path, the Ulysses + Ring hybrid, two merges of partials and two
+large permutations.
 
 Multi-GPU: every rank runs its own independent replica of the step (the
 head groups / batches of the path are independent; no collective on the data
@@ -607,6 +608,7 @@ def extra_measurements(args, peaks, peak_kind, flush):
     res["llama8b_32k_ring_forward_per_device"] = ring_forward_measurement(peaks, flush, stream)
     res["llama8b_32k_ring_backward_per_device"] = ring_backward_measurement(peaks, flush, stream)
     res.update(next_row_measurements(peaks, flush, stream))
+    res["merge_partials"] = merge_measurement(peaks, flush, stream)
     # the q shapes of llama8b_32k (256 MiB) and packed_128k (1 GiB)
     for S_, label in ((32768, "permute_256MiB"), (131072, "permute_1GiB")):
         x = torch.randn((1, S_, 32, 128), device="cuda").to(torch.bfloat16)
@@ -620,6 +622,41 @@ def extra_measurements(args, peaks, peak_kind, flush):
                       "frac_of_hbm": round(min(g1, g2) / peaks["hbm_gbs"], 4),
                       "shape": f"[1][{S_}][32][128] bf16, P=8"}
         del x, y
+    return res
+
+
+def merge_measurement(peaks, flush, stream, reps=20):
+    """sp_attn_merge_partials against measured HBM bandwidth on inputs larger
+    than L2: a 2-way merge of full llama8b_32k-shaped partials and an 8-way
+    merge of 8192-token partials.  Bytes per row: P partial rows of 2d bytes
+    and P log-sum-exps read, one row and one log-sum-exp written."""
+    import torch
+
+    from sequence_parallelism_gb300 import _lib
+
+    res = {"kernel": "merge_vec_kernel", "bound": "hbm", "peak": peaks["hbm_gbs"],
+           "unit": "GB/s"}
+    fr = []
+    for P_, S_ in ((2, 32768), (8, 8192)):
+        H, d = 32, 128
+        g = torch.Generator(device="cuda").manual_seed(11 + P_)
+        outs = torch.randn((P_, 1, S_, H, d), device="cuda", generator=g).to(torch.bfloat16)
+        lses = torch.randn((P_, 1, H, S_), device="cuda", generator=g)
+        out = torch.empty((1, S_, H, d), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((1, H, S_), dtype=torch.float32, device="cuda")
+        t, _, clocks = _timed(lambda: _lib.sp_attn_merge_partials(outs, lses, out, lse), flush,
+                              stream, reps)
+        rows = S_ * H
+        nbytes = rows * ((P_ + 1) * (2 * d + 4))
+        gbs = nbytes / (t * 1e-3) / 1e9
+        f = gbs / peaks["hbm_gbs"]
+        fr.append(f)
+        res[f"P{P_}"] = {"shape": f"{P_} x [1][{S_}][{H}][{d}] bf16", "us": round(t * 1e3, 1),
+                         "bytes": nbytes, "achieved": round(gbs, 1), "frac": round(f, 4),
+                         "clocks": clocks}
+        del outs, lses, out, lse
+    res["frac"] = round(min(fr), 4)
+    res["note"] = "L2 flushed before each rep; median of reps; frac is the lower of the two"
     return res
 
 

@@ -133,10 +133,11 @@ struct Vec<float> {
 // lanes_per_row = d / Vec<T>::kN divides 32; the output and every partial
 // row are 16-byte aligned; P <= kMaxP.  Rows are visited token-fastest
 // within a (batch, head), so that neighbouring rows' log-sum-exps are
-// neighbours in memory, and every lane issues all loads of kRows rows (its
-// log-sum-exps and 16-byte pieces of every partial) before any arithmetic:
-// a merge moves little data per row, so loads in flight set its speed.
-template <typename T, int kMaxP, int kRows>
+// neighbours in memory, and every lane issues all loads of its row (the P
+// log-sum-exps and the 16-byte pieces of every partial) before any
+// arithmetic.  (Two rows per lane in flight were slower at every size
+// measured, L2-resident or not.)
+template <typename T, int kMaxP>
 __global__ void __launch_bounds__(256) merge_vec_kernel(const uint4* __restrict__ outs,
                                                         const float* __restrict__ lses, int P,
                                                         int B, int S, int H, int lanes_per_row,
@@ -152,57 +153,46 @@ __global__ void __launch_bounds__(256) merge_vec_kernel(const uint4* __restrict_
   const long long lse_pstride = static_cast<long long>(B) * H * S;
   const long long out_pstride = nrows * lanes_per_row;  // in 16-byte pieces
   const long long step = nwarps * rows_per_warp;        // rows per sweep of all warps
-  for (long long r0 = warp * rows_per_warp + sub; r0 < nrows; r0 += step * kRows) {
-    float l[kRows][kMaxP];
-    uint4 xv[kRows][kMaxP];
-    long long src[kRows];
+  for (long long r = warp * rows_per_warp + sub; r < nrows; r += step) {
+    // r = (b, h, t), t fastest: the lse index
+    const int t = static_cast<int>(r % S);
+    const long long bh = r / S;
+    const int h = static_cast<int>(bh % H);
+    const long long b = bh / H;
+    const long long src = ((b * S + t) * H + h) * lanes_per_row + piece;  // (b, t, h)
+    float l[kMaxP];
+    uint4 xv[kMaxP];
 #pragma unroll
-    for (int u = 0; u < kRows; ++u) {
-      const long long r = r0 + u * step;  // (b, h, t), t fastest: the lse index
-      const bool live = r < nrows;
-      const int t = static_cast<int>(r % S);
-      const long long bh = r / S;
-      const int h = static_cast<int>(bh % H);
-      const long long b = bh / H;
-      src[u] = ((b * S + t) * H + h) * lanes_per_row + piece;  // (b, t, h): the out index
+    for (int p = 0; p < kMaxP; ++p) {
+      l[p] = p < P ? lses[p * lse_pstride + r] : -INFINITY;
+      if (p < P) xv[p] = outs[p * out_pstride + src];
+    }
+    float m = -INFINITY, w = 0.f;
 #pragma unroll
-      for (int p = 0; p < kMaxP; ++p) {
-        const bool on = live && p < P;
-        l[u][p] = on ? lses[p * lse_pstride + r] : -INFINITY;
-        if (on) xv[u][p] = outs[p * out_pstride + src[u]];
-      }
+    for (int p = 0; p < kMaxP; ++p) m = fmaxf(m, l[p]);
+    if (m == -INFINITY) {  // every partial empty
+      out[src] = make_uint4(0u, 0u, 0u, 0u);
+      if (lse && piece == 0) lse[r] = -INFINITY;
+      continue;
     }
 #pragma unroll
-    for (int u = 0; u < kRows; ++u) {
-      const long long r = r0 + u * step;
-      if (r >= nrows) break;
-      float m = -INFINITY, w = 0.f;
+    for (int p = 0; p < kMaxP; ++p)
+      if (p < P) w += expf(l[p] - m);
+    const float inv_w = 1.f / w;
+    float acc[kN];
 #pragma unroll
-      for (int p = 0; p < kMaxP; ++p) m = fmaxf(m, l[u][p]);
-      if (m == -INFINITY) {  // every partial empty
-        out[src[u]] = make_uint4(0u, 0u, 0u, 0u);
-        if (lse && piece == 0) lse[r] = -INFINITY;
-        continue;
-      }
+    for (int e = 0; e < kN; ++e) acc[e] = 0.f;
 #pragma unroll
-      for (int p = 0; p < kMaxP; ++p)
-        if (p < P) w += expf(l[u][p] - m);
-      const float inv_w = 1.f / w;
-      float acc[kN];
+    for (int p = 0; p < kMaxP; ++p) {
+      if (p >= P) break;
+      const float coef = (l[p] == -INFINITY) ? 0.f : expf(l[p] - m) * inv_w;
+      float x[kN];
+      Vec<T>::load(xv[p], x);
 #pragma unroll
-      for (int e = 0; e < kN; ++e) acc[e] = 0.f;
-#pragma unroll
-      for (int p = 0; p < kMaxP; ++p) {
-        if (p >= P) break;
-        const float coef = (l[u][p] == -INFINITY) ? 0.f : expf(l[u][p] - m) * inv_w;
-        float x[kN];
-        Vec<T>::load(xv[u][p], x);
-#pragma unroll
-        for (int e = 0; e < kN; ++e) acc[e] = fmaf(coef, x[e], acc[e]);
-      }
-      out[src[u]] = Vec<T>::store(acc);
-      if (lse && piece == 0) lse[r] = m + logf(w);
+      for (int e = 0; e < kN; ++e) acc[e] = fmaf(coef, x[e], acc[e]);
     }
+    out[src] = Vec<T>::store(acc);
+    if (lse && piece == 0) lse[r] = m + logf(w);
   }
 }
 
@@ -232,20 +222,24 @@ extern "C" sp_status sp_attn_merge_partials(const void* outs, const float* lses,
       const uint4* in = static_cast<const uint4*>(outs);
       uint4* o = static_cast<uint4*>(out);
       const unsigned g = static_cast<unsigned>(blocks);
+      // the partial count fixes how many loads a lane keeps in flight
       if (dtype == SP_BF16) {
         if (P <= 2)
-          sp::merge_vec_kernel<__nv_bfloat16, 2, 2><<<g, 256, 0, st>>>(in, lses, P, B, S, H,
-                                                                      lanes, o, lse);
+          sp::merge_vec_kernel<__nv_bfloat16, 2><<<g, 256, 0, st>>>(in, lses, P, B, S, H, lanes,
+                                                                   o, lse);
+        else if (P <= 4)
+          sp::merge_vec_kernel<__nv_bfloat16, 4><<<g, 256, 0, st>>>(in, lses, P, B, S, H, lanes,
+                                                                   o, lse);
         else
-          sp::merge_vec_kernel<__nv_bfloat16, 8, 1><<<g, 256, 0, st>>>(in, lses, P, B, S, H,
-                                                                      lanes, o, lse);
+          sp::merge_vec_kernel<__nv_bfloat16, 8><<<g, 256, 0, st>>>(in, lses, P, B, S, H, lanes,
+                                                                   o, lse);
       } else {
         if (P <= 2)
-          sp::merge_vec_kernel<float, 2, 2><<<g, 256, 0, st>>>(in, lses, P, B, S, H, lanes, o,
-                                                              lse);
+          sp::merge_vec_kernel<float, 2><<<g, 256, 0, st>>>(in, lses, P, B, S, H, lanes, o, lse);
+        else if (P <= 4)
+          sp::merge_vec_kernel<float, 4><<<g, 256, 0, st>>>(in, lses, P, B, S, H, lanes, o, lse);
         else
-          sp::merge_vec_kernel<float, 8, 1><<<g, 256, 0, st>>>(in, lses, P, B, S, H, lanes, o,
-                                                              lse);
+          sp::merge_vec_kernel<float, 8><<<g, 256, 0, st>>>(in, lses, P, B, S, H, lanes, o, lse);
       }
       if (cudaGetLastError() != cudaSuccess) return SP_ERR_CUDA;
       sp::g_last_launches = 1;

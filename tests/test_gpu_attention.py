@@ -181,6 +181,38 @@ def test_merge_partials_parity(sp, dtype):
     assert (np32(out)[1, 7, 2] == 0).all()
 
 
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 8, 9])
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("bf16", 256), ("bf16", 48),
+                                     ("f32", 128), ("f32", 32)])
+def test_merge_partials_every_form(sp, P, dtype, d):
+    """Every kernel form of the merge (16-byte pieces with room for 2, 4 or 8
+    partials; one warp per row for head sizes that do not split into pieces
+    dividing a warp, or more than 8 partials) against the oracle's merge.
+    The oracle gets the same rounded inputs, so the result differs from it
+    only by float32 arithmetic and one rounding of the output: at most half
+    an output ulp (at most 2^-8 of |x| for bf16's 8 significant bits, 2^-24
+    for float32's 24) plus float32 noise."""
+    B, S, H = 2, 97, 3   # 582 rows: several warps' worth of rows and a ragged tail
+    g = torch.Generator(device="cuda")
+    g.manual_seed(900 + 10 * P + d)
+    outs = torch.randn((P, B, S, H, d), generator=g, device="cuda").to(torch_dtype(dtype))
+    lses = torch.randn((P, B, H, S), generator=g, device="cuda") * 3
+    lses[0, :, :, :6] = float("-inf")      # an empty partial gets weight 0
+    lses[:, 1, 2, 50] = float("-inf")      # a row with nothing at all
+    out, lse = sp.merge_partials(outs, lses)
+    torch.cuda.synchronize()
+    ro, rl = oracle.merge_partials(np32(outs).astype(np.float64), lses.cpu().numpy())
+    got = np32(out).astype(np.float64)
+    half_ulp = 2.0 ** -8 if dtype == "bf16" else 2.0 ** -24
+    err = np.abs(got - ro) - (half_ulp * np.abs(ro) + 4e-6 * np.abs(ro).max())
+    assert err.max() <= 0, f"P={P} {dtype} d={d}: excess {err.max():.3g}"
+    fin = np.isfinite(rl)
+    lg = lse.cpu().numpy()
+    assert np.array_equal(np.isfinite(lg), fin)
+    assert np.abs(lg[fin] - rl[fin]).max() <= 1e-5
+    assert (np32(out)[1, 50, 2] == 0).all()
+
+
 def test_constant_values_give_ones(sp):
     """v = 1: every softmax row sums to one (bf16 P rounding is the only
     error)."""
