@@ -770,10 +770,12 @@ def backward_measurement(peaks, flush, stream, name="llama8b_32k", order="contig
 
 def ring_forward_measurement(peaks, flush, stream, reps=10):
     """The forward of an 8-device ring simulated on one GPU (llama8b_32k,
-    contiguous blocks), as dist.ring_attention runs it on each device: P
-    sp_ring_block_step calls per device, each partial folded into the
-    running result by sp_attn_merge_partials (P^2 = 64 steps, 56 merges per
-    rep).  FLOPs: the attention's algorithmic count."""
+    contiguous blocks), as dist.ring_attention runs it on each device: step 0
+    by sp_ring_block_step, steps 1..P-1 folded into the running result by
+    sp_ring_block_step_accumulate (P^2 = 64 calls per rep).  Also timed: the
+    same ring with every step written by sp_ring_block_step and folded by
+    sp_attn_merge_partials (56 merges).  FLOPs: the attention's algorithmic
+    count."""
     import torch
 
     import sequence_parallelism_gb300 as sp
@@ -795,7 +797,19 @@ def ring_forward_measurement(peaks, flush, stream, reps=10):
     lses = [torch.empty((2, B, Hq, Lb), dtype=torch.float32, device="cuda") for _ in range(2)]
     ws = sp.attention_workspace(B, S, True)
 
-    def ring():
+    def ring_accumulate():
+        for i in range(P):
+            for s_ in range(P):
+                j = (i - s_) % P
+                if s_ == 0:
+                    _lib.sp_ring_block_step(qb[i], kb[j], vb[j], pos, S, P, "contiguous", i, j,
+                                            0.0, outs[0][0], lses[0][0], ws)
+                else:
+                    _lib.sp_ring_block_step_accumulate(qb[i], kb[j], vb[j], pos, S, P,
+                                                       "contiguous", i, j, 0.0, outs[0][0],
+                                                       lses[0][0], ws)
+
+    def ring_merge():
         for i in range(P):
             cur = 0
             for s_ in range(P):
@@ -808,18 +822,21 @@ def ring_forward_measurement(peaks, flush, stream, reps=10):
                                                 lses[1 - cur][0])
                     cur = 1 - cur
 
-    t, _, clocks = _timed(ring, flush, stream, reps)
+    t, _, clocks = _timed(ring_accumulate, flush, stream, reps)
+    t2, _, clocks2 = _timed(ring_merge, flush, stream, reps)
     st_, code = _lib.sp_get_device_error(ws)
     if st_ != 0:
         raise RuntimeError(f"device error word {code:#x} in the ring forward")
     fl = attention_flops(cfg, pos_np)
-    tf = fl / (t * 1e-3) / 1e12
+    tf, tf2 = fl / (t * 1e-3) / 1e12, fl / (t2 * 1e-3) / 1e12
     return {"ms": round(t, 4), "TFLOP/s": round(tf, 1),
             "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
-            "calls_per_rep": P * P, "merges_per_rep": P * (P - 1), "reps": reps,
-            "clocks": clocks,
-            "note": "64 sp_ring_block_step calls and 56 two-way merges (8 simulated devices x "
-                    "8 ring steps; causal pairs with j > i find no allowed tile), median of reps"}
+            "calls_per_rep": P * P, "reps": reps, "clocks": clocks,
+            "step_and_merge": {"ms": round(t2, 4), "TFLOP/s": round(tf2, 1),
+                               "frac_of_bf16_peak": round(tf2 / peaks["bf16_tflops"], 4),
+                               "merges_per_rep": P * (P - 1), "clocks": clocks2},
+            "note": "8 simulated devices x 8 ring steps; causal contiguous pairs with j > i add "
+                    "nothing (the accumulating call returns without a launch); median of reps"}
 
 
 def ring_backward_measurement(peaks, flush, stream, reps=5):

@@ -241,6 +241,30 @@ sp_status sp_ring_block_step(const void* q_blk, const void* k_blk, const void* v
                              sp_dtype dtype, void* out_blk, float* lse_blk, void* workspace,
                              size_t workspace_bytes, sp_stream_t stream);
 
+/* sp_ring_block_step_accumulate: sp_ring_block_step folded into a running
+ * result, the step a device of the ring repeats ("Ring Attention", "Cómo
+ * funciona la atención en anillo": each arriving block's partial is combined
+ * with what the device has so far by the cumulative softmax).  On entry
+ * out_blk / lse_blk (lse_blk required) hold the running result of the steps
+ * so far; on return they hold it merged with pair (i, j)'s partial:
+ *   lse' = log(exp(lse) + exp(lse_ij)),
+ *   out' = exp(lse - lse') * out + exp(lse_ij - lse') * out_ij
+ * where out_ij is the partial before rounding to bf16.  A row whose running
+ * lse is -inf takes the partial alone and its running out is not read (it
+ * may hold anything); rows with no allowed key in block j keep their values
+ * bit for bit.  Running lse values must be finite or -inf.  Contiguous blocks
+ * under the causal mask with j > i add nothing, and the call returns SP_OK
+ * without a launch.  The result equals sp_ring_block_step into a temporary
+ * followed by sp_attn_merge_partials of the two, up to one bf16 rounding of
+ * the partial.  SP_ERR_UNSUPPORTED unless dtype is SP_BF16 (d = 128); other
+ * arguments and errors as for sp_ring_block_step. */
+sp_status sp_ring_block_step_accumulate(const void* q_blk, const void* k_blk, const void* v_blk,
+                                        const int32_t* position_ids, int B, int S, int Hq,
+                                        int Hkv, int d, int P, sp_block_order order, int i, int j,
+                                        float scale, sp_dtype dtype, void* out_blk,
+                                        float* lse_blk, void* workspace, size_t workspace_bytes,
+                                        sp_stream_t stream);
+
 /* Query block i against the whole sequence, visited in ring order: what a
  * device computes once K and V have been all-gathered instead of passed
  * around the ring ("Ulysses序列并行技术详解：ms-swift如何降低长序列显存占用":

@@ -15,6 +15,7 @@ without the built library raises ImportError -- there is no CPU path.
     blockwise_attention_backward(...)          dq, dk, dv from out, dout and lse
     doc_starts(position_ids)                   O(n) causal-mask carrier
     ring_block_step(q_blk, k_blk, v_blk, ...)  one device's ring step on block tensors
+    ring_block_step_accumulate(...)            the same step folded into a running result
     ring_block_step_backward(...)              its gradient parts, into float32 accumulators
     query_block_attention(q_blk, k, v, ...)    one device's query block against all K/V
 
@@ -30,7 +31,8 @@ from ._lib import SPError  # noqa: F401
 __all__ = ["seq_to_head", "head_to_seq", "blockwise_attention", "ring_step", "merge_partials",
            "ulysses_attention", "ulysses_attention_backward", "ulysses_ring_attention",
            "blockwise_attention_backward",
-           "doc_starts", "attention_workspace", "ring_block_step", "ring_block_step_backward",
+           "doc_starts", "attention_workspace", "ring_block_step", "ring_block_step_accumulate",
+           "ring_block_step_backward",
            "query_block_attention",
            "SPError"]
 
@@ -109,6 +111,20 @@ def ring_block_step(q_blk, k_blk, v_blk, P, i, j, order="contiguous", position_i
         workspace = attention_workspace(B, S, position_ids is not None, q_blk.device)
     return _lib.sp_ring_block_step(q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, scale,
                                    out, lse, workspace)
+
+
+def ring_block_step_accumulate(q_blk, k_blk, v_blk, P, i, j, out, lse, order="contiguous",
+                               position_ids=None, scale=0.0, workspace=None):
+    """ring_block_step folded into a running result: (out [B][S/P][Hq][d],
+    lse [B][Hq][S/P] float32) hold the merge of the steps so far (rows with
+    lse = -inf: none yet) and are updated in place by the log-sum-exp merge
+    with pair (i, j)'s partial.  bf16, d = 128."""
+    B, Lb = q_blk.shape[:2]
+    S = Lb * P
+    if workspace is None:
+        workspace = attention_workspace(B, S, position_ids is not None, q_blk.device)
+    return _lib.sp_ring_block_step_accumulate(q_blk, k_blk, v_blk, position_ids, S, P, order, i,
+                                              j, scale, out, lse, workspace)
 
 
 def ring_block_step_backward(q_blk, k_blk, v_blk, out_blk, dout_blk, lse_blk, P, i, j,

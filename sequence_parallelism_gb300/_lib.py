@@ -28,7 +28,7 @@ EXPORTS = (
     "sp_segment_starts_workspace_bytes", "sp_segment_starts", "sp_blockwise_attn_workspace_bytes",
     "sp_blockwise_attn_split_workspace_bytes",
     "sp_blockwise_attn_fwd", "sp_blockwise_attn_step", "sp_blockwise_attn_fwd_noalloc",
-    "sp_ring_block_step", "sp_query_block_attn_fwd",
+    "sp_ring_block_step", "sp_ring_block_step_accumulate", "sp_query_block_attn_fwd",
     "sp_ring_block_step_bwd_workspace_bytes", "sp_ring_block_step_bwd",
     "sp_ulysses_ring_attn_workspace_bytes", "sp_ulysses_ring_attn_fwd",
     "sp_blockwise_attn_bwd_workspace_bytes", "sp_blockwise_attn_bwd", "sp_set_bwd_dq_reduction",
@@ -70,6 +70,8 @@ def _load():
                                        i, vp, vp, vp, vp, sz, vp]),
         "sp_ring_block_step": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i, vp, vp, vp,
                                    sz, vp]),
+        "sp_ring_block_step_accumulate": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, i, i, f, i,
+                                              vp, vp, vp, sz, vp]),
         "sp_query_block_attn_fwd": (i, [vp, vp, vp, vp, i, i, i, i, i, i, i, i, f, i, vp, vp, vp,
                                         sz, vp]),
         "sp_ulysses_ring_attn_workspace_bytes": (sz, [i, i, i, i, i, i, i]),
@@ -228,6 +230,24 @@ def sp_ring_block_step(q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, sca
     if Lb * P != S or k_blk.shape[1] != Lb:
         raise ValueError("block tensors must hold S/P rows")
     _check("sp_ring_block_step", _lib.sp_ring_block_step(
+        _ptr(q_blk), _ptr(k_blk), _ptr(v_blk), _ptr(position_ids), B, S, Hq, Hkv, d, P,
+        _ORDERS[order], i, j, float(scale), _dtype(q_blk), _ptr(out_blk), _ptr(lse_blk),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out_blk, lse_blk
+
+
+def sp_ring_block_step_accumulate(q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, scale,
+                                  out_blk, lse_blk, workspace, stream=None):
+    """sp_ring_block_step folded into the running result (out_blk, lse_blk),
+    which it updates in place."""
+    _dense(q_blk, k_blk, v_blk, position_ids, out_blk, lse_blk, workspace)
+    if lse_blk is None:
+        raise ValueError("the running lse is required")
+    B, Lb, Hq, d = q_blk.shape
+    Hkv = k_blk.shape[2]
+    if Lb * P != S or k_blk.shape[1] != Lb:
+        raise ValueError("block tensors must hold S/P rows")
+    _check("sp_ring_block_step_accumulate", _lib.sp_ring_block_step_accumulate(
         _ptr(q_blk), _ptr(k_blk), _ptr(v_blk), _ptr(position_ids), B, S, Hq, Hkv, d, P,
         _ORDERS[order], i, j, float(scale), _dtype(q_blk), _ptr(out_blk), _ptr(lse_blk),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))

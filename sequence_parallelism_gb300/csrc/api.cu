@@ -40,7 +40,7 @@ sp_status attn(const void* q, const void* k, const void* v, const int32_t* posit
                int pos_rows, int B, int S, int Hq, int Hkv, int d, int P, sp_block_order order,
                int step_begin, int step_end, float scale, sp_dtype dtype, void* out, float* lse,
                void* workspace, size_t workspace_bytes, sp_stream_t stream, int q_block,
-               int kv_block) {
+               int kv_block, bool accumulate) {
   g_last_launches = 0;
   if (!q || !k || !v || !out) return SP_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || d < 1 || P < 1) return SP_ERR_INVALID_ARG;
@@ -65,10 +65,15 @@ sp_status attn(const void* q, const void* k, const void* v, const int32_t* posit
     if (static_cast<long long>(B) * Hq * P * pairs > 0x7fffffffLL) return SP_ERR_UNSUPPORTED;
   }
   if (pos_rows < 1 || B % pos_rows != 0) return SP_ERR_INVALID_ARG;
+  if (accumulate && (q_block < 0 || kv_block < 0 || !lse)) return SP_ERR_INVALID_ARG;
+  if (accumulate && dtype != SP_BF16) return SP_ERR_UNSUPPORTED;
   const int causal = position_ids != nullptr;
   if (!workspace || !aligned(workspace, 256) ||
       workspace_bytes < sp_blockwise_attn_workspace_bytes(pos_rows, S, causal))
     return SP_ERR_WORKSPACE;
+  // contiguous blocks under the causal mask: every key of block j > i comes
+  // after every query of block i, so the pair adds nothing to a running result
+  if (accumulate && causal && order == SP_ORDER_CONTIGUOUS && kv_block > q_block) return SP_OK;
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -108,6 +113,7 @@ sp_status attn(const void* q, const void* k, const void* v, const int32_t* posit
   a.scale = scale > 0.f ? scale : static_cast<float>(1.0 / sqrt(static_cast<double>(d)));
   a.scratch = nullptr;
   a.scratch_bytes = 0;
+  a.accumulate = accumulate ? 1 : 0;
   if (!causal && workspace_bytes > kWsHeaderBytes) {
     a.scratch = ws + kWsHeaderBytes;
     a.scratch_bytes = workspace_bytes - kWsHeaderBytes;
@@ -182,6 +188,20 @@ extern "C" sp_status sp_ring_block_step(const void* q_blk, const void* k_blk, co
   return sp::attn(q_blk, k_blk, v_blk, position_ids, B, B, S, Hq, Hkv, d, P, order, step,
                   step + 1, scale, dtype, out_blk, lse_blk, workspace, workspace_bytes, stream, i,
                   j);
+}
+
+extern "C" sp_status sp_ring_block_step_accumulate(
+    const void* q_blk, const void* k_blk, const void* v_blk, const int32_t* position_ids, int B,
+    int S, int Hq, int Hkv, int d, int P, sp_block_order order, int i, int j, float scale,
+    sp_dtype dtype, void* out_blk, float* lse_blk, void* workspace, size_t workspace_bytes,
+    sp_stream_t stream) {
+  sp::NvtxRange nvtx_range("sp_ring_block_step_accumulate");
+  sp::g_last_launches = 0;
+  if (P < 1 || i < 0 || i >= P || j < 0 || j >= P) return SP_ERR_INVALID_ARG;
+  const int step = ((i - j) % P + P) % P;
+  return sp::attn(q_blk, k_blk, v_blk, position_ids, B, B, S, Hq, Hkv, d, P, order, step,
+                  step + 1, scale, dtype, out_blk, lse_blk, workspace, workspace_bytes, stream, i,
+                  j, true);
 }
 
 extern "C" sp_status sp_query_block_attn_fwd(const void* q_blk, const void* k, const void* v,

@@ -71,7 +71,7 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, true);
 enum : int {
   kErrQFull = 0x101, kErrKvEmpty = 0x102, kErrKvFull = 0x103, kErrSFull = 0x104,
   kErrPFull = 0x105, kErrOFull = 0x106, kErrDrain = 0x107, kErrUnit = 0x108,
-  kErrQEmpty = 0x109, kErrOFree = 0x10a
+  kErrQEmpty = 0x109, kErrOFree = 0x10a, kErrAccFull = 0x10b
 };
 
 struct Tmaps {
@@ -155,6 +155,7 @@ struct __align__(8) Barriers {
   uint64_t p_full[kQTiles];
   uint64_t o_full[kQTiles];
   uint64_t o_free[kQTiles];  // epilogue read O: the next unit may overwrite it
+  uint64_t acc_full[kQTiles];  // accumulate form: a half of the running output landed
   uint64_t done;
 };
 
@@ -211,6 +212,13 @@ __device__ __forceinline__ void make_unit(int w, const AttnArgs& a, int n_pairs,
 // the other roles read in place (a slot is released at the end of the unit).  The next unit's Q is loaded as
 // soon as the current unit's last S MMAs are done, and its first S MMAs run
 // while the softmax warps are still in the current unit's epilogue.
+//
+// kAcc (per-device form, one ring step): out / lse hold a running result on
+// entry, and the epilogue folds this step's partial into it by the
+// log-sum-exp merge instead of writing the partial.  The running output
+// tile comes in through the same swizzled stage the stores use (one TMA load
+// per 64-column half); a unit without tiles leaves its rows untouched.
+template <bool kAcc>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bf16_kernel(const __grid_constant__ Tmaps tm, AttnArgs a, float scale_log2, int n_pairs,
                      int n_whole, int split_k, int n_work, float* __restrict__ part_o,
@@ -248,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars.p_full[t]), kBM);
       mbar_init(smem_u32(&bars.o_full[t]), 1);
       mbar_init(smem_u32(&bars.o_free[t]), kBM);
+      mbar_init(smem_u32(&bars.acc_full[t]), 1);
     }
     mbar_init(smem_u32(&bars.done), 1);
     abort_s = 0;
@@ -481,6 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_base + 256 + t * 128;
     int it = 0;  // tiles over the CTA's life
     int qn = 0;  // units with tiles so far
+    int qa = 0;  // running-output loads so far (accumulate form)
     bool ok = true;
     for (int seq = 0; ok; ++seq) {
       const int xs = seq & 1;
@@ -613,6 +623,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // ---------------------------------------------------------- epilogue
+      if (kAcc && U.n_tiles == 0) {  // nothing to fold in: the running rows stay
+        mbar_arrive(smem_u32(&bars.unit_empty[xs]));
+        continue;
+      }
+      const uint32_t stage = smem_stage + t * kStageBytes;
+      const bool leader = row == 0;
+      int c2, c3;
+      coord_q(U.i, U.u0 + t * kBM, c2, c3);
+      float lse_run = -INFINITY;
+      if (kAcc) {
+        // the running output's first half and the running lse, in flight
+        // while the last PV completes
+        if (row_live) lse_run = a.lse[(static_cast<long long>(U.b) * a.Hq + U.hq) * Lb + u];
+        if (leader) {
+          bulk_wait_group_read0();  // the stage's previous store has read it
+          mbar_arrive_expect_tx(smem_u32(&bars.acc_full[t]), kStageBytes);
+          tma_load_5d(stage, &tm.o, smem_u32(&bars.acc_full[t]), 0, U.hq, c2, c3, U.b);
+        }
+      }
       const bool have = U.n_tiles > 0 && ok;
       if (have) {
         const bool got = mbar_wait(smem_u32(&bars.o_full[t]), qn & 1, abort_flag, a.err, kErrOFull);
@@ -622,6 +651,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool any = have && ok && l > 0.f;
       const float inv = any ? 1.f / l : 0.f;
       const float row_lse = any ? (m_use + lg2(l)) * 0.69314718055994530942f : -INFINITY;
+      // out = c_new * O + c_run * out_run, lse = lse_out (without kAcc: the
+      // partial itself)
+      float c_new = inv, c_run = 0.f, lse_out = row_lse;
+      if (kAcc) {
+        const float mx = fmaxf(row_lse, lse_run);
+        if (mx == -INFINITY) {  // neither has a key: the row stays as it is
+          c_new = 0.f;
+          c_run = 1.f;
+        } else {
+          const float wn = expf(row_lse - mx), wr = expf(lse_run - mx);
+          const float wsum = wn + wr;
+          c_new = inv * (wn / wsum);
+          c_run = wr / wsum;
+          lse_out = mx + logf(wsum);
+        }
+        if (c_new == 0.f) lse_out = lse_run;  // nothing added: the row keeps its bits
+      }
       // the whole O row in one round trip, then O goes back to the MMA warp
       // (the next unit's first PV overwrites it) before the stores
       uint32_t r[kD];
@@ -638,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(smem_u32(&bars.o_free[t]));
         ++qn;
       }
-      if (U.split > 1) {
+      if (!kAcc && U.split > 1) {
         // one piece of a split item: normalized partial O and its lse (fp32),
         // combined afterwards by merge_split_kernel
         const long long prow = static_cast<long long>(U.sidx) * kRowsPerCta + t * kBM + row;
@@ -654,23 +700,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         // time, the layout a 64 x 128-row TMA box with 128-byte swizzle has)
         // and one bulk tensor store per half: coalesced, and asynchronous
         // for the warpgroup
-        const uint32_t stage = smem_stage + t * kStageBytes;
-        const bool leader = row == 0;
-        int c2, c3;
-        coord_q(U.i, U.u0 + t * kBM, c2, c3);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          if (leader) bulk_wait_group_read0();  // the stage's previous store has read it
+          if (leader) {
+            bulk_wait_group_read0();  // the stage's previous store has read it
+            if (kAcc && h == 1) {
+              mbar_arrive_expect_tx(smem_u32(&bars.acc_full[t]), kStageBytes);
+              tma_load_5d(stage, &tm.o, smem_u32(&bars.acc_full[t]), 64, U.hq, c2, c3, U.b);
+            }
+          }
+          if (kAcc) {
+            // every thread passes both named barriers whatever the outcome
+            // (a timeout is recorded in the error word)
+            if (!mbar_wait(smem_u32(&bars.acc_full[t]), qa & 1, abort_flag, a.err, kErrAccFull))
+              ok = false;
+            ++qa;
+          }
           named_bar_sync(1 + t, kBM);
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const int e = h * 64 + c * 8;
-            const uint4 v = make_uint4(
-                pack_bf16(__uint_as_float(r[e]) * inv, __uint_as_float(r[e + 1]) * inv),
-                pack_bf16(__uint_as_float(r[e + 2]) * inv, __uint_as_float(r[e + 3]) * inv),
-                pack_bf16(__uint_as_float(r[e + 4]) * inv, __uint_as_float(r[e + 5]) * inv),
-                pack_bf16(__uint_as_float(r[e + 6]) * inv, __uint_as_float(r[e + 7]) * inv));
             const uint32_t addr = stage + row * 128 + ((c ^ (row & 7)) << 4);
+            float y[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) y[k] = __uint_as_float(r[e + k]) * c_new;
+            uint4 v = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
+                                 pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+            if (kAcc && c_run > 0.f) {  // c_run = 0: the running row is not read
+              uint32_t o[4];
+              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+                           : "r"(addr)
+                           : "memory");
+              if (c_new == 0.f) {  // nothing to add (then c_run = 1): the bits stay
+                v = make_uint4(o[0], o[1], o[2], o[3]);
+              } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  y[2 * k] = fmaf(c_run, __uint_as_float(o[k] << 16), y[2 * k]);
+                  y[2 * k + 1] = fmaf(c_run, __uint_as_float(o[k] & 0xffff0000u), y[2 * k + 1]);
+                }
+                v = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]),
+                               pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+              }
+            }
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
                          "r"(v.y), "r"(v.z), "r"(v.w)
                          : "memory");
@@ -685,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (row_live && a.lse) {
           const bool blk = a.q_block >= 0;  // per-device lse: [B][Hq][S/P]
           a.lse[(static_cast<long long>(U.b) * a.Hq + U.hq) * (blk ? Lb : a.S) + (blk ? u : tq)] =
-              row_lse;
+              lse_out;
         }
       }
       mbar_arrive(smem_u32(&bars.unit_empty[xs]));
@@ -769,7 +842,9 @@ int launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
   const int n_pairs = (Lb + kRowsPerCta - 1) / kRowsPerCta;
   const long long items = static_cast<long long>(a.B) * a.Hq * (qb ? 1 : a.P) * n_pairs;
   const size_t smem = kSmemBytes + 1024;
-  if (cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(attn_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return -1;
   const float scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
@@ -782,7 +857,7 @@ int launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
   const long long rem = items % G;
   const long long full = items - rem;
   int split = 1;
-  if (!a.doc_start && a.scratch && rem > 0) {
+  if (!a.doc_start && a.scratch && rem > 0 && !a.accumulate) {
     const long long tiles = static_cast<long long>(a.step_end - a.step_begin) *
                             ((Lb + kBN - 1) / kBN);
     long long k = G / rem;
@@ -796,16 +871,22 @@ int launch_attn_bf16(const AttnArgs& a, cudaStream_t stream) {
   const long long n_work = split == 1 ? items : full + rem * split;
   const unsigned grid = static_cast<unsigned>(n_work < G ? n_work : G);
   if (split == 1) {
-    attn_bf16_kernel<<<grid, kThreads, smem, stream>>>(tm, a, scale_log2, n_pairs,
-                                                       static_cast<int>(items), 1,
-                                                       static_cast<int>(n_work), nullptr, nullptr);
+    if (a.accumulate)
+      attn_bf16_kernel<true><<<grid, kThreads, smem, stream>>>(
+          tm, a, scale_log2, n_pairs, static_cast<int>(items), 1, static_cast<int>(n_work),
+          nullptr, nullptr);
+    else
+      attn_bf16_kernel<false><<<grid, kThreads, smem, stream>>>(
+          tm, a, scale_log2, n_pairs, static_cast<int>(items), 1, static_cast<int>(n_work),
+          nullptr, nullptr);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
   }
   float* part_o = static_cast<float*>(a.scratch);
   float* part_lse = part_o + static_cast<size_t>(rem * split) * kRowsPerCta * kD;
-  attn_bf16_kernel<<<grid, kThreads, smem, stream>>>(tm, a, scale_log2, n_pairs,
-                                                     static_cast<int>(full), split,
-                                                     static_cast<int>(n_work), part_o, part_lse);
+  attn_bf16_kernel<false><<<grid, kThreads, smem, stream>>>(tm, a, scale_log2, n_pairs,
+                                                            static_cast<int>(full), split,
+                                                            static_cast<int>(n_work), part_o,
+                                                            part_lse);
   merge_split_kernel<<<static_cast<unsigned>(rem * (kRowsPerCta / 8)), 256, 0, stream>>>(
       a, n_pairs, static_cast<int>(full), split, part_o, part_lse);
   return cudaGetLastError() == cudaSuccess ? 2 : -1;

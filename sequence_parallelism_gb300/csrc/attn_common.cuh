@@ -33,6 +33,8 @@ struct AttnArgs {
   float scale;                 // multiplies q.k (natural-log domain)
   void* scratch;               // optional workspace beyond the minimum (256-aligned)
   size_t scratch_bytes;
+  int accumulate;              // 1: out / lse hold a running result that this call's
+                               // partial is folded into (bf16 per-device form only)
 };
 
 // Scratch that lets a non-causal bf16 call split the items of its last,
@@ -73,12 +75,14 @@ constexpr int kBwdRowPad = 128;  // Lbp = S / P rounded up to a multiple of this
 // position_ids != NULL, then the f32 or bf16 kernel).  position_ids has
 // pos_rows rows; attention batch b reads row b % pos_rows (pos_rows divides B).
 // q_block / kv_block: the per-device form of AttnArgs (-1: whole sequence).
+// accumulate: fold the partial into the running (out, lse) instead of
+// writing it (a single ring step of the bf16 per-device form).
 // Sets g_last_launches.
 sp_status attn(const void* q, const void* k, const void* v, const int32_t* position_ids,
                int pos_rows, int B, int S, int Hq, int Hkv, int d, int P, sp_block_order order,
                int step_begin, int step_end, float scale, sp_dtype dtype, void* out, float* lse,
                void* workspace, size_t workspace_bytes, sp_stream_t stream, int q_block = -1,
-               int kv_block = -1);
+               int kv_block = -1, bool accumulate = false);
 
 // Both return the number of kernels launched, or -1 on a CUDA error.
 int launch_attn_f32(const AttnArgs& a, cudaStream_t stream);

@@ -58,6 +58,24 @@ class LibraryKernels:
         _lib.sp_ring_block_step(q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, 0.0, out,
                                 lse, ws)
 
+    def ring_step_accumulate(self, q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, out,
+                             lse):
+        """Folds pair (i, j)'s partial into the running (out, lse): one call
+        for bf16 with d = 128, else the step into a temporary and the merge
+        (both on the library's kernels)."""
+        ws = self.workspace(q_blk.shape[0], S, position_ids is not None, q_blk.device)
+        if q_blk.dtype == torch.bfloat16 and q_blk.shape[3] == 128:
+            _lib.sp_ring_block_step_accumulate(q_blk, k_blk, v_blk, position_ids, S, P, order,
+                                               i, j, 0.0, out, lse, ws)
+            return
+        outs = torch.empty((2,) + tuple(out.shape), dtype=out.dtype, device=out.device)
+        lses = torch.empty((2,) + tuple(lse.shape), dtype=lse.dtype, device=lse.device)
+        outs[0].copy_(out)
+        lses[0].copy_(lse)
+        _lib.sp_ring_block_step(q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, 0.0,
+                                outs[1], lses[1], ws)
+        _lib.sp_attn_merge_partials(outs, lses, out, lse)
+
     def ring_step_backward(self, q_blk, k_blk, v_blk, out_blk, dout_blk, lse_blk, position_ids,
                            S, P, order, i, j, dq_acc, dk_acc, dv_acc):
         B, _, Hq, _ = q_blk.shape
@@ -131,8 +149,9 @@ def ring_attention(q_blk, k_blk, v_blk, position_ids, order="contiguous", group=
 
     Step s: the partial of query block i against the key/value block held,
     j = (i - s) mod P, is folded into the running result by the log-sum-exp
-    merge; meanwhile the held block goes to rank i + 1 and the next one
-    arrives from rank i - 1 into the second of two buffers.
+    merge (step 0 writes it, the later steps accumulate into it); meanwhile
+    the held block goes to rank i + 1 and the next one arrives from rank
+    i - 1 into the second of two buffers.
     """
     kn = _kernels(kernels)
     P, i = _world(group)
@@ -140,13 +159,8 @@ def ring_attention(q_blk, k_blk, v_blk, position_ids, order="contiguous", group=
     S = Lb * P
     nxt_rank, prv_rank = _peer(group, (i + 1) % P), _peer(group, (i - 1) % P)
     kv = [(k_blk, v_blk), (torch.empty_like(k_blk), torch.empty_like(v_blk))]
-    # two stacks [2][...]: slot 0 the running result, slot 1 the new partial;
-    # the merge of one stack writes slot 0 of the other
-    outs = [torch.empty((2, B, Lb, Hq, d), dtype=q_blk.dtype, device=q_blk.device)
-            for _ in range(2)]
-    lses = [torch.empty((2, B, Hq, Lb), dtype=_lse_dtype(q_blk), device=q_blk.device)
-            for _ in range(2)]
-    cur = 0
+    out = torch.empty((B, Lb, Hq, d), dtype=q_blk.dtype, device=q_blk.device)
+    lse = torch.empty((B, Hq, Lb), dtype=_lse_dtype(q_blk), device=q_blk.device)
     for s in range(P):
         j = (i - s) % P
         reqs = []
@@ -159,15 +173,13 @@ def ring_attention(q_blk, k_blk, v_blk, position_ids, order="contiguous", group=
                 dist.P2POp(dist.irecv, nk, prv_rank, group),
                 dist.P2POp(dist.irecv, nv, prv_rank, group)])
         hk, hv = kv[s % 2]
-        slot = 0 if s == 0 else 1
-        kn.ring_step(q_blk, hk, hv, position_ids, S, P, order, i, j, outs[cur][slot],
-                     lses[cur][slot])
-        if s > 0:
-            kn.merge(outs[cur], lses[cur], outs[1 - cur][0], lses[1 - cur][0])
-            cur = 1 - cur
+        if s == 0:
+            kn.ring_step(q_blk, hk, hv, position_ids, S, P, order, i, j, out, lse)
+        else:
+            kn.ring_step_accumulate(q_blk, hk, hv, position_ids, S, P, order, i, j, out, lse)
         for r in reqs:
             r.wait()
-    return outs[cur][0], lses[cur][0]
+    return out, lse
 
 
 def ring_attention_backward(q_blk, k_blk, v_blk, out_blk, dout_blk, lse_blk, position_ids,

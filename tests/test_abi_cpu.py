@@ -176,6 +176,24 @@ def test_per_device_entry_points_reject_bad_arguments(lib):
     assert lib.sp_last_launch_count() == 0
 
 
+def test_accumulating_step_arguments(lib):
+    """sp_ring_block_step_accumulate: the per-device checks, plus a required
+    running lse and bf16 only; a contiguous causal pair with j > i adds
+    nothing and returns SP_OK without a launch (checked here on pointers the
+    call must not touch)."""
+    f32 = ctypes.c_float
+    acc = lambda i, j, dtype=0, lse=FAKE, pos=None, order=0, P=4: \
+        lib.sp_ring_block_step_accumulate(
+            FAKE, FAKE, FAKE, pos, 1, 1024, 2, 1, 128, P, order, i, j, f32(0.0), dtype, FAKE, lse,
+            FAKE_WS, ctypes.c_size_t(1 << 20), None)
+    for i, j in ((4, 0), (0, 4), (-1, 0), (0, -1)):
+        assert acc(i, j) == SP_ERR_INVALID_ARG
+    assert acc(1, 0, lse=None) == SP_ERR_INVALID_ARG
+    assert acc(1, 0, dtype=1) == SP_ERR_UNSUPPORTED
+    assert acc(0, 1, pos=FAKE) == SP_OK
+    assert lib.sp_last_launch_count() == 0
+
+
 def test_permutation_threshold_setting_round_trips(lib):
     lib.sp_permute_set_bulk_min_bytes.restype = ctypes.c_size_t
     lib.sp_permute_set_bulk_min_bytes.argtypes = [ctypes.c_size_t]

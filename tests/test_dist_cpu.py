@@ -64,6 +64,25 @@ class OracleKernels:
         out.copy_(torch.from_numpy(o[:, ti]))
         lse.copy_(torch.from_numpy(l_[:, :, ti]))
 
+    def ring_step_accumulate(self, q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, out,
+                             lse):
+        """Checks that the running result handed in is the merge of the steps
+        device i has taken so far (j' = i, i - 1, ..., j + 1), then folds in
+        pair (i, j)'s partial."""
+        ti = oracle.block_tokens(S, P, i, order)
+        step = (i - j) % P
+        parts = [oracle.ring_partial(self.q, self.k, self.v, P, s_, order, self.pos)
+                 for s_ in range(step)]
+        ro, rl = oracle.merge_partials(np.stack([p_[0][:, ti] for p_ in parts]),
+                                       np.stack([p_[1][:, :, ti] for p_ in parts]))
+        assert np.abs(out.numpy() - ro).max() < 1e-12, "running result out of step"
+        fin = np.isfinite(rl)
+        assert np.array_equal(np.isfinite(lse.numpy()), fin)
+        assert np.abs(lse.numpy()[fin] - rl[fin]).max() < 1e-12
+        part_o, part_l = torch.empty_like(out), torch.empty_like(lse)
+        self.ring_step(q_blk, k_blk, v_blk, position_ids, S, P, order, i, j, part_o, part_l)
+        self.merge(torch.stack([out, part_o]), torch.stack([lse, part_l]), out, lse)
+
     def _pair_parts(self, S, P, order, i, j):
         ti, tj = oracle.block_tokens(S, P, i, order), oracle.block_tokens(S, P, j, order)
         return oracle.ring_partial_backward(

@@ -79,6 +79,98 @@ def test_ring_block_step_every_pair(sp, case):
                         dtype, f"{case} merged device {i}")
 
 
+@pytest.mark.parametrize("case", [c for c in CASES if c[0] == "bf16"])
+def test_ring_block_step_accumulate_every_device(sp, case):
+    """Each device i folds its P steps, in ring order, into one running
+    result with sp_ring_block_step_accumulate, starting from lse = -inf and
+    an output of NaNs (which must not be read).  After every step the running
+    result equals the oracle's merge of the partials so far, and after the
+    last one block i's rows of full attention; contiguous causal pairs with
+    j > i launch nothing and leave the result bit for bit."""
+    from sequence_parallelism_gb300 import _lib
+    dtype, B, S, Hq, Hkv, d, P, order, pos_kind = case
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 4300 + S, dtype)
+    pos = _positions(pos_kind, B, S, 79)
+    tpos = None if pos is None else torch.from_numpy(pos).cuda()
+    qn, kn, vn = np32(q), np32(k), np32(v)
+    ws = sp.attention_workspace(B, S, pos is not None)
+    blocks = [oracle.block_tokens(S, P, p, order) for p in range(P)]
+    parts = [oracle.ring_partial(qn, kn, vn, P, s, order, pos) for s in range(P)]
+    full_o, full_l = oracle.full_attention(qn, kn, vn, pos)
+    for i in range(P):
+        tok = blocks[i]
+        out = torch.full((B, S // P, Hq, d), float("nan"), dtype=q.dtype, device="cuda")
+        lse = torch.full((B, Hq, S // P), float("-inf"), dtype=torch.float32, device="cuda")
+        for s in range(P):
+            j = (i - s) % P
+            before = (out.clone(), lse.clone())
+            sp.ring_block_step_accumulate(_block(q, tok), _block(k, blocks[j]),
+                                          _block(v, blocks[j]), P, i, j, out, lse, order, tpos,
+                                          workspace=ws)
+            torch.cuda.synchronize()
+            if pos is not None and order == "contiguous" and j > i:
+                assert _lib.sp_last_launch_count() == 0
+                assert torch.equal(out.view(torch.int16), before[0].view(torch.int16))
+                assert torch.equal(lse, before[1])
+            ro, rl = oracle.merge_partials(np.stack([p_[0][:, tok] for p_ in parts[:s + 1]]),
+                                           np.stack([p_[1][:, :, tok] for p_ in parts[:s + 1]]))
+            fin = np.isfinite(rl)
+            got = np32(out)
+            assert not np.isnan(got[np.broadcast_to(fin.transpose(0, 2, 1)[..., None],
+                                                    got.shape)]).any()
+            check_attention(np.where(fin.transpose(0, 2, 1)[..., None], got, 0.0),
+                            lse.cpu().numpy(), np.where(fin.transpose(0, 2, 1)[..., None], ro, 0.0),
+                            rl, dtype, f"{case} device {i} after step {s}")
+        check_attention(np32(out), lse.cpu().numpy(), full_o[:, tok], full_l[:, :, tok], dtype,
+                        f"{case} device {i} accumulated")
+
+
+@pytest.mark.parametrize("case", [c for c in CASES if c[0] == "bf16"])
+def test_ring_block_step_accumulate_onto_any_running_result(sp, case):
+    """A running result that is not a ring's own (random rows, random finite
+    lse, some rows at -inf): every pair (i, j) folded onto it must equal the
+    oracle's two-way merge of it with the pair's partial, and rows with no
+    allowed key in block j keep their bits."""
+    dtype, B, S, Hq, Hkv, d, P, order, pos_kind = case
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 4400 + S, dtype)
+    pos = _positions(pos_kind, B, S, 80)
+    tpos = None if pos is None else torch.from_numpy(pos).cuda()
+    qn, kn, vn = np32(q), np32(k), np32(v)
+    ws = sp.attention_workspace(B, S, pos is not None)
+    blocks = [oracle.block_tokens(S, P, p, order) for p in range(P)]
+    g = torch.Generator(device="cuda").manual_seed(4401 + S)
+    Lb = S // P
+    for s in range(P):
+        part_o, part_l = oracle.ring_partial(qn, kn, vn, P, s, order, pos)
+        for i in range(P):
+            j = (i - s) % P
+            tok = blocks[i]
+            # |x| < 3: half a bf16 ulp stays below the output bar
+            run_o = (torch.randn((B, Lb, Hq, d), generator=g, device="cuda") * 0.5).to(q.dtype)
+            run_l = torch.randn((B, Hq, Lb), generator=g, device="cuda") * 4
+            run_l[:, :, ::7] = float("-inf")
+            run_o[:, ::7] = float("nan")   # not read: those rows' lse is -inf
+            out, lse = run_o.clone(), run_l.clone()
+            sp.ring_block_step_accumulate(_block(q, tok), _block(k, blocks[j]),
+                                          _block(v, blocks[j]), P, i, j, out, lse, order, tpos,
+                                          workspace=ws)
+            torch.cuda.synchronize()
+            rl_in = run_l.cpu().numpy()
+            ro_in = np.where(np.isfinite(rl_in).transpose(0, 2, 1)[..., None],
+                             np32(run_o), 0.0)
+            ro, rl = oracle.merge_partials(np.stack([ro_in, part_o[:, tok]]),
+                                           np.stack([rl_in, part_l[:, :, tok]]))
+            fin = np.isfinite(rl)
+            mask = fin.transpose(0, 2, 1)[..., None]
+            check_attention(np.where(mask, np32(out), 0.0), lse.cpu().numpy(),
+                            np.where(mask, ro, 0.0), rl, dtype, f"{case} i={i} j={j}")
+            # rows with no key in block j: untouched, bit for bit
+            keep = torch.from_numpy(~np.isfinite(part_l[:, :, tok])).cuda()  # [B][Hq][Lb]
+            keep_rows = keep.transpose(1, 2)  # [B][Lb][Hq]
+            assert torch.equal(lse[keep], run_l[keep])
+            assert torch.equal(out.view(torch.int16)[keep_rows], run_o.view(torch.int16)[keep_rows])
+
+
 @pytest.mark.parametrize("case", CASES)
 def test_query_block_against_whole_sequence(sp, case):
     from sequence_parallelism_gb300 import _lib
