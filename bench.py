@@ -768,14 +768,14 @@ def backward_measurement(peaks, flush, stream, name="llama8b_32k", order="contig
     return res
 
 
-def ring_forward_measurement(peaks, flush, stream, reps=10):
+def ring_forward_measurement(peaks, flush, stream, reps=10, compare=True):
     """The forward of an 8-device ring simulated on one GPU (llama8b_32k,
     contiguous blocks), as dist.ring_attention runs it on each device: step 0
     by sp_ring_block_step, steps 1..P-1 folded into the running result by
     sp_ring_block_step_accumulate (P^2 = 64 calls per rep).  Also timed: the
     same ring with every step written by sp_ring_block_step and folded by
-    sp_attn_merge_partials (56 merges).  FLOPs: the attention's algorithmic
-    count."""
+    sp_attn_merge_partials (56 merges), unless compare is False.  FLOPs: the
+    attention's algorithmic count."""
     import torch
 
     import sequence_parallelism_gb300 as sp
@@ -823,20 +823,23 @@ def ring_forward_measurement(peaks, flush, stream, reps=10):
                     cur = 1 - cur
 
     t, _, clocks = _timed(ring_accumulate, flush, stream, reps)
-    t2, _, clocks2 = _timed(ring_merge, flush, stream, reps)
+    fl = attention_flops(cfg, pos_np)
+    tf = fl / (t * 1e-3) / 1e12
+    res = {"ms": round(t, 4), "TFLOP/s": round(tf, 1),
+           "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
+           "calls_per_rep": P * P, "reps": reps, "clocks": clocks,
+           "note": "8 simulated devices x 8 ring steps; causal contiguous pairs with j > i add "
+                   "nothing (the accumulating call returns without a launch); median of reps"}
+    if compare:
+        t2, _, clocks2 = _timed(ring_merge, flush, stream, reps)
+        tf2 = fl / (t2 * 1e-3) / 1e12
+        res["step_and_merge"] = {"ms": round(t2, 4), "TFLOP/s": round(tf2, 1),
+                                 "frac_of_bf16_peak": round(tf2 / peaks["bf16_tflops"], 4),
+                                 "merges_per_rep": P * (P - 1), "clocks": clocks2}
     st_, code = _lib.sp_get_device_error(ws)
     if st_ != 0:
         raise RuntimeError(f"device error word {code:#x} in the ring forward")
-    fl = attention_flops(cfg, pos_np)
-    tf, tf2 = fl / (t * 1e-3) / 1e12, fl / (t2 * 1e-3) / 1e12
-    return {"ms": round(t, 4), "TFLOP/s": round(tf, 1),
-            "frac_of_bf16_peak": round(tf / peaks["bf16_tflops"], 4),
-            "calls_per_rep": P * P, "reps": reps, "clocks": clocks,
-            "step_and_merge": {"ms": round(t2, 4), "TFLOP/s": round(tf2, 1),
-                               "frac_of_bf16_peak": round(tf2 / peaks["bf16_tflops"], 4),
-                               "merges_per_rep": P * (P - 1), "clocks": clocks2},
-            "note": "8 simulated devices x 8 ring steps; causal contiguous pairs with j > i add "
-                    "nothing (the accumulating call returns without a launch); median of reps"}
+    return res
 
 
 def ring_backward_measurement(peaks, flush, stream, reps=5):

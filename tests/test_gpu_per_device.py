@@ -171,6 +171,37 @@ def test_ring_block_step_accumulate_onto_any_running_result(sp, case):
             assert torch.equal(out.view(torch.int16)[keep_rows], run_o.view(torch.int16)[keep_rows])
 
 
+@pytest.mark.parametrize("case", [CASES[1], CASES[4], CASES[5]])
+def test_library_kernels_accumulate_both_paths(sp, case):
+    """dist.LibraryKernels.ring_step_accumulate, as dist.ring_attention calls
+    it: one accumulating call for bf16 with d = 128, else the step into a
+    temporary and the merge.  Device i's ring folded step by step equals
+    block i's rows of full attention."""
+    from sequence_parallelism_gb300 import dist as spd
+    dtype, B, S, Hq, Hkv, d, P, order, pos_kind = case
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 4600 + S, dtype)
+    pos = _positions(pos_kind, B, S, 82)
+    tpos = None if pos is None else torch.from_numpy(pos).cuda()
+    full_o, full_l = oracle.full_attention(np32(q), np32(k), np32(v), pos)
+    kern = spd.LibraryKernels()
+    blocks = [oracle.block_tokens(S, P, p, order) for p in range(P)]
+    for i in range(P):
+        tok = blocks[i]
+        out = torch.empty((B, S // P, Hq, d), dtype=q.dtype, device="cuda")
+        lse = torch.empty((B, Hq, S // P), dtype=torch.float32, device="cuda")
+        for s in range(P):
+            j = (i - s) % P
+            args = (_block(q, tok), _block(k, blocks[j]), _block(v, blocks[j]), tpos, S, P,
+                    order, i, j, out, lse)
+            if s == 0:
+                kern.ring_step(*args)
+            else:
+                kern.ring_step_accumulate(*args)
+        torch.cuda.synchronize()
+        check_attention(np32(out), lse.cpu().numpy(), full_o[:, tok], full_l[:, :, tok], dtype,
+                        f"{case} device {i}")
+
+
 @pytest.mark.parametrize("case", CASES)
 def test_query_block_against_whole_sequence(sp, case):
     from sequence_parallelism_gb300 import _lib
