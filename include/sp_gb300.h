@@ -410,7 +410,9 @@ sp_status sp_blockwise_attn_bwd(const void* q, const void* k, const void* v, con
  * SP_ERR_UNSUPPORTED; tensor pointers 16-byte aligned.  workspace:
  * sp_ring_block_step_bwd_workspace_bytes(B, S, Hq, P, position_ids != NULL)
  * bytes, 256-byte aligned.  Errors as for sp_blockwise_attn_bwd, and
- * SP_ERR_INVALID_ARG for i or j outside [0, P).
+ * SP_ERR_INVALID_ARG for i or j outside [0, P).  Contiguous blocks under the
+ * causal mask with j > i have no allowed pair: the call returns SP_OK
+ * without a launch and the accumulators keep their values.
  * ------------------------------------------------------------------------ */
 size_t sp_ring_block_step_bwd_workspace_bytes(int B, int S, int Hq, int P, int causal);
 sp_status sp_ring_block_step_bwd(const void* q_blk, const void* k_blk, const void* v_blk,

@@ -211,6 +211,9 @@ extern "C" sp_status sp_ring_block_step_bwd(const void* q_blk, const void* k_blk
   const sp::BlockBwdLayout L = sp::block_bwd_layout(B, S, Hq, P, causal);
   if (!workspace || !sp::aligned(workspace, 256) || workspace_bytes < L.total)
     return SP_ERR_WORKSPACE;
+  // contiguous blocks under the causal mask: no query of block i may attend a
+  // key of block j > i, so the pair's gradient parts are zero
+  if (causal && order == SP_ORDER_CONTIGUOUS && j > i) return SP_OK;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint8_t* p0 = ws + sp::kWsHeaderBytes;

@@ -194,6 +194,19 @@ def test_accumulating_step_arguments(lib):
     assert lib.sp_last_launch_count() == 0
 
 
+def test_ring_step_backward_skips_pairs_without_allowed_keys(lib):
+    """sp_ring_block_step_bwd: a contiguous causal pair with j > i returns
+    SP_OK without a launch and without touching the (fake) tensors; block
+    indices are still validated first."""
+    f32 = ctypes.c_float
+    bwd = lambda i, j, pos, order=0: lib.sp_ring_block_step_bwd(
+        FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, pos, 1, 1024, 2, 1, 128, 4, order, i, j, f32(0.0), 0,
+        FAKE, FAKE, FAKE, FAKE_WS, ctypes.c_size_t(1 << 30), None)
+    assert bwd(0, 1, FAKE) == SP_OK and bwd(2, 3, FAKE) == SP_OK
+    assert lib.sp_last_launch_count() == 0
+    assert bwd(0, 4, FAKE) == SP_ERR_INVALID_ARG
+
+
 def test_permutation_threshold_setting_round_trips(lib):
     lib.sp_permute_set_bulk_min_bytes.restype = ctypes.c_size_t
     lib.sp_permute_set_bulk_min_bytes.argtypes = [ctypes.c_size_t]

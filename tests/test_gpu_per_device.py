@@ -258,6 +258,8 @@ def test_ring_block_step_backward_every_pair(sp, case):
                     _block(out, blocks[i]), _block(dout, blocks[i]), tl(lse, i))
             _lib.sp_ring_block_step_bwd(*args, tpos, S, P, order, i, j, 0.0, *acc, ws)
             torch.cuda.synchronize()
+            if pos is not None and order == "contiguous" and j > i:
+                assert _lib.sp_last_launch_count() == 0   # nothing allowed: no launch
             ref = oracle.ring_partial_backward(*(np32(a) for a in args[:5]),
                                                args[5].cpu().numpy(), S, P, i, j, order, pos)
             for name, got, r in zip(("dq", "dk", "dv"), acc, ref):
