@@ -97,6 +97,36 @@ def test_ring_step_writes_stay_inside(sp, order):
                         f"ring step {step} {order}")
 
 
+@pytest.mark.parametrize("order", ["contiguous", "striped"])
+def test_accumulating_ring_step_writes_stay_inside(sp, order):
+    """Each device's ring on 200-row blocks (one 256-row unit whose last 56
+    rows lie past the block: the running output's TMA load reads them as
+    zeros, the store drops them): step 0 writes the guarded running result,
+    steps 1..P-1 fold into it; nothing lands outside out, lse or the
+    workspace, and the result is block i's rows of full attention."""
+    B, S, Hq, Hkv, d, P = 2, 600, 2, 1, 128, 3
+    q, k, v = workloads.small_case(B, S, Hq, Hkv, d, 720, "bf16")
+    pos = _positions("packed", B, S, 720)
+    tpos = torch.from_numpy(pos).cuda()
+    full_o, full_l = oracle.full_attention(np32(q), np32(k), np32(v), pos)
+    blocks = [oracle.block_tokens(S, P, p_, order) for p_ in range(P)]
+    blk = lambda t, p_: t[:, torch.from_numpy(blocks[p_]).cuda()].contiguous()
+    for i in range(P):
+        out = Guarded((B, S // P, Hq, d), q.dtype)
+        lse = Guarded((B, Hq, S // P), torch.float32)
+        ws = _workspace(_lib.sp_blockwise_attn_workspace_bytes(B, S, True))
+        for s_ in range(P):
+            j = (i - s_) % P
+            call = _lib.sp_ring_block_step if s_ == 0 else _lib.sp_ring_block_step_accumulate
+            call(blk(q, i), blk(k, j), blk(v, j), tpos, S, P, order, i, j, 0.0, out.t, lse.t,
+                 ws.t)
+        what = f"accumulating ring {order} device {i}"
+        _assert_guarded(what, ("out", out), ("lse", lse), ("workspace", ws))
+        _no_nan(what, out=out.t)
+        check_attention(np32(out.t), lse.t.cpu().numpy(), full_o[:, blocks[i]],
+                        full_l[:, :, blocks[i]], "bf16", what)
+
+
 @pytest.fixture(params=["tma_staged", "default"])
 def path(request):
     """Every permutation that meets the bulk-copy rules on the TMA-staged
